@@ -1,1 +1,235 @@
-"""GB300 TN GEMM library (placeholder until the binding lands)."""
+"""GB300 (sm_103a) TN GEMM: C = A @ B.T with fp16/bf16 (fp32 accumulate) and int8->int32.
+
+A thin ctypes binding over the C ABI of ``libgemm_gb300.so`` (declared in
+``include/gemm.h``), with the same function names.  It only marshals
+arguments: every step of the GEMM runs in the library's CUDA kernels.  If the
+library is missing or cannot load, every call raises; nothing here computes a
+result on the CPU or through another library.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+from ._build import LIB_PATH, build_library
+
+__all__ = [
+    "GEMM_F16", "GEMM_BF16", "GEMM_I8_I32", "GEMM_LAYOUT_TN", "GemmError", "Plan",
+    "build_library", "gemm_plan_create", "gemm_plan_create_with_config", "gemm_run",
+    "gemm_plan_check", "gemm_plan_destroy", "gemm_plan_get_config", "gemm_plan_set_timeout",
+    "gemm_select_config", "gemm_tile_coords", "gemm_workspace_bytes", "gemm_status_string",
+    "gemm_abi_version", "library", "DTYPES",
+]
+
+GEMM_F16, GEMM_BF16, GEMM_I8_I32 = 0, 1, 2
+GEMM_LAYOUT_TN = 0
+DTYPES = {"f16": GEMM_F16, "bf16": GEMM_BF16, "i8": GEMM_I8_I32}
+
+STATUS_NAMES = {
+    0: "GEMM_OK", 1: "GEMM_ERR_INVALID_ARG", 2: "GEMM_ERR_UNSUPPORTED", 3: "GEMM_ERR_ALIGNMENT",
+    4: "GEMM_ERR_NO_DEVICE", 5: "GEMM_ERR_ARCH", 6: "GEMM_ERR_OOM", 7: "GEMM_ERR_TENSORMAP",
+    8: "GEMM_ERR_LAUNCH", 9: "GEMM_ERR_DEVICE_TIMEOUT", 10: "GEMM_ERR_CUDA",
+}
+
+
+class GemmError(RuntimeError):
+    def __init__(self, status: int, what: str = ""):
+        self.status = status
+        self.name = STATUS_NAMES.get(status, str(status))
+        super().__init__("%s%s" % (what + ": " if what else "", gemm_status_string(status)))
+
+
+class gemm_config_t(ctypes.Structure):
+    _fields_ = [("block_n", ctypes.c_int32), ("stages", ctypes.c_int32),
+                ("split_k", ctypes.c_int32), ("raster_group", ctypes.c_int32),
+                ("max_ctas", ctypes.c_int32)]
+
+    def as_dict(self):
+        return {f: int(getattr(self, f)) for f, _ in self._fields_}
+
+
+_lock = threading.Lock()
+_lib = None
+
+
+def library() -> ctypes.CDLL:
+    """The loaded C-ABI library (raises if it has not been built)."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(LIB_PATH):
+                raise RuntimeError("libgemm_gb300.so is not built (run "
+                                   "dense_gemm_hgemm_gb300.build_library())")
+            lib = ctypes.CDLL(LIB_PATH)
+            i64, i32, vp = ctypes.c_int64, ctypes.c_int32, ctypes.c_void_p
+            cfgp = ctypes.POINTER(gemm_config_t)
+            sig = {
+                "gemm_plan_create": ([i64, i64, i64, i32, i32, ctypes.POINTER(vp)], i32),
+                "gemm_plan_create_with_config": ([i64, i64, i64, i32, i32, cfgp,
+                                                  ctypes.POINTER(vp)], i32),
+                "gemm_run": ([vp, vp, vp, vp, vp], i32),
+                "gemm_plan_check": ([vp, vp], i32),
+                "gemm_plan_destroy": ([vp], i32),
+                "gemm_plan_get_config": ([vp, cfgp], i32),
+                "gemm_plan_set_timeout": ([vp, ctypes.c_uint64], i32),
+                "gemm_select_config": ([i64, i64, i64, i32, i32, cfgp], i32),
+                "gemm_tile_coords": ([i64, i64, i32, i64, ctypes.POINTER(i64),
+                                      ctypes.POINTER(i64)], i32),
+                "gemm_workspace_bytes": ([i64, i64, i64, i32, cfgp, ctypes.POINTER(ctypes.c_size_t)], i32),
+                "gemm_status_string": ([i32], ctypes.c_char_p),
+                "gemm_abi_version": ([], i32),
+            }
+            for name, (args, res) in sig.items():
+                fn = getattr(lib, name)
+                fn.argtypes = args
+                fn.restype = res
+            _lib = lib
+    return _lib
+
+
+def _check(status: int, what: str):
+    if status != 0:
+        raise GemmError(status, what)
+
+
+def _dtype_code(dtype) -> int:
+    return DTYPES[dtype] if isinstance(dtype, str) else int(dtype)
+
+
+def _ptr(x) -> int | None:
+    """Device address of a torch tensor (or an int address)."""
+    if x is None:
+        return None
+    if isinstance(x, int):
+        return x
+    return x.data_ptr()
+
+
+def _stream(stream) -> int | None:
+    if stream is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def _config(cfg) -> gemm_config_t:
+    if isinstance(cfg, gemm_config_t):
+        return cfg
+    c = gemm_config_t()
+    c.block_n = int(cfg.get("block_n", 128))
+    c.stages = int(cfg.get("stages", 0))
+    c.split_k = int(cfg.get("split_k", 1))
+    c.raster_group = int(cfg.get("raster_group", 16))
+    c.max_ctas = int(cfg.get("max_ctas", 0))
+    return c
+
+
+def gemm_status_string(status: int) -> str:
+    return library().gemm_status_string(int(status)).decode()
+
+
+def gemm_abi_version() -> int:
+    return int(library().gemm_abi_version())
+
+
+def gemm_plan_create(M: int, N: int, K: int, dtype="f16", layout: int = GEMM_LAYOUT_TN) -> int:
+    h = ctypes.c_void_p()
+    _check(library().gemm_plan_create(M, N, K, _dtype_code(dtype), layout, ctypes.byref(h)),
+           "gemm_plan_create")
+    return h.value
+
+
+def gemm_plan_create_with_config(M, N, K, dtype, config, layout: int = GEMM_LAYOUT_TN) -> int:
+    h = ctypes.c_void_p()
+    c = _config(config)
+    _check(library().gemm_plan_create_with_config(M, N, K, _dtype_code(dtype), layout,
+                                                  ctypes.byref(c), ctypes.byref(h)),
+           "gemm_plan_create_with_config")
+    return h.value
+
+
+def gemm_run(plan: int, A, B, C, stream=None) -> None:
+    _check(library().gemm_run(plan, _ptr(A), _ptr(B), _ptr(C), _stream(stream)), "gemm_run")
+
+
+def gemm_plan_check(plan: int, stream=None) -> None:
+    _check(library().gemm_plan_check(plan, _stream(stream)), "gemm_plan_check")
+
+
+def gemm_plan_destroy(plan: int) -> None:
+    _check(library().gemm_plan_destroy(plan), "gemm_plan_destroy")
+
+
+def gemm_plan_get_config(plan: int) -> dict:
+    c = gemm_config_t()
+    _check(library().gemm_plan_get_config(plan, ctypes.byref(c)), "gemm_plan_get_config")
+    return c.as_dict()
+
+
+def gemm_plan_set_timeout(plan: int, ns: int) -> None:
+    _check(library().gemm_plan_set_timeout(plan, int(ns)), "gemm_plan_set_timeout")
+
+
+def gemm_select_config(M, N, K, dtype, num_sms: int) -> dict:
+    c = gemm_config_t()
+    _check(library().gemm_select_config(M, N, K, _dtype_code(dtype), num_sms, ctypes.byref(c)),
+           "gemm_select_config")
+    return c.as_dict()
+
+
+def gemm_tile_coords(m_blocks: int, n_blocks: int, raster_group: int, tile: int):
+    m = ctypes.c_int64()
+    n = ctypes.c_int64()
+    _check(library().gemm_tile_coords(m_blocks, n_blocks, raster_group, tile, ctypes.byref(m),
+                                      ctypes.byref(n)), "gemm_tile_coords")
+    return m.value, n.value
+
+
+def gemm_workspace_bytes(M, N, K, dtype, config) -> int:
+    b = ctypes.c_size_t()
+    c = _config(config)
+    _check(library().gemm_workspace_bytes(M, N, K, _dtype_code(dtype), ctypes.byref(c),
+                                          ctypes.byref(b)), "gemm_workspace_bytes")
+    return int(b.value)
+
+
+class Plan:
+    """Owning wrapper of a plan handle: ``with Plan(M, N, K, "f16") as p: p.run(A, B, C)``."""
+
+    def __init__(self, M: int, N: int, K: int, dtype="f16", config=None):
+        self.M, self.N, self.K, self.dtype = M, N, K, dtype
+        self.handle = (gemm_plan_create(M, N, K, dtype) if config is None
+                       else gemm_plan_create_with_config(M, N, K, dtype, config))
+
+    @property
+    def config(self) -> dict:
+        return gemm_plan_get_config(self.handle)
+
+    def run(self, A, B, C, stream=None) -> None:
+        gemm_run(self.handle, A, B, C, stream)
+
+    def check(self, stream=None) -> None:
+        gemm_plan_check(self.handle, stream)
+
+    def set_timeout(self, ns: int) -> None:
+        gemm_plan_set_timeout(self.handle, ns)
+
+    def close(self) -> None:
+        if self.handle:
+            gemm_plan_destroy(self.handle)
+            self.handle = None
+
+    def __enter__(self):
+        return self
+
+    def __exit__(self, *exc):
+        self.close()
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass

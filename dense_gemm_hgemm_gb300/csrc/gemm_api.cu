@@ -1,0 +1,478 @@
+// gemm_api.cu -- the C ABI declared in include/gemm.h.
+//
+// Host-side work only: argument and alignment validation, configuration choice,
+// plan memory, tensor-map encoding (cuTensorMapEncodeTiled obtained through
+// cudaGetDriverEntryPointByVersion, so the library needs no -lcuda), and the
+// launches.  Every GEMM step runs in the kernels of gemm_inst_*.cu and
+// gemm_aux.cu; there is no host or library fallback.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+#include <string.h>
+
+#include <mutex>
+#include <new>
+
+#include "gemm.h"
+#include "gemm_config.h"
+#include "gemm_launch.h"
+#include "gemm_sched.h"
+
+namespace {
+
+constexpr uint64_t kDefaultTimeoutNs = 2000000000ull;
+constexpr size_t kAlign = 256;
+
+size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+struct PlanMemory {
+    size_t error_off, counters_off, ws_off, a16_off, b16_off, total;
+};
+
+}  // namespace
+
+struct gemm_plan {
+    int64_t M, N, K;
+    gemm_dtype_t dtype;
+    gemm_config_t cfg;          // effective configuration
+    int device;
+    int num_sms;
+    int out_kind;
+    gbg::LaunchShape shape;
+    gbg::KParams kp;
+    PlanMemory mem;
+    uint8_t* dmem;              // one device allocation holding everything below
+    int32_t* d_error;
+    uint32_t* d_counters;
+    void* d_ws;
+    void* d_a16;
+    void* d_b16;
+    const void* map_a_src;      // tensor-map cache keys
+    const void* map_b_src;
+    bool map_a_valid, map_b_valid;
+    CUtensorMap map_a, map_b;
+};
+
+namespace {
+
+gemm_status_t validate_shape(int64_t M, int64_t N, int64_t K, gemm_dtype_t dtype,
+                             gemm_layout_t layout) {
+    if (dtype != GEMM_F16 && dtype != GEMM_BF16 && dtype != GEMM_I8_I32) return GEMM_ERR_UNSUPPORTED;
+    if (layout != GEMM_LAYOUT_TN) return GEMM_ERR_UNSUPPORTED;
+    if (M < 0 || N < 0 || K < 0) return GEMM_ERR_INVALID_ARG;
+    if (M > INT32_MAX || N > INT32_MAX || K > INT32_MAX) return GEMM_ERR_INVALID_ARG;
+    const bool i8 = dtype == GEMM_I8_I32;
+    // Row strides must be multiples of 16 bytes: K * in_bytes for A and B,
+    // N * out_bytes for C.
+    if (K % (i8 ? 16 : 8) != 0) return GEMM_ERR_ALIGNMENT;
+    if (N % (i8 ? 4 : 8) != 0) return GEMM_ERR_ALIGNMENT;
+    // Work-decomposition indices are 32-bit.
+    const int64_t tiles = ((M + gbg::kBM - 1) / gbg::kBM) * ((N + 63) / 64);
+    if (tiles > (int64_t{1} << 30)) return GEMM_ERR_INVALID_ARG;
+    return GEMM_OK;
+}
+
+bool valid_block_n(int bn, gemm_dtype_t dtype) {
+    if (dtype == GEMM_I8_I32) return bn == 64 || bn == 128;
+    return bn == 64 || bn == 128 || bn == 256;
+}
+
+// Fill the derived fields of a configuration for a shape (split-K made exact:
+// every K slice non-empty).  Returns GEMM_ERR_INVALID_ARG for a bad config.
+gemm_status_t normalise_config(int64_t M, int64_t N, int64_t K, gemm_dtype_t dtype,
+                               const gemm_config_t& in, gemm_config_t* out,
+                               int32_t* kb_per_split) {
+    gemm_config_t c = in;
+    if (!valid_block_n(c.block_n, dtype)) return GEMM_ERR_INVALID_ARG;
+    if (c.stages == 0) c.stages = gbg::default_stages(c.block_n);
+    if (c.stages != gbg::default_stages(c.block_n)) return GEMM_ERR_INVALID_ARG;
+    if (c.split_k < 1 || c.raster_group < 1 || c.max_ctas < 0) return GEMM_ERR_INVALID_ARG;
+    const int64_t num_kb = (K + gbg::kBK - 1) / gbg::kBK;
+    int64_t s = c.split_k;
+    if (num_kb == 0) s = 1;
+    if (s > num_kb && num_kb > 0) s = num_kb;
+    const int64_t per = num_kb > 0 ? (num_kb + s - 1) / s : 0;
+    if (per > 0) s = (num_kb + per - 1) / per;
+    const int64_t m_blocks = (M + gbg::kBM - 1) / gbg::kBM;
+    const int64_t n_blocks = (N + c.block_n - 1) / c.block_n;
+    if (m_blocks * n_blocks * s > INT32_MAX) return GEMM_ERR_INVALID_ARG;
+    c.split_k = static_cast<int32_t>(s);
+    if (c.raster_group > m_blocks && m_blocks > 0) c.raster_group = static_cast<int32_t>(m_blocks);
+    *out = c;
+    *kb_per_split = static_cast<int32_t>(per);
+    return GEMM_OK;
+}
+
+PlanMemory plan_memory(int64_t M, int64_t N, int64_t K, gemm_dtype_t dtype, const gemm_config_t& c) {
+    PlanMemory m{};
+    size_t off = 0;
+    m.error_off = off;
+    off += kAlign;
+    const int64_t tiles = ((M + gbg::kBM - 1) / gbg::kBM) * ((N + c.block_n - 1) / c.block_n);
+    m.counters_off = off;
+    if (c.split_k > 1) off += round_up(static_cast<size_t>(tiles) * 4, kAlign);
+    m.ws_off = off;
+    if (c.split_k > 1)
+        off += round_up(static_cast<size_t>(tiles) * c.split_k * gbg::kBM * c.block_n * 4, kAlign);
+    m.a16_off = off;
+    if (dtype == GEMM_I8_I32) off += round_up(static_cast<size_t>(M) * K * 2, kAlign);
+    m.b16_off = off;
+    if (dtype == GEMM_I8_I32) off += round_up(static_cast<size_t>(N) * K * 2, kAlign);
+    m.total = off;
+    return m;
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    });
+    return fn;
+}
+
+// 2-D map over a rows x K K-contiguous 16-bit matrix; box = 64 (K) x box_rows,
+// 128-byte swizzle (one 64-element row of the box = one 128-byte swizzle span),
+// zero fill outside the matrix.
+gemm_status_t encode_kmajor(CUtensorMap* map, const void* base, int64_t rows, int64_t K,
+                            int box_rows, CUtensorMapDataType dt) {
+    PFN_cuTensorMapEncodeTiled_v12000 fn = encode_fn();
+    if (!fn) return GEMM_ERR_TENSORMAP;
+    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(rows)};
+    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(K) * 2};
+    const cuuint32_t box[2] = {static_cast<cuuint32_t>(gbg::kBK), static_cast<cuuint32_t>(box_rows)};
+    const cuuint32_t estr[2] = {1, 1};
+    const CUresult r = fn(map, dt, 2, const_cast<void*>(base), dims, strides, box, estr,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? GEMM_OK : GEMM_ERR_TENSORMAP;
+}
+
+CUtensorMapDataType operand_type(gemm_dtype_t dt) {
+    return dt == GEMM_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+}
+
+gemm_status_t device_of_caller(int* device, int* num_sms) {
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess) {
+        cudaGetLastError();
+        return GEMM_ERR_NO_DEVICE;
+    }
+    int major = 0, minor = 0, sms = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+        cudaGetLastError();
+        return GEMM_ERR_NO_DEVICE;
+    }
+    if (major != 10 || minor != 3) return GEMM_ERR_ARCH;
+    *device = dev;
+    *num_sms = sms;
+    return GEMM_OK;
+}
+
+gemm_status_t create_plan(int64_t M, int64_t N, int64_t K, gemm_dtype_t dtype,
+                          gemm_layout_t layout, const gemm_config_t* user_cfg, gemm_plan_t* out) {
+    if (!out) return GEMM_ERR_INVALID_ARG;
+    *out = nullptr;
+    gemm_status_t st = validate_shape(M, N, K, dtype, layout);
+    if (st != GEMM_OK) return st;
+    if (user_cfg) {
+        gemm_config_t tmp;
+        int32_t per;
+        st = normalise_config(M, N, K, dtype, *user_cfg, &tmp, &per);
+        if (st != GEMM_OK) return st;
+    }
+    int dev = 0, sms = 0;
+    st = device_of_caller(&dev, &sms);
+    if (st != GEMM_OK) return st;
+
+    gemm_config_t want = user_cfg ? *user_cfg : gbg::select_config(M, N, K, dtype, sms);
+    gemm_config_t cfg;
+    int32_t kb_per_split = 0;
+    st = normalise_config(M, N, K, dtype, want, &cfg, &kb_per_split);
+    if (st != GEMM_OK) return st;
+
+    gemm_plan* p = new (std::nothrow) gemm_plan();
+    if (!p) return GEMM_ERR_OOM;
+    p->M = M;
+    p->N = N;
+    p->K = K;
+    p->dtype = dtype;
+    p->cfg = cfg;
+    p->device = dev;
+    p->num_sms = sms;
+    p->out_kind = dtype == GEMM_F16 ? gbg::kOutF16 : (dtype == GEMM_BF16 ? gbg::kOutBF16 : gbg::kOutI32);
+    p->mem = plan_memory(M, N, K, dtype, cfg);
+    if (cudaMalloc(reinterpret_cast<void**>(&p->dmem), p->mem.total) != cudaSuccess) {
+        cudaGetLastError();
+        delete p;
+        return GEMM_ERR_OOM;
+    }
+    if (cudaMemset(p->dmem, 0, p->mem.a16_off) != cudaSuccess) {   // error word + counters
+        cudaGetLastError();
+        cudaFree(p->dmem);
+        delete p;
+        return GEMM_ERR_CUDA;
+    }
+    p->d_error = reinterpret_cast<int32_t*>(p->dmem + p->mem.error_off);
+    p->d_counters = reinterpret_cast<uint32_t*>(p->dmem + p->mem.counters_off);
+    p->d_ws = p->dmem + p->mem.ws_off;
+    p->d_a16 = p->dmem + p->mem.a16_off;
+    p->d_b16 = p->dmem + p->mem.b16_off;
+
+    size_t smem = 0;
+    if (gbg::gemm_prepare(cfg.block_n, cfg.stages, p->out_kind, &smem) != cudaSuccess) {
+        cudaGetLastError();
+        cudaFree(p->dmem);
+        delete p;
+        return GEMM_ERR_LAUNCH;
+    }
+
+    gbg::KParams& kp = p->kp;
+    memset(&kp, 0, sizeof(kp));
+    kp.M = static_cast<int32_t>(M);
+    kp.N = static_cast<int32_t>(N);
+    kp.K = static_cast<int32_t>(K);
+    kp.num_kb = static_cast<int32_t>((K + gbg::kBK - 1) / gbg::kBK);
+    kp.m_blocks = static_cast<int32_t>((M + gbg::kBM - 1) / gbg::kBM);
+    kp.n_blocks = static_cast<int32_t>((N + cfg.block_n - 1) / cfg.block_n);
+    kp.split_k = cfg.split_k;
+    kp.kb_per_split = kb_per_split;
+    // Integer mode: chunks of 8 k-blocks (512 products of magnitude <= 2^14, so
+    // every fp32 partial sum is an integer of magnitude <= 2^23: exact).
+    kp.chunk_kb = dtype == GEMM_I8_I32 ? 8 : (kb_per_split > 0 ? kb_per_split : 1);
+    kp.raster_group = cfg.raster_group;
+    kp.num_units = kp.m_blocks * kp.n_blocks * kp.split_k;
+    const uint32_t fmt = dtype == GEMM_BF16 ? 1u : 0u;
+    kp.idesc = (1u << 4)                                         // D: fp32
+               | (fmt << 7) | (fmt << 10)                        // A, B: fp16 or bf16
+               | (static_cast<uint32_t>(cfg.block_n >> 3) << 17)  // N / 8
+               | (static_cast<uint32_t>(gbg::kBM >> 4) << 24);    // M / 16
+    kp.tx_extra = 0;
+    kp.workspace = p->d_ws;
+    kp.counters = p->d_counters;
+    kp.error_word = p->d_error;
+    kp.timeout_ns = kDefaultTimeoutNs;
+
+    const int cap = cfg.max_ctas > 0 ? cfg.max_ctas : sms;
+    p->shape.grid = kp.num_units < cap ? kp.num_units : cap;
+    if (p->shape.grid < 1) p->shape.grid = 1;
+    p->shape.block = gbg::kThreads;
+    p->shape.smem_bytes = smem;
+
+    if (dtype == GEMM_I8_I32 && M > 0 && N > 0 && K > 0) {
+        st = encode_kmajor(&p->map_a, p->d_a16, M, K, gbg::kBM, CU_TENSOR_MAP_DATA_TYPE_FLOAT16);
+        if (st == GEMM_OK)
+            st = encode_kmajor(&p->map_b, p->d_b16, N, K, cfg.block_n, CU_TENSOR_MAP_DATA_TYPE_FLOAT16);
+        if (st != GEMM_OK) {
+            cudaFree(p->dmem);
+            delete p;
+            return st;
+        }
+        p->map_a_valid = p->map_b_valid = true;
+    }
+    *out = p;
+    return GEMM_OK;
+}
+
+}  // namespace
+
+namespace gbg {
+
+cudaError_t gemm_prepare(int bn, int stages, int out, size_t* smem_bytes) {
+    switch (out) {
+        case kOutF16: return gemm_prepare_f16(bn, stages, smem_bytes);
+        case kOutBF16: return gemm_prepare_bf16(bn, stages, smem_bytes);
+        case kOutI32: return gemm_prepare_i32(bn, stages, smem_bytes);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
+cudaError_t gemm_launch(int bn, int stages, int out, const LaunchShape& shape,
+                        const CUtensorMap& a, const CUtensorMap& b, const KParams& p,
+                        cudaStream_t stream) {
+    switch (out) {
+        case kOutF16: return gemm_launch_f16(bn, stages, shape, a, b, p, stream);
+        case kOutBF16: return gemm_launch_bf16(bn, stages, shape, a, b, p, stream);
+        case kOutI32: return gemm_launch_i32(bn, stages, shape, a, b, p, stream);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
+}  // namespace gbg
+
+extern "C" {
+
+gemm_status_t gemm_plan_create(int64_t M, int64_t N, int64_t K, gemm_dtype_t dtype,
+                               gemm_layout_t layout, gemm_plan_t* plan) {
+    return create_plan(M, N, K, dtype, layout, nullptr, plan);
+}
+
+gemm_status_t gemm_plan_create_with_config(int64_t M, int64_t N, int64_t K, gemm_dtype_t dtype,
+                                           gemm_layout_t layout, const gemm_config_t* config,
+                                           gemm_plan_t* plan) {
+    if (!config) return GEMM_ERR_INVALID_ARG;
+    return create_plan(M, N, K, dtype, layout, config, plan);
+}
+
+gemm_status_t gemm_run(gemm_plan_t p, const void* A, const void* B, void* C, void* stream_ptr) {
+    if (!p) return GEMM_ERR_INVALID_ARG;
+    if (p->M == 0 || p->N == 0) return GEMM_OK;
+    if (!C || (p->K > 0 && (!A || !B))) return GEMM_ERR_INVALID_ARG;
+    if ((reinterpret_cast<uintptr_t>(A) | reinterpret_cast<uintptr_t>(B) |
+         reinterpret_cast<uintptr_t>(C)) & 15u)
+        return GEMM_ERR_ALIGNMENT;
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess) {
+        cudaGetLastError();
+        return GEMM_ERR_NO_DEVICE;
+    }
+    if (dev != p->device) return GEMM_ERR_INVALID_ARG;
+    cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_ptr);
+    const int64_t out_bytes = p->M * p->N * (p->dtype == GEMM_I8_I32 ? 4 : 2);
+
+    if (p->K == 0) {
+        if (gbg::launch_zero_fill(C, out_bytes, p->num_sms, stream) != cudaSuccess) {
+            cudaGetLastError();
+            return GEMM_ERR_LAUNCH;
+        }
+        return GEMM_OK;
+    }
+
+    if (p->dtype == GEMM_I8_I32) {
+        if (gbg::launch_widen_i8(static_cast<const int8_t*>(A), p->M * p->K,
+                                 static_cast<const int8_t*>(B), p->N * p->K, p->d_a16, p->d_b16,
+                                 p->num_sms, stream) != cudaSuccess) {
+            cudaGetLastError();
+            return GEMM_ERR_LAUNCH;
+        }
+    } else {
+        const CUtensorMapDataType dt = operand_type(p->dtype);
+        if (!p->map_a_valid || p->map_a_src != A) {
+            p->map_a_valid = false;
+            const gemm_status_t st = encode_kmajor(&p->map_a, A, p->M, p->K, gbg::kBM, dt);
+            if (st != GEMM_OK) return st;
+            p->map_a_src = A;
+            p->map_a_valid = true;
+        }
+        if (!p->map_b_valid || p->map_b_src != B) {
+            p->map_b_valid = false;
+            const gemm_status_t st = encode_kmajor(&p->map_b, B, p->N, p->K, p->cfg.block_n, dt);
+            if (st != GEMM_OK) return st;
+            p->map_b_src = B;
+            p->map_b_valid = true;
+        }
+    }
+    p->kp.C = C;
+    if (gbg::gemm_launch(p->cfg.block_n, p->cfg.stages, p->out_kind, p->shape, p->map_a, p->map_b,
+                         p->kp, stream) != cudaSuccess) {
+        cudaGetLastError();
+        return GEMM_ERR_LAUNCH;
+    }
+    return GEMM_OK;
+}
+
+gemm_status_t gemm_plan_check(gemm_plan_t p, void* stream_ptr) {
+    if (!p) return GEMM_ERR_INVALID_ARG;
+    if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream_ptr)) != cudaSuccess) {
+        cudaGetLastError();
+        return GEMM_ERR_CUDA;
+    }
+    int32_t word = 0;
+    if (cudaMemcpy(&word, p->d_error, sizeof(word), cudaMemcpyDeviceToHost) != cudaSuccess) {
+        cudaGetLastError();
+        return GEMM_ERR_CUDA;
+    }
+    if (word != 0) {
+        const int32_t zero = 0;
+        cudaMemcpy(p->d_error, &zero, sizeof(zero), cudaMemcpyHostToDevice);
+        return GEMM_ERR_DEVICE_TIMEOUT;
+    }
+    return GEMM_OK;
+}
+
+gemm_status_t gemm_plan_destroy(gemm_plan_t p) {
+    if (!p) return GEMM_OK;
+    gemm_status_t st = GEMM_OK;
+    if (p->dmem && cudaFree(p->dmem) != cudaSuccess) {
+        cudaGetLastError();
+        st = GEMM_ERR_CUDA;
+    }
+    delete p;
+    return st;
+}
+
+gemm_status_t gemm_plan_get_config(gemm_plan_t p, gemm_config_t* config) {
+    if (!p || !config) return GEMM_ERR_INVALID_ARG;
+    *config = p->cfg;
+    return GEMM_OK;
+}
+
+gemm_status_t gemm_plan_set_timeout(gemm_plan_t p, uint64_t ns) {
+    if (!p) return GEMM_ERR_INVALID_ARG;
+    p->kp.timeout_ns = ns ? ns : kDefaultTimeoutNs;
+    return GEMM_OK;
+}
+
+gemm_status_t gemm_select_config(int64_t M, int64_t N, int64_t K, gemm_dtype_t dtype,
+                                 int32_t num_sms, gemm_config_t* config) {
+    if (!config || num_sms < 1) return GEMM_ERR_INVALID_ARG;
+    gemm_status_t st = validate_shape(M, N, K, dtype, GEMM_LAYOUT_TN);
+    if (st != GEMM_OK) return st;
+    int32_t per = 0;
+    return normalise_config(M, N, K, dtype, gbg::select_config(M, N, K, dtype, num_sms), config, &per);
+}
+
+gemm_status_t gemm_tile_coords(int64_t m_blocks, int64_t n_blocks, int32_t raster_group,
+                               int64_t tile, int64_t* m_blk, int64_t* n_blk) {
+    if (!m_blk || !n_blk || m_blocks < 1 || n_blocks < 1 || raster_group < 1 || tile < 0 ||
+        m_blocks * n_blocks > INT32_MAX || tile >= m_blocks * n_blocks)
+        return GEMM_ERR_INVALID_ARG;
+    int32_t m = 0, n = 0;
+    gbg::raster_tile(static_cast<int32_t>(m_blocks), static_cast<int32_t>(n_blocks), raster_group,
+                     static_cast<int32_t>(tile), &m, &n);
+    *m_blk = m;
+    *n_blk = n;
+    return GEMM_OK;
+}
+
+gemm_status_t gemm_workspace_bytes(int64_t M, int64_t N, int64_t K, gemm_dtype_t dtype,
+                                   const gemm_config_t* config, size_t* bytes) {
+    if (!config || !bytes) return GEMM_ERR_INVALID_ARG;
+    gemm_status_t st = validate_shape(M, N, K, dtype, GEMM_LAYOUT_TN);
+    if (st != GEMM_OK) return st;
+    gemm_config_t c;
+    int32_t per = 0;
+    st = normalise_config(M, N, K, dtype, *config, &c, &per);
+    if (st != GEMM_OK) return st;
+    *bytes = plan_memory(M, N, K, dtype, c).total;
+    return GEMM_OK;
+}
+
+const char* gemm_status_string(gemm_status_t s) {
+    switch (s) {
+        case GEMM_OK: return "GEMM_OK";
+        case GEMM_ERR_INVALID_ARG: return "GEMM_ERR_INVALID_ARG: invalid argument";
+        case GEMM_ERR_UNSUPPORTED: return "GEMM_ERR_UNSUPPORTED: unsupported dtype or layout";
+        case GEMM_ERR_ALIGNMENT: return "GEMM_ERR_ALIGNMENT: pointer or row stride not 16-byte aligned";
+        case GEMM_ERR_NO_DEVICE: return "GEMM_ERR_NO_DEVICE: no CUDA device";
+        case GEMM_ERR_ARCH: return "GEMM_ERR_ARCH: device is not sm_103";
+        case GEMM_ERR_OOM: return "GEMM_ERR_OOM: device allocation failed";
+        case GEMM_ERR_TENSORMAP: return "GEMM_ERR_TENSORMAP: tensor map encoding failed";
+        case GEMM_ERR_LAUNCH: return "GEMM_ERR_LAUNCH: kernel launch failed";
+        case GEMM_ERR_DEVICE_TIMEOUT: return "GEMM_ERR_DEVICE_TIMEOUT: a kernel wait ran out";
+        case GEMM_ERR_CUDA: return "GEMM_ERR_CUDA: CUDA runtime error";
+        default: return "unknown gemm_status_t";
+    }
+}
+
+int32_t gemm_abi_version(void) { return GEMM_ABI_VERSION; }
+
+}  // extern "C"

@@ -1,0 +1,80 @@
+// gemm_aux.cu -- small HBM-bound kernels around the GEMM:
+//   * widen_i8: int8 operands -> fp16 copies (every int8 value is exact in fp16),
+//     the input side of the integer mode of the tensor-core kernel;
+//   * zero_fill: C = 0 for K == 0 (the empty sum).
+// Both are grid-stride loops over 16-byte vectors sized to a whole number of
+// waves of the SMs.
+#include <cuda_fp16.h>
+#include <stdint.h>
+
+#include "gemm_launch.h"
+
+namespace gbg {
+namespace {
+
+__device__ __forceinline__ uint32_t widen_pair(int8_t lo, int8_t hi) {
+    __half2 h = __halves2half2(__int2half_rn(lo), __int2half_rn(hi));
+    return *reinterpret_cast<uint32_t*>(&h);
+}
+
+// na, nb: number of 16-element groups of A and of B.
+__global__ void __launch_bounds__(256) widen_i8_kernel(const int4* __restrict__ a, int64_t na,
+                                                       const int4* __restrict__ b, int64_t nb,
+                                                       uint4* __restrict__ a16,
+                                                       uint4* __restrict__ b16) {
+    const int64_t total = na + nb;
+    const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+    for (int64_t g = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; g < total;
+         g += stride) {
+        const bool in_a = g < na;
+        const int64_t i = in_a ? g : g - na;
+        const int4 v = __ldg((in_a ? a : b) + i);
+        const int8_t* x = reinterpret_cast<const int8_t*>(&v);
+        uint4 lo, hi;
+        lo.x = widen_pair(x[0], x[1]);
+        lo.y = widen_pair(x[2], x[3]);
+        lo.z = widen_pair(x[4], x[5]);
+        lo.w = widen_pair(x[6], x[7]);
+        hi.x = widen_pair(x[8], x[9]);
+        hi.y = widen_pair(x[10], x[11]);
+        hi.z = widen_pair(x[12], x[13]);
+        hi.w = widen_pair(x[14], x[15]);
+        uint4* dst = (in_a ? a16 : b16) + 2 * i;
+        dst[0] = lo;
+        dst[1] = hi;
+    }
+}
+
+__global__ void __launch_bounds__(256) zero_fill_kernel(uint4* __restrict__ dst, int64_t n) {
+    const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+    for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n; i += stride)
+        dst[i] = make_uint4(0u, 0u, 0u, 0u);
+}
+
+int grid_for(int64_t work_items, int num_sms) {
+    const int64_t per_wave = static_cast<int64_t>(num_sms) * 8;    // 8 x 256 threads per SM
+    int64_t blocks = (work_items + 255) / 256;
+    if (blocks > per_wave) blocks = per_wave;
+    if (blocks < 1) blocks = 1;
+    return static_cast<int>(blocks);
+}
+
+}  // namespace
+
+cudaError_t launch_widen_i8(const int8_t* a, int64_t na, const int8_t* b, int64_t nb, void* a16,
+                            void* b16, int num_sms, cudaStream_t stream) {
+    // na, nb are element counts, multiples of 16 (K % 16 == 0).
+    const int64_t ga = na / 16, gb = nb / 16;
+    widen_i8_kernel<<<grid_for(ga + gb, num_sms), 256, 0, stream>>>(
+        reinterpret_cast<const int4*>(a), ga, reinterpret_cast<const int4*>(b), gb,
+        reinterpret_cast<uint4*>(a16), reinterpret_cast<uint4*>(b16));
+    return cudaGetLastError();
+}
+
+cudaError_t launch_zero_fill(void* dst, int64_t bytes, int num_sms, cudaStream_t stream) {
+    const int64_t n = bytes / 16;   // C rows are multiples of 16 bytes
+    zero_fill_kernel<<<grid_for(n, num_sms), 256, 0, stream>>>(reinterpret_cast<uint4*>(dst), n);
+    return cudaGetLastError();
+}
+
+}  // namespace gbg

@@ -1,0 +1,84 @@
+// gemm_config.h -- per-shape kernel configuration (host only).
+//
+// The pages tune tile shape, pipeline depth and swizzle with an RL agent
+// ("H100 GEMM L2驻留优化：warp-specialized TMA异步拷贝与RL调优策略", paragraph on
+// the RL agent and the "RL Search Space" list; "RL驱动CUDA L2 GEMM内核自动调优",
+// paragraph on RL autotune).  Here the choice comes from a measured table
+// (gemm_config_table.inc, written by tune.py from a sweep on the target GPU);
+// shapes not in the table use the cost model below.
+#pragma once
+#include <stdint.h>
+
+#include "gemm.h"
+#include "gemm_launch.h"
+
+namespace gbg {
+
+struct TableEntry {
+    int32_t M, N, K, dtype;
+    int32_t block_n, split_k, raster_group;
+};
+
+#include "gemm_config_table.inc"   // static const TableEntry kTunedTable[]; kTunedCount
+
+inline int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+// Relative main-loop efficiency of a 128 x BN tile: per 64-wide k-block the MMA
+// needs 128*BN*64/4096 cycles and shared memory delivers 128 B/cycle, so BN=256
+// is MMA-bound, BN=128 sits at the shared-memory limit and BN=64 is
+// shared-memory bound at about 2/3.
+inline double tile_efficiency(int bn) { return bn == 256 ? 1.0 : (bn == 128 ? 0.9 : 0.6); }
+
+inline gemm_config_t model_config(int64_t M, int64_t N, int64_t K, gemm_dtype_t dtype, int sms) {
+    gemm_config_t c;
+    c.stages = 0;
+    c.max_ctas = 0;
+    c.raster_group = 16;
+    c.split_k = 1;
+    const int64_t mb = ceil_div(M, kBM);
+    const int64_t num_kb = ceil_div(K, kBK);
+    const int cands_f[3] = {256, 128, 64};
+    const int cands_i[2] = {128, 64};
+    const int* cands = dtype == GEMM_I8_I32 ? cands_i : cands_f;
+    const int ncand = dtype == GEMM_I8_I32 ? 2 : 3;
+    double best = 1e300;
+    c.block_n = cands[ncand - 1];
+    for (int i = 0; i < ncand; ++i) {
+        const int bn = cands[i];
+        const int64_t tiles = mb * ceil_div(N, bn);
+        const double waves = static_cast<double>(ceil_div(tiles, sms));
+        const double t = waves * bn / tile_efficiency(bn);
+        if (t < best * 0.999) {
+            best = t;
+            c.block_n = bn;
+        }
+    }
+    // Few output tiles and a long K: slice K so that more SMs take part.
+    const int64_t tiles = mb * ceil_div(N, c.block_n);
+    if (tiles * 2 <= sms && num_kb >= 8) {
+        int64_t s = sms / tiles;
+        if (s > num_kb / 4) s = num_kb / 4;
+        if (s > 16) s = 16;
+        if (s < 1) s = 1;
+        c.split_k = static_cast<int32_t>(s);
+    }
+    return c;
+}
+
+inline gemm_config_t select_config(int64_t M, int64_t N, int64_t K, gemm_dtype_t dtype, int sms) {
+    for (int i = 0; i < kTunedCount; ++i) {
+        const TableEntry& e = kTunedTable[i];
+        if (e.M == M && e.N == N && e.K == K && e.dtype == static_cast<int32_t>(dtype)) {
+            gemm_config_t c;
+            c.block_n = e.block_n;
+            c.stages = 0;
+            c.split_k = e.split_k;
+            c.raster_group = e.raster_group;
+            c.max_ctas = 0;
+            return c;
+        }
+    }
+    return model_config(M, N, K, dtype, sms);
+}
+
+}  // namespace gbg

@@ -1,0 +1,49 @@
+// gemm_inst_f16.cu -- instantiations and launchers of the TN GEMM kernel with
+// f16 output.  Variants: (tile width BN, ring depth STAGES).
+#include "gemm_kernel.cuh"
+#include "gemm_launch.h"
+
+namespace gbg {
+namespace {
+
+template <int BN, int STAGES>
+cudaError_t prepare_one(size_t* smem_bytes) {
+    const size_t bytes = SmemLayout<BN, STAGES>::kTotal;
+    *smem_bytes = bytes;
+    return cudaFuncSetAttribute(gemm_tn_kernel<BN, STAGES, kOutF16>,
+                                cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(bytes));
+}
+
+template <int BN, int STAGES>
+cudaError_t launch_one(const LaunchShape& s, const CUtensorMap& a, const CUtensorMap& b,
+                       const KParams& p, cudaStream_t stream) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(s.grid));
+    cfg.blockDim = dim3(static_cast<unsigned>(s.block));
+    cfg.dynamicSmemBytes = s.smem_bytes;
+    cfg.stream = stream;
+    cfg.attrs = nullptr;
+    cfg.numAttrs = 0;
+    return cudaLaunchKernelEx(&cfg, gemm_tn_kernel<BN, STAGES, kOutF16>, a, b, p);
+}
+
+}  // namespace
+
+cudaError_t gemm_prepare_f16(int bn, int stages, size_t* smem_bytes) {
+#define X(B, S) \
+    if (bn == B && stages == S) return prepare_one<B, S>(smem_bytes);
+    X(64, 8) X(128, 6) X(256, 4)
+#undef X
+    return cudaErrorInvalidValue;
+}
+
+cudaError_t gemm_launch_f16(int bn, int stages, const LaunchShape& s, const CUtensorMap& a,
+                             const CUtensorMap& b, const KParams& p, cudaStream_t stream) {
+#define X(B, S) \
+    if (bn == B && stages == S) return launch_one<B, S>(s, a, b, p, stream);
+    X(64, 8) X(128, 6) X(256, 4)
+#undef X
+    return cudaErrorInvalidValue;
+}
+
+}  // namespace gbg

@@ -1,0 +1,606 @@
+// gemm_kernel.cuh -- persistent, warp-specialised TN GEMM for sm_103a (GB300).
+//
+//   C[M,N] = A[M,K] * B[N,K]^T        A, B K-contiguous; C N-contiguous.
+//
+// One CTA per SM, 192 threads in three roles:
+//   warp 0      TMA producer: one elected thread streams 128 x 64 A tiles and
+//               BN x 64 B tiles into a STAGES-deep shared-memory ring with
+//               cp.async.bulk.tensor (128-byte swizzle); each slot's mbarrier
+//               counts the landed bytes (expect_tx / complete_tx).
+//   warp 1      TMEM owner + MMA issuer: one elected thread issues
+//               tcgen05.mma (kind::f16, M=128, N=BN, K=16) into a TMEM fp32
+//               accumulator and returns each ring slot with tcgen05.commit.
+//   warps 2..5  epilogue: tcgen05.ld the accumulator (warp w reads TMEM lanes
+//               32*(w%4) ..), convert, store.  The accumulator is double
+//               buffered in TMEM so the epilogue of one tile runs under the
+//               main loop of the next.
+//
+// This is the GB300 counterpart of the warp-specialised producer/consumer
+// design in "H100 GEMM L2驻留优化：warp-specialized TMA异步拷贝与RL调优策略"
+// (paragraph on warp specialisation and the three-way overlap; lists "TMA
+// Descriptor", "Async Pipeline"), with WGMMA replaced by a single-thread
+// tcgen05.mma issuer and register accumulators replaced by TMEM.  The TMA
+// protocol (elected issuing thread, __grid_constant__ tensor maps, mbarrier
+// byte accounting for loads, zero fill outside the tensor) follows "B-08.
+// Hopper TMA：从单线程 Bulk Copy 到吞吐墙", sections 3.1 and 3.2.
+//
+// Integer mode (OUT == kOutI32): operands are int8 values already widened to
+// fp16 (exact); the MMA accumulates fp32 over chunks of at most `chunk_kb`
+// k-blocks, short enough that every partial sum is an integer below 2^24 in
+// magnitude and therefore exact in fp32; the epilogue rounds each chunk to
+// int32 and sums the chunks in integer registers.
+//
+// Every wait is bounded (globaltimer); on expiry the thread records a site code
+// in the error word, raises a CTA-wide abort flag, and all roles unwind to the
+// common exit, which waits for in-flight copies and MMAs and frees TMEM.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <stdint.h>
+
+#include "gemm_kernel_params.h"
+#include "gemm_sched.h"
+
+namespace gbg {
+
+template <int BN, int STAGES>
+struct SmemLayout {
+    static constexpr int kBTileBytes = BN * kBK * 2;
+    static constexpr int kStageBytes = kATileBytes + kBTileBytes;
+    static constexpr int kRingBytes = STAGES * kStageBytes;
+    static constexpr int kCtlBytes = 256;
+    static constexpr int kTotal = 1024 /* alignment slack */ + kRingBytes + kCtlBytes;
+    static_assert(kBTileBytes % 1024 == 0, "128B-swizzle tiles must stay 1024-byte aligned");
+    static_assert(STAGES * 16 + 5 * 8 + 16 <= kCtlBytes, "control block overflow");
+};
+
+// Control block after the ring.
+template <int STAGES>
+struct alignas(8) SharedCtl {
+    uint64_t full[STAGES];
+    uint64_t empty[STAGES];
+    uint64_t tmem_full[2];
+    uint64_t tmem_empty[2];
+    uint64_t drain;
+    uint32_t tmem_base;
+    int32_t abort;
+    int32_t splitk_last;
+};
+
+// ----------------------------------------------------------------------------
+// PTX wrappers
+// ----------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t smem_addr(const void* p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ uint64_t global_timer_ns() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+__device__ __forceinline__ bool elect_one_sync() {
+    uint32_t pred = 0;
+    asm volatile(
+        "{\n\t"
+        ".reg .b32 rx;\n\t"
+        ".reg .pred px;\n\t"
+        "elect.sync rx|px, %1;\n\t"
+        "@px mov.s32 %0, 1;\n\t"
+        "}"
+        : "+r"(pred)
+        : "r"(0xffffffffu));
+    return pred != 0;
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void fence_barrier_init() {
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+    uint32_t done;
+    asm volatile(
+        "{\n\t"
+        ".reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t"
+        "}"
+        : "=r"(done)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return done != 0;
+}
+
+struct Watch {
+    volatile int32_t* abort;   // CTA-wide abort flag (shared memory)
+    int32_t* error_word;       // plan error word (global memory)
+    uint64_t timeout_ns;
+};
+
+// Wait until the barrier phase with `parity` has completed.  Returns false if
+// the CTA is aborting or the wait ran out (then it records `site`).
+__device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity, const Watch& w,
+                                           int32_t site) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = global_timer_ns();
+    for (uint32_t n = 1;; ++n) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if ((n & 31u) == 0) {
+            if (*w.abort) return false;
+            if (global_timer_ns() - t0 > w.timeout_ns) {
+                *w.abort = 1;
+                atomicCAS(w.error_word, 0, site);
+                return false;
+            }
+        }
+    }
+}
+
+// Bounded wait used only while unwinding (ignores the abort flag).
+__device__ __forceinline__ bool wait_phase_unwind(uint32_t bar, uint32_t parity, uint64_t limit_ns) {
+    const uint64_t t0 = global_timer_ns();
+    while (!mbar_try_wait(bar, parity)) {
+        if (global_timer_ns() - t0 > limit_ns) return false;
+    }
+    return true;
+}
+
+__device__ __forceinline__ void prefetch_tmap(const CUtensorMap* m) {
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(m)) : "memory");
+}
+
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, uint32_t bar,
+                                            int32_t x, int32_t y) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%3, %4}], [%2];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(x), "r"(y)
+        : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() {
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+__device__ __forceinline__ void tmem_alloc(uint32_t dst_smem, uint32_t ncols) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem),
+                 "r"(ncols)
+                 : "memory");
+}
+__device__ __forceinline__ void tmem_relinquish() {
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
+                 : "memory");
+}
+
+// D[tmem] (+)= A[smem] * B[smem]^T, M=128, N=BN, K=16, fp32 accumulate.
+__device__ __forceinline__ void umma_f16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                         uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t"
+        ".reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t"
+        "}" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+// Arrive (once) on `bar` when every tcgen05.mma issued so far by this thread is done.
+__device__ __forceinline__ void umma_commit(uint32_t bar) {
+    asm volatile(
+        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+        : "memory");
+}
+
+// Shared-memory matrix descriptor for a K-major operand tile written by TMA
+// with 128-byte swizzle: rows of 128 bytes, 8-row (1024-byte) swizzle atoms
+// stacked at a 1024-byte stride.
+__device__ __forceinline__ uint64_t sw128_kmajor_desc(uint32_t saddr) {
+    return static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4)   // start address / 16
+           | (static_cast<uint64_t>(1) << 16)                // leading byte offset (unused here)
+           | (static_cast<uint64_t>(1024 >> 4) << 32)        // stride byte offset: 8 rows * 128 B
+           | (static_cast<uint64_t>(1) << 46)                // descriptor version (tcgen05)
+           | (static_cast<uint64_t>(2) << 61);               // swizzle mode: 128 B
+}
+
+// 32 lanes x 32 consecutive 32-bit TMEM columns -> 32 registers per thread.
+__device__ __forceinline__ void tmem_ld_32x32b_x32(uint32_t taddr, uint32_t (&r)[32]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
+        "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
+          "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]),
+          "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
+          "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]),
+          "=r"(r[31])
+        : "r"(taddr)
+        : "memory");
+}
+
+__device__ __forceinline__ void tmem_ld_wait() {
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t count) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ uint4 ld_cg_u4(const void* p) {
+    return __ldcg(reinterpret_cast<const uint4*>(p));
+}
+
+// ----------------------------------------------------------------------------
+// epilogue helpers: one thread owns one output row and 32 consecutive columns
+// ----------------------------------------------------------------------------
+template <int OUT>
+__device__ __forceinline__ uint32_t pack2(float lo, float hi) {
+    if constexpr (OUT == kOutF16) {
+        __half2 h = __floats2half2_rn(lo, hi);
+        return *reinterpret_cast<uint32_t*>(&h);
+    } else {
+        __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+        return *reinterpret_cast<uint32_t*>(&h);
+    }
+}
+
+// Store 32 fp32 values (as bits) of row `row`, columns [col, col+32) as fp16/bf16.
+template <int OUT>
+__device__ __forceinline__ void store_half_row32(void* C, int32_t N, int32_t row, int32_t col,
+                                                 const uint32_t (&v)[32]) {
+    uint16_t* base = reinterpret_cast<uint16_t*>(C) + static_cast<int64_t>(row) * N;
+#pragma unroll
+    for (int g = 0; g < 4; ++g) {
+        const int32_t c = col + g * 8;
+        if (c < N) {   // N % 8 == 0: an 8-column group is entirely in or out
+            uint4 q;
+            q.x = pack2<OUT>(__uint_as_float(v[g * 8 + 0]), __uint_as_float(v[g * 8 + 1]));
+            q.y = pack2<OUT>(__uint_as_float(v[g * 8 + 2]), __uint_as_float(v[g * 8 + 3]));
+            q.z = pack2<OUT>(__uint_as_float(v[g * 8 + 4]), __uint_as_float(v[g * 8 + 5]));
+            q.w = pack2<OUT>(__uint_as_float(v[g * 8 + 6]), __uint_as_float(v[g * 8 + 7]));
+            *reinterpret_cast<uint4*>(base + c) = q;
+        }
+    }
+}
+
+// Store 32 int32 values of row `row`, columns [col, col+32).
+__device__ __forceinline__ void store_i32_row32(void* C, int32_t N, int32_t row, int32_t col,
+                                                const uint32_t* v) {
+    uint32_t* base = reinterpret_cast<uint32_t*>(C) + static_cast<int64_t>(row) * N;
+#pragma unroll
+    for (int g = 0; g < 8; ++g) {
+        const int32_t c = col + g * 4;
+        if (c < N) {   // N % 4 == 0
+            *reinterpret_cast<uint4*>(base + c) =
+                make_uint4(v[g * 4 + 0], v[g * 4 + 1], v[g * 4 + 2], v[g * 4 + 3]);
+        }
+    }
+}
+
+__device__ __forceinline__ void store_ws32(uint32_t* dst, const uint32_t* v) {
+#pragma unroll
+    for (int g = 0; g < 8; ++g)
+        __stcg(reinterpret_cast<uint4*>(dst) + g,
+               make_uint4(v[g * 4 + 0], v[g * 4 + 1], v[g * 4 + 2], v[g * 4 + 3]));
+}
+
+// ----------------------------------------------------------------------------
+// the kernel
+// ----------------------------------------------------------------------------
+template <int BN, int STAGES, int OUT>
+__global__ void __launch_bounds__(kThreads, 1)
+    gemm_tn_kernel(const __grid_constant__ CUtensorMap tmap_a,
+                   const __grid_constant__ CUtensorMap tmap_b, const KParams p) {
+    using L = SmemLayout<BN, STAGES>;
+    static_assert(BN == 64 || BN == 128 || BN == 256, "tile width");
+    static_assert(OUT != kOutI32 || BN <= 128, "integer mode keeps BN int32 sums in registers");
+    constexpr uint32_t kTmemCols = 2 * BN;   // two accumulator buffers; 128/256/512 columns
+    constexpr uint32_t kStageTx = L::kStageBytes;
+
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw_addr = smem_addr(smem_raw);
+    uint8_t* smem = smem_raw + ((1024u - (raw_addr & 1023u)) & 1023u);
+    const uint32_t ring = smem_addr(smem);                       // A slots, then B slots
+    const uint32_t ring_b = ring + STAGES * kATileBytes;
+    SharedCtl<STAGES>* ctl = reinterpret_cast<SharedCtl<STAGES>*>(smem + L::kRingBytes);
+
+    const int warp = __shfl_sync(0xffffffffu, static_cast<int>(threadIdx.x) / 32, 0);
+    const int lane = static_cast<int>(threadIdx.x) & 31;
+
+    if (warp == 0 && lane == 0) {
+        prefetch_tmap(&tmap_a);
+        prefetch_tmap(&tmap_b);
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(smem_addr(&ctl->full[s]), 1);
+            mbar_init(smem_addr(&ctl->empty[s]), 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(smem_addr(&ctl->tmem_full[b]), 1);
+            mbar_init(smem_addr(&ctl->tmem_empty[b]), kEpiWarps);
+        }
+        mbar_init(smem_addr(&ctl->drain), 1);
+        ctl->abort = 0;
+        ctl->splitk_last = 0;
+        fence_barrier_init();
+    }
+    if (warp == 1) {
+        tmem_alloc(smem_addr(&ctl->tmem_base), kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = ctl->tmem_base;
+    const Watch watch{&ctl->abort, p.error_word, p.timeout_ns};
+
+    if (warp == 0) {
+        // ------------------------------------------------------------ producer
+        if (elect_one_sync()) {
+            int stage = 0;
+            uint32_t phase = 0;
+            int issued = 0;
+            bool ok = true;
+            for (int32_t u = blockIdx.x; ok && u < p.num_units; u += gridDim.x) {
+                const UnitCoord c = unit_coord(u, p.split_k, p.kb_per_split, p.num_kb, p.m_blocks,
+                                               p.n_blocks, p.raster_group);
+                for (int32_t kb = c.kb_begin; kb < c.kb_end; ++kb) {
+                    const uint32_t full = smem_addr(&ctl->full[stage]);
+                    if (!wait_phase(smem_addr(&ctl->empty[stage]), phase ^ 1u, watch,
+                                    kSiteProducerEmpty)) {
+                        ok = false;
+                        break;
+                    }
+                    mbar_arrive_expect_tx(full, kStageTx + p.tx_extra);
+                    tma_load_2d(ring + stage * kATileBytes, &tmap_a, full, kb * kBK, c.m_blk * kBM);
+                    tma_load_2d(ring_b + stage * L::kBTileBytes, &tmap_b, full, kb * kBK,
+                                c.n_blk * BN);
+                    ++issued;
+                    if (++stage == STAGES) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+            }
+            // Let every copy this thread issued land before the CTA can exit
+            // (immediate in normal operation: the MMA issuer consumed them all;
+            // matters when some role gave up on a wait).
+            {
+                int s = stage;
+                uint32_t ph = phase;
+                const int pending = issued < STAGES ? issued : STAGES;
+                for (int i = 0; i < pending; ++i) {
+                    if (--s < 0) {
+                        s = STAGES - 1;
+                        ph ^= 1u;
+                    }
+                    wait_phase_unwind(smem_addr(&ctl->full[s]), ph, 100000000ull);
+                }
+            }
+            (void)ok;
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        // ------------------------------------------------------------ MMA issuer
+        if (elect_one_sync()) {
+            int stage = 0;
+            uint32_t phase = 0;
+            uint32_t acc_iter = 0;
+            bool ok = true;
+            for (int32_t u = blockIdx.x; ok && u < p.num_units; u += gridDim.x) {
+                const UnitCoord c = unit_coord(u, p.split_k, p.kb_per_split, p.num_kb, p.m_blocks,
+                                               p.n_blocks, p.raster_group);
+                for (int32_t k0 = c.kb_begin; ok && k0 < c.kb_end; k0 += p.chunk_kb) {
+                    const int32_t k1 = (k0 + p.chunk_kb < c.kb_end) ? k0 + p.chunk_kb : c.kb_end;
+                    const uint32_t buf = acc_iter & 1u;
+                    const uint32_t acc_phase = (acc_iter >> 1) & 1u;
+                    if (!wait_phase(smem_addr(&ctl->tmem_empty[buf]), acc_phase ^ 1u, watch,
+                                    kSiteMmaTmemEmpty)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t d_tmem = tmem_base + buf * BN;
+                    for (int32_t kb = k0; kb < k1; ++kb) {
+                        if (!wait_phase(smem_addr(&ctl->full[stage]), phase, watch, kSiteMmaFull)) {
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after();
+                        const uint64_t a_desc = sw128_kmajor_desc(ring + stage * kATileBytes);
+                        const uint64_t b_desc = sw128_kmajor_desc(ring_b + stage * L::kBTileBytes);
+#pragma unroll
+                        for (int k = 0; k < kBK / 16; ++k) {
+                            // +32 bytes along K per instruction (encoded >> 4)
+                            umma_f16(d_tmem, a_desc + 2u * k, b_desc + 2u * k, p.idesc,
+                                     (kb > k0 || k > 0) ? 1u : 0u);
+                        }
+                        umma_commit(smem_addr(&ctl->empty[stage]));
+                        if (++stage == STAGES) {
+                            stage = 0;
+                            phase ^= 1u;
+                        }
+                    }
+                    if (!ok) break;
+                    umma_commit(smem_addr(&ctl->tmem_full[buf]));
+                    ++acc_iter;
+                }
+            }
+            // Drain: every MMA issued above completes before TMEM is released.
+            umma_commit(smem_addr(&ctl->drain));
+            wait_phase_unwind(smem_addr(&ctl->drain), 0, 100000000ull);
+        }
+        __syncwarp();
+    } else {
+        // ------------------------------------------------------------ epilogue
+        const int quad = warp & 3;                    // TMEM lanes this warp may access
+        const int row_in_tile = quad * 32 + lane;
+        const int epi_tid = (warp - 2) * 32 + lane;   // 0..127
+        const uint32_t lane_addr = static_cast<uint32_t>(quad * 32) << 16;
+        uint32_t acc_iter = 0;
+        bool ok = true;
+        for (int32_t u = blockIdx.x; ok && u < p.num_units; u += gridDim.x) {
+            const UnitCoord c = unit_coord(u, p.split_k, p.kb_per_split, p.num_kb, p.m_blocks,
+                                           p.n_blocks, p.raster_group);
+            const int32_t row = c.m_blk * kBM + row_in_tile;
+            const int32_t col0 = c.n_blk * BN;
+            const bool split = p.split_k > 1;
+            uint32_t* ws_row = nullptr;
+            if (split)
+                ws_row = reinterpret_cast<uint32_t*>(p.workspace) +
+                         (static_cast<int64_t>(u) * kBM + row_in_tile) * BN;
+
+            if constexpr (OUT == kOutI32) {
+                uint32_t sum[BN];
+#pragma unroll
+                for (int i = 0; i < BN; ++i) sum[i] = 0u;
+                for (int32_t k0 = c.kb_begin; k0 < c.kb_end; k0 += p.chunk_kb) {
+                    const uint32_t buf = acc_iter & 1u;
+                    const uint32_t acc_phase = (acc_iter >> 1) & 1u;
+                    if (!wait_phase(smem_addr(&ctl->tmem_full[buf]), acc_phase, watch,
+                                    kSiteEpiTmemFull)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+#pragma unroll
+                    for (int j = 0; j < BN / 32; ++j) {
+                        uint32_t v[32];
+                        tmem_ld_32x32b_x32(tmem_base + lane_addr + buf * BN + j * 32, v);
+                        tmem_ld_wait();
+#pragma unroll
+                        for (int i = 0; i < 32; ++i)
+                            sum[j * 32 + i] +=
+                                static_cast<uint32_t>(__float2int_rn(__uint_as_float(v[i])));
+                    }
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(smem_addr(&ctl->tmem_empty[buf]));
+                    ++acc_iter;
+                }
+                if (!ok) break;
+#pragma unroll
+                for (int j = 0; j < BN / 32; ++j) {
+                    if (split) {
+                        store_ws32(ws_row + j * 32, &sum[j * 32]);
+                    } else if (row < p.M) {
+                        store_i32_row32(p.C, p.N, row, col0 + j * 32, &sum[j * 32]);
+                    }
+                }
+            } else {
+                const uint32_t buf = acc_iter & 1u;
+                const uint32_t acc_phase = (acc_iter >> 1) & 1u;
+                if (!wait_phase(smem_addr(&ctl->tmem_full[buf]), acc_phase, watch,
+                                kSiteEpiTmemFull)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+#pragma unroll 1
+                for (int j = 0; j < BN / 32; ++j) {
+                    uint32_t v[32];
+                    tmem_ld_32x32b_x32(tmem_base + lane_addr + buf * BN + j * 32, v);
+                    tmem_ld_wait();
+                    if (split) {
+                        store_ws32(ws_row + j * 32, v);
+                    } else if (row < p.M) {
+                        store_half_row32<OUT>(p.C, p.N, row, col0 + j * 32, v);
+                    }
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(smem_addr(&ctl->tmem_empty[buf]));
+                ++acc_iter;
+            }
+
+            if (split) {
+                // Publish this slice; the last slice to arrive sums all slices in
+                // slice order 0..S-1 (fixed order: identical results every run).
+                __threadfence();
+                named_bar_sync(1, kEpiWarps * 32);
+                if (epi_tid == 0) {
+                    const uint32_t prev = atomicAdd(&p.counters[c.tile], 1u);
+                    const int32_t last = (prev == static_cast<uint32_t>(p.split_k - 1)) ? 1 : 0;
+                    if (last) atomicExch(&p.counters[c.tile], 0u);
+                    ctl->splitk_last = last;
+                }
+                named_bar_sync(1, kEpiWarps * 32);
+                const int32_t last = *reinterpret_cast<volatile int32_t*>(&ctl->splitk_last);
+                if (last && row < p.M) {
+                    __threadfence();
+                    const uint32_t* tile_ws = reinterpret_cast<const uint32_t*>(p.workspace) +
+                                              (static_cast<int64_t>(c.tile) * p.split_k * kBM +
+                                               row_in_tile) * BN;
+                    const int64_t slice_stride = static_cast<int64_t>(kBM) * BN;
+#pragma unroll 1
+                    for (int j = 0; j < BN / 32; ++j) {
+                        uint32_t v[32];
+                        if constexpr (OUT == kOutI32) {
+#pragma unroll
+                            for (int i = 0; i < 32; ++i) v[i] = 0u;
+                        } else {
+#pragma unroll
+                            for (int i = 0; i < 32; ++i) v[i] = __float_as_uint(0.0f);
+                        }
+                        for (int32_t s = 0; s < p.split_k; ++s) {
+                            const uint32_t* src = tile_ws + s * slice_stride + j * 32;
+#pragma unroll
+                            for (int g = 0; g < 8; ++g) {
+                                const uint4 q = ld_cg_u4(src + g * 4);
+                                if constexpr (OUT == kOutI32) {
+                                    v[g * 4 + 0] += q.x;
+                                    v[g * 4 + 1] += q.y;
+                                    v[g * 4 + 2] += q.z;
+                                    v[g * 4 + 3] += q.w;
+                                } else {
+                                    v[g * 4 + 0] = __float_as_uint(__uint_as_float(v[g * 4 + 0]) + __uint_as_float(q.x));
+                                    v[g * 4 + 1] = __float_as_uint(__uint_as_float(v[g * 4 + 1]) + __uint_as_float(q.y));
+                                    v[g * 4 + 2] = __float_as_uint(__uint_as_float(v[g * 4 + 2]) + __uint_as_float(q.z));
+                                    v[g * 4 + 3] = __float_as_uint(__uint_as_float(v[g * 4 + 3]) + __uint_as_float(q.w));
+                                }
+                            }
+                        }
+                        if constexpr (OUT == kOutI32) {
+                            store_i32_row32(p.C, p.N, row, col0 + j * 32, v);
+                        } else {
+                            store_half_row32<OUT>(p.C, p.N, row, col0 + j * 32, v);
+                        }
+                    }
+                }
+            }
+        }
+    }
+
+    // ---------------------------------------------------------------- teardown
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem_base, kTmemCols);
+    }
+}
+
+}  // namespace gbg

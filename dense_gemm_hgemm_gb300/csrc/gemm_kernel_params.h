@@ -1,0 +1,42 @@
+// gemm_kernel_params.h -- kernel parameter block and constants shared by the
+// kernels and the host planner.
+#pragma once
+#include <stdint.h>
+
+#include "gemm_sched.h"
+
+namespace gbg {
+
+constexpr int kThreads = 192;
+constexpr int kEpiWarps = 4;
+constexpr int kATileBytes = kBM * kBK * 2;   // 16 KiB
+
+enum OutKind : int { kOutF16 = 0, kOutBF16 = 1, kOutI32 = 2 };
+
+// Wait-site codes written to the error word when a wait runs out.
+enum WaitSite : int32_t {
+    kSiteProducerEmpty = 1,
+    kSiteMmaFull = 2,
+    kSiteMmaTmemEmpty = 3,
+    kSiteEpiTmemFull = 4,
+};
+
+struct KParams {
+    int32_t M, N, K;
+    int32_t num_kb;         // ceil(K / kBK)
+    int32_t m_blocks, n_blocks;
+    int32_t split_k;        // K slices per tile
+    int32_t kb_per_split;   // k-blocks per slice
+    int32_t chunk_kb;       // k-blocks per accumulation chunk (integer mode), else >= kb_per_split
+    int32_t raster_group;
+    int32_t num_units;      // m_blocks * n_blocks * split_k
+    uint32_t idesc;         // tcgen05 instruction descriptor
+    uint32_t tx_extra;      // extra bytes each ring slot expects (0 in normal operation)
+    void* C;
+    void* workspace;        // split-K partials: [num_units][kBM][BN] fp32 (int32 in integer mode)
+    uint32_t* counters;     // split-K arrival counter per tile (self-resetting)
+    int32_t* error_word;
+    uint64_t timeout_ns;
+};
+
+}  // namespace gbg

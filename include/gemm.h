@@ -1,0 +1,172 @@
+/*
+ * gemm.h -- C ABI of the GB300 (sm_103a) TN GEMM library  libgemm_gb300.so
+ *
+ * The operation (HGEMM and its int8 variant):
+ *
+ *     C[i][j] = sum_{k<K} A[i][k] * B[j][k]          0 <= i < M, 0 <= j < N
+ *
+ * with A an M x K row-major matrix, B an N x K row-major matrix (both contiguous
+ * along K: the "row-major A, column-major B" layout of the HGEMM kernels in
+ * "RL驱动CUDA L2 GEMM内核自动调优：A100/H100 tile size与融合优化", paragraph on tile
+ * size and data layout) and C an M x N row-major matrix that is overwritten
+ * (no alpha/beta, C is never read).
+ *
+ *   GEMM_F16    : fp16 A, B;  fp32 accumulation;  fp16 C (round to nearest even)
+ *   GEMM_BF16   : bf16 A, B;  fp32 accumulation;  bf16 C (round to nearest even)
+ *   GEMM_I8_I32 : int8 A, B;  exact integer sum;  int32 C (two's-complement wrap
+ *                 modulo 2^32 if a sum leaves the int32 range)
+ *   (fp16 / int8 precision switch of the same post, paragraph on multi-precision
+ *    adaptation; the fp32 accumulator is this library's reading where the post
+ *    is silent.)
+ *
+ * Ownership and threading
+ *   - A plan is created for one (M, N, K, dtype, layout) on the device that is
+ *     current at creation time and must be used with that device current.
+ *   - The plan owns its device memory (error word, split-K partials and
+ *     counters, int8 conversion buffers).  A, B and C are owned by the caller,
+ *     are device pointers, and must stay valid until the stream work finishes.
+ *   - gemm_run is asynchronous on the caller's stream.  A plan holds one set of
+ *     scratch buffers: do not run the same plan on two streams at once.
+ *   - No host locks are taken; distinct plans may be used from distinct threads.
+ *
+ * Errors
+ *   Every call returns a gemm_status_t.  Argument and alignment problems are
+ *   reported before any device work is queued.  No call falls back to another
+ *   backend or to the CPU.  Kernels bound every wait; a wait that runs out sets
+ *   the plan's device error word, which gemm_plan_check reports as
+ *   GEMM_ERR_DEVICE_TIMEOUT.
+ */
+#ifndef GB300_GEMM_H
+#define GB300_GEMM_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define GEMM_ABI_VERSION 1
+
+typedef enum {
+    GEMM_F16 = 0,
+    GEMM_BF16 = 1,
+    GEMM_I8_I32 = 2
+} gemm_dtype_t;
+
+typedef enum {
+    GEMM_LAYOUT_TN = 0   /* A[M,K] row-major, B[N,K] row-major, C[M,N] row-major */
+} gemm_layout_t;
+
+typedef enum {
+    GEMM_OK = 0,
+    GEMM_ERR_INVALID_ARG = 1,     /* negative size, NULL pointer, bad config, wrong device */
+    GEMM_ERR_UNSUPPORTED = 2,     /* unknown dtype or layout */
+    GEMM_ERR_ALIGNMENT = 3,       /* pointer not 16-byte aligned or row stride not a multiple of 16 B */
+    GEMM_ERR_NO_DEVICE = 4,       /* no CUDA device / driver */
+    GEMM_ERR_ARCH = 5,            /* current device is not compute capability 10.3 */
+    GEMM_ERR_OOM = 6,             /* device allocation for the plan failed */
+    GEMM_ERR_TENSORMAP = 7,       /* cuTensorMapEncodeTiled rejected a descriptor */
+    GEMM_ERR_LAUNCH = 8,          /* kernel launch failed */
+    GEMM_ERR_DEVICE_TIMEOUT = 9,  /* a kernel wait ran out (reported by gemm_plan_check) */
+    GEMM_ERR_CUDA = 10            /* any other CUDA runtime error */
+} gemm_status_t;
+
+/*
+ * Kernel configuration (what the per-shape table chooses; see gemm_select_config).
+ *   block_n      : output tile width, 64, 128 or 256 (tile height is 128 rows;
+ *                  int8 allows 64 or 128)
+ *   stages       : depth of the shared-memory ring; 0 = the default for block_n
+ *   split_k      : number of K slices per output tile (>= 1); slices are summed
+ *                  in a fixed order, so results are run-to-run identical
+ *   raster_group : m-blocks per band of the L2-friendly tile order (>= 1)
+ *   max_ctas     : persistent grid cap; 0 = one CTA per SM
+ */
+typedef struct {
+    int32_t block_n;
+    int32_t stages;
+    int32_t split_k;
+    int32_t raster_group;
+    int32_t max_ctas;
+} gemm_config_t;
+
+typedef struct gemm_plan *gemm_plan_t;
+
+/*
+ * Create a plan.  Validates the arguments (sizes >= 0; K a multiple of 8 for
+ * fp16/bf16 and of 16 for int8 so that A and B rows are 16-byte aligned; N a
+ * multiple of 8 for fp16/bf16 and of 4 for int8 so that C rows are 16-byte
+ * aligned), checks the current device is an sm_103 part, picks the kernel
+ * configuration from the built-in table and allocates the plan's scratch
+ * memory.  On success *plan receives a handle that gemm_plan_destroy frees.
+ * Row-stride rule: "TMA/2D tensor" alignment of "B-08. Hopper TMA：从单线程 Bulk
+ * Copy 到吞吐墙" (www.lqnn.cn), section 6.1 (global base 16 B, strides multiples
+ * of 16 B).
+ */
+gemm_status_t gemm_plan_create(int64_t M, int64_t N, int64_t K, gemm_dtype_t dtype,
+                               gemm_layout_t layout, gemm_plan_t *plan);
+
+/* As gemm_plan_create, with an explicit configuration instead of the table's. */
+gemm_status_t gemm_plan_create_with_config(int64_t M, int64_t N, int64_t K, gemm_dtype_t dtype,
+                                           gemm_layout_t layout, const gemm_config_t *config,
+                                           gemm_plan_t *plan);
+
+/*
+ * Queue C = A * B^T on `stream` (a cudaStream_t; NULL = the legacy default
+ * stream).  A, B, C: device pointers, 16-byte aligned, in the plan's layout and
+ * element types.  M == 0 or N == 0 queues nothing; K == 0 writes zeros to C.
+ * Returns after queueing; errors of the queued work surface through
+ * gemm_plan_check or the CUDA stream.
+ */
+gemm_status_t gemm_run(gemm_plan_t plan, const void *A, const void *B, void *C, void *stream);
+
+/*
+ * Synchronise `stream`, then read and clear the plan's device error word.
+ * GEMM_ERR_DEVICE_TIMEOUT if a kernel of this plan gave up on a wait,
+ * GEMM_ERR_CUDA if the stream reported an error, else GEMM_OK.
+ */
+gemm_status_t gemm_plan_check(gemm_plan_t plan, void *stream);
+
+/* Free a plan and its device memory.  NULL is a no-op. */
+gemm_status_t gemm_plan_destroy(gemm_plan_t plan);
+
+/* The configuration a plan runs with. */
+gemm_status_t gemm_plan_get_config(gemm_plan_t plan, gemm_config_t *config);
+
+/*
+ * Set the limit, in nanoseconds, after which a kernel wait of this plan gives
+ * up (default 2e9).  ns == 0 restores the default.
+ */
+gemm_status_t gemm_plan_set_timeout(gemm_plan_t plan, uint64_t ns);
+
+/*
+ * Host-only query (no device work): the configuration the table picks for a
+ * shape on a GPU with `num_sms` SMs, after validating the shape as
+ * gemm_plan_create does.
+ */
+gemm_status_t gemm_select_config(int64_t M, int64_t N, int64_t K, gemm_dtype_t dtype,
+                                 int32_t num_sms, gemm_config_t *config);
+
+/*
+ * Host-only: the output tile (m_blk, n_blk) that the persistent scheduler
+ * assigns to linear tile index `tile` for an m_blocks x n_blocks tile grid in
+ * bands of `raster_group` m-blocks (the same function the kernels evaluate).
+ */
+gemm_status_t gemm_tile_coords(int64_t m_blocks, int64_t n_blocks, int32_t raster_group,
+                               int64_t tile, int64_t *m_blk, int64_t *n_blk);
+
+/* Bytes of device memory a plan for this shape/config allocates (host-only). */
+gemm_status_t gemm_workspace_bytes(int64_t M, int64_t N, int64_t K, gemm_dtype_t dtype,
+                                   const gemm_config_t *config, size_t *bytes);
+
+/* Static description of a status code. */
+const char *gemm_status_string(gemm_status_t status);
+
+/* GEMM_ABI_VERSION of the built library. */
+int32_t gemm_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GB300_GEMM_H */

@@ -1,0 +1,159 @@
+"""Host-side checks of the C ABI (no GPU needed): exports, validation, planning logic."""
+import os
+import re
+
+import pytest
+import torch
+
+from dense_gemm_hgemm_gb300 import workloads
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HAS_GPU = torch.cuda.is_available()
+
+
+def _declared_functions():
+    text = open(os.path.join(ROOT, "include", "gemm.h"), encoding="utf-8").read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(gemm_[a-z_0-9]+)\s*\(", text)))
+
+
+def test_header_declares_the_boundary():
+    names = _declared_functions()
+    for required in ("gemm_plan_create", "gemm_run", "gemm_plan_destroy", "gemm_plan_check",
+                     "gemm_status_string"):
+        assert required in names
+
+
+def test_library_exports_every_declared_symbol(gemm_lib):
+    lib = gemm_lib.library()
+    missing = [n for n in _declared_functions() if not hasattr(lib, n)]
+    assert not missing, missing
+
+
+def test_exported_symbols_are_c_linkage(gemm_lib):
+    import subprocess
+    out = subprocess.run(["nm", "-D", "--defined-only", gemm_lib.LIB_PATH] if hasattr(gemm_lib, "LIB_PATH")
+                         else ["nm", "-D", "--defined-only", gemm_lib._build.LIB_PATH],
+                         capture_output=True, text=True, check=True).stdout
+    exported = set(line.split()[-1] for line in out.splitlines() if line.strip())
+    for n in _declared_functions():
+        assert n in exported, n
+
+
+def test_abi_version_and_status_strings(gemm_lib):
+    assert gemm_lib.gemm_abi_version() == 1
+    for code, name in gemm_lib.STATUS_NAMES.items():
+        assert gemm_lib.gemm_status_string(code).startswith(name)
+    assert "unknown" in gemm_lib.gemm_status_string(1234)
+
+
+def _create_status(g, M, N, K, dtype, layout=0):
+    import ctypes
+    h = ctypes.c_void_p()
+    st = g.library().gemm_plan_create(M, N, K, dtype, layout, ctypes.byref(h))
+    if st == 0:
+        g.gemm_plan_destroy(h.value)
+    return st
+
+
+@pytest.mark.parametrize("args,expect", [
+    ((64, 64, 64, 7, 0), 2),        # unknown dtype
+    ((64, 64, 64, 0, 1), 2),        # unknown layout
+    ((-1, 64, 64, 0, 0), 1),        # negative M
+    ((64, -8, 64, 0, 0), 1),
+    ((64, 64, -8, 1, 0), 1),
+    ((64, 64, 60, 0, 0), 3),        # K*2 bytes not a multiple of 16
+    ((64, 60, 64, 0, 0), 3),        # N*2 bytes not a multiple of 16
+    ((64, 64, 40, 2, 0), 3),        # int8: K must be a multiple of 16
+    ((64, 62, 64, 2, 0), 3),        # int32 C: N must be a multiple of 4
+    ((2 ** 31, 64, 64, 0, 0), 1),   # beyond 32-bit indices
+])
+def test_create_validates_before_touching_the_device(gemm_lib, args, expect):
+    assert _create_status(gemm_lib, *args) == expect
+
+
+@pytest.mark.skipif(HAS_GPU, reason="checks the no-device path")
+def test_create_without_gpu_reports_no_device(gemm_lib):
+    assert _create_status(gemm_lib, 128, 128, 64, 0) == 4
+
+
+def test_null_handles(gemm_lib):
+    lib = gemm_lib.library()
+    assert lib.gemm_plan_destroy(None) == 0
+    assert lib.gemm_run(None, None, None, None, None) == 1
+    assert lib.gemm_plan_check(None, None) == 1
+    assert lib.gemm_plan_get_config(None, None) == 1
+    assert lib.gemm_plan_set_timeout(None, 5) == 1
+    assert lib.gemm_plan_create(64, 64, 64, 0, 0, None) == 1
+
+
+def test_select_config_valid_for_every_workload(gemm_lib):
+    shapes = [(w.M, w.N, w.K, w.dtype) for w in workloads.NAMED + tuple(workloads.sweep_shapes())]
+    for M, N, K, dt in shapes:
+        c = gemm_lib.gemm_select_config(M, N, K, dt, 152)
+        bn = c["block_n"]
+        assert bn in ((64, 128) if dt == "i8" else (64, 128, 256)), (M, N, K, c)
+        assert c["stages"] in (4, 6, 8)
+        num_kb = -(-K // 64)
+        assert 1 <= c["split_k"] <= num_kb
+        per = -(-num_kb // c["split_k"])
+        assert (c["split_k"] - 1) * per < num_kb          # no empty K slice
+        assert 1 <= c["raster_group"]
+
+
+def test_select_config_big_shapes_fill_the_gpu(gemm_lib):
+    for w in (workloads.SQUARE_8192, workloads.FFN_BF16, workloads.INT8_4096):
+        c = gemm_lib.gemm_select_config(w.M, w.N, w.K, w.dtype, 152)
+        tiles = -(-w.M // 128) * -(-w.N // c["block_n"])
+        assert tiles >= 152 and c["split_k"] == 1
+
+
+def test_select_config_splits_k_for_few_tiles(gemm_lib):
+    c = gemm_lib.gemm_select_config(128, 128, 4096, "f16", 152)
+    assert c["split_k"] > 1
+
+
+@pytest.mark.parametrize("mb,nb,g", [(1, 1, 1), (7, 3, 2), (64, 32, 16), (33, 57, 8), (5, 9, 16)])
+def test_raster_is_a_bijection(gemm_lib, mb, nb, g):
+    seen = set()
+    for t in range(mb * nb):
+        m, n = gemm_lib.gemm_tile_coords(mb, nb, g, t)
+        assert 0 <= m < mb and 0 <= n < nb
+        seen.add((m, n))
+    assert len(seen) == mb * nb
+
+
+def test_raster_bands_keep_concurrent_tiles_compact(gemm_lib):
+    # 152 consecutive tiles of a 64 x 32 grid in bands of 16 m-blocks touch at
+    # most 16 m-blocks and ceil(152/16)+1 n-blocks.
+    ms, ns = set(), set()
+    for t in range(152):
+        m, n = gemm_lib.gemm_tile_coords(64, 32, 16, t)
+        ms.add(m)
+        ns.add(n)
+    assert len(ms) <= 16 and len(ns) <= 11
+
+
+def test_workspace_bytes(gemm_lib):
+    base = gemm_lib.gemm_workspace_bytes(128, 128, 4096, "f16", {"block_n": 128, "split_k": 1})
+    split = gemm_lib.gemm_workspace_bytes(128, 128, 4096, "f16", {"block_n": 128, "split_k": 4})
+    assert split - base >= 4 * 128 * 128 * 4
+    i8 = gemm_lib.gemm_workspace_bytes(256, 512, 1024, "i8", {"block_n": 128})
+    assert i8 >= (256 + 512) * 1024 * 2
+    with pytest.raises(gemm_lib.GemmError):
+        gemm_lib.gemm_workspace_bytes(128, 128, 64, "i8", {"block_n": 256})
+    with pytest.raises(gemm_lib.GemmError):
+        gemm_lib.gemm_workspace_bytes(128, 128, 64, "f16", {"block_n": 96})
+    with pytest.raises(gemm_lib.GemmError):
+        gemm_lib.gemm_workspace_bytes(128, 128, 64, "f16", {"block_n": 128, "stages": 3})
+
+
+def test_product_path_has_no_oracle_or_fallback():
+    """The package never imports the oracle, torch matmul or another GEMM backend."""
+    pkg = os.path.join(ROOT, "dense_gemm_hgemm_gb300")
+    banned = re.compile(r"import oracle|from oracle|torch\.matmul|cublas|triton|np\.dot|\.mm\(|einsum|bmm")
+    for dirpath, _, files in os.walk(pkg):
+        for f in files:
+            if f.endswith((".py", ".cu", ".cuh", ".h", ".inc")):
+                text = open(os.path.join(dirpath, f), encoding="utf-8").read()
+                assert not banned.search(text), (f, banned.search(text).group(0))
