@@ -1,0 +1,583 @@
+#!/usr/bin/env python
+"""Benchmark: the fp16 TN GEMM shape sweep (343 shapes, M, N, K in {64..4096}).
+
+One step = one gemm_run for every shape of the sweep, each on its own
+device-resident A, B, C (2.77 GB of distinct operands per step, more than the
+129 MB L2, so no step finds the previous step's data in L2).  `value` is the
+whole-job throughput sum(2*M*N*K) / step time in TFLOP/s, over all ranks.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Prints one JSON line (rank 0).  Also reported on that line (measured outside
+the timed region): `e2e` (the same sweep through the C ABI with operands copied
+from pinned host memory and C copied back inside the timed region), `named`
+(µs/call and TFLOP/s of the named workloads: 64x4096x64 and 128x2048x128 fp16,
+8192^3 fp16, the 4096x14336x4096 bf16 FFN shape, 4096^3 int8->int32), the
+roofline of the sweep, GPU clocks sampled during the timed region, and the CPU
+oracle timed on a bounded sample (`cpu_baseline`).
+
+--impl reference times the CPU oracle (the only reference this method has) on a
+bounded sample of the same sweep, on the host cores, and prints the same line
+with "impl": "reference".
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+from dense_gemm_hgemm_gb300 import inputs, workloads  # noqa: E402
+
+METRIC = "GEMM TFLOPS and % of roofline per (M,N,K,dtype); µs/call at 64x4096x64 fp16"
+UNIT = "TFLOP/s"
+WORKLOAD = "hgemm_tn_fp16_sweep_343_shapes_M_N_K_in_64..4096"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+# --------------------------------------------------------------------------- helpers
+
+def parse_args(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=300)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--skip-extras", action="store_true",
+                    help="only the timed sweep (no e2e, named workloads or CPU baseline)")
+    ap.add_argument("--ncu-steps", type=int, default=0,
+                    help="run this many untimed steps and exit (for profiler launch lists)")
+    return ap.parse_args(argv)
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return {k: float(d[k]) for k in FALLBACK_PEAKS}, "measured"
+    except (OSError, KeyError, ValueError):
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+class Dist:
+    """Rank bookkeeping; torch.distributed only when launched with WORLD_SIZE > 1."""
+
+    def __init__(self, backend=None):
+        self.world = int(os.environ.get("WORLD_SIZE", "1"))
+        self.rank = int(os.environ.get("RANK", "0"))
+        self.local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+        self.pg = None
+        if self.world > 1:
+            import torch.distributed as dist
+            if backend is None:
+                backend = "nccl" if torch.cuda.is_available() else "gloo"
+            dist.init_process_group(backend=backend)
+            self.pg = dist
+            self.backend = backend
+
+    def barrier(self):
+        if self.pg is not None:
+            if self.backend == "nccl":
+                self.pg.barrier(device_ids=[self.local_rank])
+            else:
+                self.pg.barrier()
+
+    def max(self, x: float) -> float:
+        if self.pg is None:
+            return x
+        dev = "cuda" if self.backend == "nccl" else "cpu"
+        t = torch.tensor([x], dtype=torch.float64, device=dev)
+        self.pg.all_reduce(t, op=self.pg.ReduceOp.MAX)
+        return float(t.item())
+
+    def close(self):
+        if self.pg is not None:
+            self.pg.destroy_process_group()
+
+
+class ClockSampler:
+    """nvidia-smi clocks / throttle reasons sampled every 100 ms while running."""
+
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), "--query-gpu=" + self.QUERY,
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+        sm = [num(r[1]) for r in rows if num(r[1]) is not None]
+        mx = [num(r[2]) for r in rows if num(r[2]) is not None]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i] == "Active"})
+        power = [num(r[3]) for r in rows if num(r[3]) is not None]
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons,
+                "samples": len(rows), "power_w_max": max(power) if power else None}
+
+
+def source_digest() -> str:
+    """Hash of the kernel sources, to tell whether stored ncu counters still apply."""
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "dense_gemm_hgemm_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(name.encode())
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def stored_traffic():
+    """Per-launch DRAM bytes of the sweep from the committed ncu summary, if current."""
+    path = os.path.join(ROOT, "profiles", "sweep_f16_dram_traffic.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+    except (OSError, ValueError):
+        return None, "no committed ncu capture"
+    if d.get("source_digest") != source_digest():
+        return None, "kernel changed since the ncu capture"
+    return d.get("dram_bytes_per_launch"), "ncu capture %s" % d.get("when", "?")
+
+
+# --------------------------------------------------------------------------- our arm
+
+def make_sweep(device):
+    """Per-shape seeded operands on the device (own buffers per shape) and plans."""
+    import dense_gemm_hgemm_gb300 as g
+    shapes = workloads.sweep_shapes()
+    items = []
+    gen = torch.Generator(device=device)
+    for w in shapes:
+        gen.manual_seed(inputs.shape_seed(w.M, w.N, w.K, w.dtype))
+        A = torch.randn(w.M, w.K, generator=gen, device=device, dtype=torch.float32).half()
+        B = torch.randn(w.N, w.K, generator=gen, device=device, dtype=torch.float32).half()
+        C = torch.empty(w.M, w.N, device=device, dtype=torch.float16)
+        items.append((w, g.Plan(w.M, w.N, w.K, "f16"), A, B, C))
+    return items
+
+
+def run_step(items, stream):
+    for _, plan, A, B, C in items:
+        plan.run(A, B, C, stream)
+
+
+def time_sweep(items, dist, steps, warmup, stream, sampler=None):
+    for _ in range(warmup):
+        run_step(items, stream)
+    torch.cuda.synchronize()
+    dist.barrier()
+    torch.cuda.synchronize()
+    if sampler:
+        sampler.start()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    t0 = time.perf_counter()
+    e0.record(stream)
+    for _ in range(steps):
+        run_step(items, stream)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    wall = time.perf_counter() - t0
+    clocks = sampler.stop() if sampler else None
+    dist.barrier()
+    ms = e0.elapsed_time(e1)
+    return ms, wall, clocks
+
+
+def per_shape_times(items, stream, reps=3):
+    """Device time of every launch of one step (events around each launch), median of reps."""
+    res = {}
+    for _ in range(reps):
+        evs = []
+        for w, plan, A, B, C in items:
+            a = torch.cuda.Event(enable_timing=True)
+            b = torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            plan.run(A, B, C, stream)
+            b.record(stream)
+            evs.append((w, a, b))
+        torch.cuda.synchronize()
+        for w, a, b in evs:
+            res.setdefault(w.name, []).append(a.elapsed_time(b))
+    return {k: statistics.median(v) for k, v in res.items()}
+
+
+def e2e_sweep(items, stream, steps):
+    """The sweep through the public API with host operands: per shape H2D A, B
+    (pinned), gemm_run, D2H C, all on one stream, timed end to end."""
+    host = []
+    h2d = d2h = 0
+    for w, plan, A, B, C in items:
+        hA = torch.empty(A.shape, dtype=A.dtype, pin_memory=True)
+        hB = torch.empty(B.shape, dtype=B.dtype, pin_memory=True)
+        hC = torch.empty(C.shape, dtype=C.dtype, pin_memory=True)
+        hA.copy_(A)
+        hB.copy_(B)
+        host.append((hA, hB, hC))
+        h2d += A.numel() * 2 + B.numel() * 2
+        d2h += C.numel() * 2
+    torch.cuda.synchronize()
+
+    def one():
+        with torch.cuda.stream(stream):
+            for (w, plan, A, B, C), (hA, hB, hC) in zip(items, host):
+                A.copy_(hA, non_blocking=True)
+                B.copy_(hB, non_blocking=True)
+                plan.run(A, B, C, stream)
+                hC.copy_(C, non_blocking=True)
+
+    one()
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    t0 = time.perf_counter()
+    e0.record(stream)
+    for _ in range(steps):
+        one()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    wall = time.perf_counter() - t0
+    ms = max(e0.elapsed_time(e1), wall * 1e3) / steps
+    return ms, h2d, d2h
+
+
+def launch_floor_us(stream, sms, n=2000):
+    import dense_gemm_hgemm_gb300 as g
+    for _ in range(100):
+        g.gemm_launch_empty(sms, stream.cuda_stream)
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(n):
+        g.gemm_launch_empty(sms, stream.cuda_stream)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) * 1e3 / n
+
+
+def named_workloads(stream, peaks, floor_us, sms):
+    """Warm µs/call (back-to-back on the same buffers, median of 5 repeats of a
+    >= 20 ms loop) and TFLOP/s with the roofline fraction for each named shape;
+    cold µs/call (L2 flushed before every call) for the two skinny shapes."""
+    import dense_gemm_hgemm_gb300 as g
+    out = {}
+    flush = torch.empty(512 * 1024 * 1024, dtype=torch.uint8, device="cuda")
+    for w in workloads.NAMED:
+        gen = torch.Generator(device="cuda")
+        gen.manual_seed(inputs.shape_seed(w.M, w.N, w.K, w.dtype))
+        if w.dtype == "i8":
+            A = torch.randint(-128, 128, (w.M, w.K), generator=gen, device="cuda", dtype=torch.int8)
+            B = torch.randint(-128, 128, (w.N, w.K), generator=gen, device="cuda", dtype=torch.int8)
+        else:
+            td = inputs.TORCH_DTYPE[w.dtype]
+            A = (torch.randn(w.M, w.K, generator=gen, device="cuda") * w.a_scale).to(td)
+            B = (torch.randn(w.N, w.K, generator=gen, device="cuda") * w.b_scale).to(td)
+        C = torch.empty(w.M, w.N, device="cuda", dtype=inputs.OUT_DTYPE[w.dtype])
+        with g.Plan(w.M, w.N, w.K, w.dtype) as plan:
+            for _ in range(20):
+                plan.run(A, B, C, stream)
+            torch.cuda.synchronize()
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            plan.run(A, B, C, stream)
+            e1.record(stream)
+            torch.cuda.synchronize()
+            one = max(e0.elapsed_time(e1), 1e-3)
+            reps = max(10, min(5000, int(20.0 / one)))
+            samples = []
+            for _ in range(5):
+                e0.record(stream)
+                for _ in range(reps):
+                    plan.run(A, B, C, stream)
+                e1.record(stream)
+                torch.cuda.synchronize()
+                samples.append(e0.elapsed_time(e1) * 1e3 / reps)
+            us = statistics.median(samples)
+            cold = None
+            if w.flops < 1e9:
+                cs = []
+                for _ in range(30):
+                    with torch.cuda.stream(stream):
+                        flush.add_(1)      # 512 MB write evicts A, B, C from the 129 MB L2
+                    e0.record(stream)
+                    plan.run(A, B, C, stream)
+                    e1.record(stream)
+                    torch.cuda.synchronize()
+                    cs.append(e0.elapsed_time(e1) * 1e3)
+                cold = statistics.median(cs)
+            plan.check(stream)
+            cfg = plan.config
+        tflops = w.flops / (us * 1e-6) / 1e12
+        t_tensor = w.flops / (peaks["bf16_tflops"] * 1e12) * 1e6
+        t_hbm = w.compulsory_bytes / (peaks["hbm_gbs"] * 1e9) * 1e6
+        t_roof = max(t_tensor, t_hbm, floor_us)
+        bound = "tensor" if t_roof == t_tensor else ("hbm" if t_roof == t_hbm else "launch")
+        out[w.name] = {
+            "M": w.M, "N": w.N, "K": w.K, "dtype": w.dtype, "us_per_call": round(us, 3),
+            "us_per_call_cold_l2": round(cold, 3) if cold is not None else None,
+            ("TOPS" if w.dtype == "i8" else "TFLOPS"): round(tflops, 2),
+            "roofline_bound": bound, "roofline_us": round(t_roof, 3),
+            "roofline_frac": round(t_roof / us, 4),
+            "tensor_frac_of_measured_peak": round(tflops / peaks["bf16_tflops"], 4),
+            "config": cfg,
+        }
+        if w.dtype == "i8":
+            out[w.name]["note"] = ("int8 runs on the fp16 tensor path (sm_103a has no tcgen05 "
+                                   "kind::i8); peak is the fp16/bf16 rate")
+        del A, B, C
+    del flush
+    torch.cuda.empty_cache()
+    return out
+
+
+def cpu_oracle_sample(budget_s: float = 15.0, rows: int = 16):
+    """Time the CPU oracle on rows [0, rows) of the sweep's shapes, in seeded
+    random shape order, until `budget_s` seconds of work; TFLOP/s achieved."""
+    import numpy as np
+
+    import oracle
+    oracle.build()
+    shapes = workloads.sweep_shapes()
+    order = torch.randperm(len(shapes), generator=torch.Generator().manual_seed(7)).tolist()
+    flops = 0
+    elapsed = 0.0
+    done = 0
+    threads = oracle.max_threads()
+    for i in order:
+        w = shapes[i]
+        A, B = inputs.make_operands(min(rows, w.M), w.N, w.K, "f16")
+        a = A.view(torch.int16).numpy().view(np.uint16)
+        b = B.view(torch.int16).numpy().view(np.uint16)
+        t0 = time.perf_counter()
+        oracle.gemm_tn_half(a, b, 0, threads)
+        elapsed += time.perf_counter() - t0
+        flops += 2 * A.shape[0] * w.N * w.K
+        done += 1
+        if elapsed >= budget_s:
+            break
+    return {"value": flops / elapsed / 1e12, "unit": UNIT, "cores": threads, "kind": "oracle",
+            "sample": "rows [0,%d) of %d of the 343 sweep shapes (seeded order), %.3g FLOP, "
+                      "%.1f s" % (rows, done, flops, elapsed)}
+
+
+def ours(args):
+    dist = Dist()
+    torch.cuda.set_device(dist.local_rank)
+    import dense_gemm_hgemm_gb300 as g
+    g.build_library()
+    peaks, peak_src = load_peaks()
+    stream = torch.cuda.Stream()
+    sms = torch.cuda.get_device_properties(dist.local_rank).multi_processor_count
+    items = make_sweep("cuda")
+    flops_step = sum(w.flops for w, *_ in items)
+    bytes_step = sum(w.compulsory_bytes for w, *_ in items)
+    torch.cuda.synchronize()
+
+    if args.ncu_steps:
+        for _ in range(args.ncu_steps):
+            run_step(items, stream)
+        torch.cuda.synchronize()
+        for _, plan, *_ in items:
+            plan.check(stream)
+        return
+
+    sampler = ClockSampler(dist.local_rank)
+    ms, wall, clocks = time_sweep(items, dist, args.steps, args.warmup, stream, sampler)
+    for _, plan, *_ in items:
+        plan.check(stream)     # raises if any kernel gave up on a wait
+    ms_max = dist.max(ms)
+    ms_step = ms_max / args.steps
+    value = dist.world * flops_step / (ms_step * 1e-3) / 1e12
+    per_gpu = flops_step / (ms_step * 1e-3) / 1e12
+
+    line = {
+        "metric": METRIC, "value": round(value, 3), "unit": UNIT, "n_gpus": dist.world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f16",
+        "data": "synthetic (seeded N(0,1) fp16 operands per shape, generated on the device)",
+        "config": {"workload": WORKLOAD, "shapes": 343, "flop_per_step": flops_step,
+                   "compulsory_bytes_per_step": bytes_step,
+                   "l2": "inputs larger than L2: each shape has its own A, B, C "
+                         "(%.2f GB per step vs 129 MB L2); no explicit flush" % (bytes_step / 1e9),
+                   "replicas": dist.world, "layout": "TN", "accumulate": "fp32"},
+        "gpu_launches": len(items) * args.steps,
+        "clocks": clocks,
+        "wall_s_timed_region": round(wall, 3),
+    }
+    traffic, traffic_note = stored_traffic()
+    line["roofline"] = {
+        "bound": "tensor", "achieved": round(per_gpu, 2),
+        "peak": peaks["bf16_tflops_sustained"], "unit": "TFLOP/s",
+        "frac": round(per_gpu / peaks["bf16_tflops_sustained"], 4),
+        "traffic": traffic,
+        "peak_source": "bf16_tflops_sustained of %s (fp16 dense rate equals bf16)" % peak_src,
+        "frac_of_burst_peak": round(per_gpu / peaks["bf16_tflops"], 4),
+        "kernel": "gemm_tn_kernel (all sweep launches; average launch = step/343)",
+        "traffic_note": traffic_note,
+    }
+
+    if not args.skip_extras and dist.rank == 0:
+        floor = launch_floor_us(stream, sms)
+        times = per_shape_times(items, stream)
+        t_meas = t_roof = 0.0
+        classes = {}
+        for w, *_ in items:
+            us = times[w.name] * 1e3
+            tt = w.flops / (peaks["bf16_tflops"] * 1e12) * 1e6
+            th = w.compulsory_bytes / (peaks["hbm_gbs"] * 1e9) * 1e6
+            tr = max(tt, th, floor)
+            kind = "tensor" if tr == tt else ("hbm" if tr == th else "launch")
+            c = classes.setdefault(kind, {"shapes": 0, "t_meas_us": 0.0, "t_roof_us": 0.0})
+            c["shapes"] += 1
+            c["t_meas_us"] += us
+            c["t_roof_us"] += tr
+            t_meas += us
+            t_roof += tr
+        for c in classes.values():
+            c["frac"] = round(c["t_roof_us"] / c["t_meas_us"], 4)
+            c["t_meas_us"] = round(c["t_meas_us"], 1)
+            c["t_roof_us"] = round(c["t_roof_us"], 1)
+        head = workloads.HEADLINE_SWEEP.name.replace("hgemm_tn_", "sweep_").replace("_f16", "_f16")
+        line["sweep_roofline"] = {
+            "launch_floor_us": round(floor, 3),
+            "t_meas_us_sum": round(t_meas, 1), "t_roof_us_sum": round(t_roof, 1),
+            "frac": round(t_roof / t_meas, 4), "by_bound": classes,
+            "rule": "per shape t_roof = max(2MNK/bf16 burst peak, compulsory bytes/HBM, "
+                    "empty-kernel launch floor); per-launch device times from events",
+            "headline_128x2048x128_us_in_sweep": round(times.get("sweep_128x2048x128_f16", 0) * 1e3, 3),
+        }
+        e2e_ms, h2d, d2h = e2e_sweep(items, stream, steps=max(3, min(20, args.steps)))
+        line["e2e"] = {"value": round(flops_step / (e2e_ms * 1e-3) / 1e12, 3), "unit": UNIT,
+                       "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                       "ms_per_step": round(e2e_ms, 3)}
+        for _, plan, *_ in items:
+            plan.close()
+        del items
+        torch.cuda.empty_cache()
+        line["named"] = named_workloads(stream, peaks, floor, sms)
+        line["cpu_baseline"] = cpu_oracle_sample()
+    if dist.rank == 0:
+        print(json.dumps(line), flush=True)
+    dist.close()
+
+
+# --------------------------------------------------------------------------- reference arm
+
+def reference(args):
+    """The CPU oracle, as it stands, on a bounded sample of the sweep per step."""
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    import numpy as np
+
+    import oracle
+    oracle.build()
+    threads = oracle.max_threads()
+    shapes = workloads.sweep_shapes()
+    order = torch.randperm(len(shapes), generator=torch.Generator().manual_seed(7)).tolist()
+    rows = 16
+    cache = {}
+
+    def operands(i):
+        if i not in cache:
+            w = shapes[i]
+            A, B = inputs.make_operands(min(rows, w.M), w.N, w.K, "f16")
+            cache[i] = (w, A.view(torch.int16).numpy().view(np.uint16),
+                        B.view(torch.int16).numpy().view(np.uint16))
+        return cache[i]
+
+    def step(n):
+        w, a, b = operands(order[n % len(order)])
+        t0 = time.perf_counter()
+        oracle.gemm_tn_half(a, b, 0, threads)
+        return time.perf_counter() - t0, 2 * a.shape[0] * w.N * w.K
+
+    for n in range(args.warmup):
+        step(n)
+    el = 0.0
+    flops = 0
+    for n in range(args.warmup, args.warmup + args.steps):
+        dt, f = step(n)
+        el += dt
+        flops += f
+    value = flops / el / 1e12
+    sample = ("one sweep shape per step (seeded rotation over the 343), rows [0,%d) of A "
+              "against all of B; %.3g FLOP over %d steps" % (rows, flops, args.steps))
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "impl": "reference",
+        "n_gpus": int(os.environ.get("WORLD_SIZE", "1")), "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": el * 1e3 / max(1, args.steps), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "shapes": 343, "sample_rows_per_shape": rows},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main(argv=None):
+    args = parse_args(argv)
+    if args.warmup < 3 and not args.ncu_steps:
+        print("warning: fewer than 3 warm-up steps", file=sys.stderr)
+    if args.impl == "reference":
+        reference(args)
+    else:
+        ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -19,7 +19,7 @@ __all__ = [
     "build_library", "gemm_plan_create", "gemm_plan_create_with_config", "gemm_run",
     "gemm_plan_check", "gemm_plan_destroy", "gemm_plan_get_config", "gemm_plan_set_timeout",
     "gemm_select_config", "gemm_tile_coords", "gemm_workspace_bytes", "gemm_status_string",
-    "gemm_abi_version", "library", "DTYPES",
+    "gemm_abi_version", "gemm_launch_empty", "library", "DTYPES",
 ]
 
 GEMM_F16, GEMM_BF16, GEMM_I8_I32 = 0, 1, 2
@@ -79,6 +79,7 @@ def library() -> ctypes.CDLL:
                 "gemm_workspace_bytes": ([i64, i64, i64, i32, cfgp, ctypes.POINTER(ctypes.c_size_t)], i32),
                 "gemm_status_string": ([i32], ctypes.c_char_p),
                 "gemm_abi_version": ([], i32),
+                "gemm_launch_empty": ([i32, vp], i32),
             }
             for name, (args, res) in sig.items():
                 fn = getattr(lib, name)
@@ -133,6 +134,10 @@ def gemm_status_string(status: int) -> str:
 
 def gemm_abi_version() -> int:
     return int(library().gemm_abi_version())
+
+
+def gemm_launch_empty(grid: int, stream=None) -> None:
+    _check(library().gemm_launch_empty(int(grid), _stream(stream)), "gemm_launch_empty")
 
 
 def gemm_plan_create(M: int, N: int, K: int, dtype="f16", layout: int = GEMM_LAYOUT_TN) -> int:

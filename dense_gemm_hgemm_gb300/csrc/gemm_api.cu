@@ -475,4 +475,13 @@ const char* gemm_status_string(gemm_status_t s) {
 
 int32_t gemm_abi_version(void) { return GEMM_ABI_VERSION; }
 
+gemm_status_t gemm_launch_empty(int32_t grid, void* stream) {
+    if (grid < 1) return GEMM_ERR_INVALID_ARG;
+    if (gbg::launch_empty(grid, reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess) {
+        cudaGetLastError();
+        return GEMM_ERR_LAUNCH;
+    }
+    return GEMM_OK;
+}
+
 }  // extern "C"

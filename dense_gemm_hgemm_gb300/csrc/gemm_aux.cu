@@ -1,7 +1,8 @@
 // gemm_aux.cu -- small HBM-bound kernels around the GEMM:
 //   * widen_i8: int8 operands -> fp16 copies (every int8 value is exact in fp16),
 //     the input side of the integer mode of the tensor-core kernel;
-//   * zero_fill: C = 0 for K == 0 (the empty sum).
+//   * zero_fill: C = 0 for K == 0 (the empty sum);
+//   * empty: a kernel with no body, for measuring the launch-latency floor.
 // Both are grid-stride loops over 16-byte vectors sized to a whole number of
 // waves of the SMs.
 #include <cuda_fp16.h>
@@ -45,6 +46,8 @@ __global__ void __launch_bounds__(256) widen_i8_kernel(const int4* __restrict__ 
     }
 }
 
+__global__ void __launch_bounds__(192) empty_kernel() {}
+
 __global__ void __launch_bounds__(256) zero_fill_kernel(uint4* __restrict__ dst, int64_t n) {
     const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
     for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n; i += stride)
@@ -68,6 +71,11 @@ cudaError_t launch_widen_i8(const int8_t* a, int64_t na, const int8_t* b, int64_
     widen_i8_kernel<<<grid_for(ga + gb, num_sms), 256, 0, stream>>>(
         reinterpret_cast<const int4*>(a), ga, reinterpret_cast<const int4*>(b), gb,
         reinterpret_cast<uint4*>(a16), reinterpret_cast<uint4*>(b16));
+    return cudaGetLastError();
+}
+
+cudaError_t launch_empty(int grid, cudaStream_t stream) {
+    empty_kernel<<<grid, 192, 0, stream>>>();
     return cudaGetLastError();
 }
 

@@ -39,5 +39,6 @@ cudaError_t gemm_launch_i32(int bn, int stages, const LaunchShape&, const CUtens
 cudaError_t launch_widen_i8(const int8_t* a, int64_t na, const int8_t* b, int64_t nb, void* a16,
                             void* b16, int num_sms, cudaStream_t stream);
 cudaError_t launch_zero_fill(void* dst, int64_t bytes, int num_sms, cudaStream_t stream);
+cudaError_t launch_empty(int grid, cudaStream_t stream);
 
 }  // namespace gbg

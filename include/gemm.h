@@ -165,6 +165,13 @@ const char *gemm_status_string(gemm_status_t status);
 /* GEMM_ABI_VERSION of the built library. */
 int32_t gemm_abi_version(void);
 
+/*
+ * Measurement aid: queue one empty kernel of `grid` CTAs x 192 threads (the
+ * GEMM kernel's block size) on `stream`.  Back-to-back launches of it give the
+ * launch-latency floor that bounds the smallest GEMMs.
+ */
+gemm_status_t gemm_launch_empty(int32_t grid, void *stream);
+
 #ifdef __cplusplus
 }
 #endif
