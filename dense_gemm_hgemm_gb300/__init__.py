@@ -19,7 +19,7 @@ __all__ = [
     "build_library", "gemm_plan_create", "gemm_plan_create_with_config", "gemm_run",
     "gemm_plan_check", "gemm_plan_destroy", "gemm_plan_get_config", "gemm_plan_set_timeout",
     "gemm_select_config", "gemm_tile_coords", "gemm_workspace_bytes", "gemm_status_string",
-    "gemm_abi_version", "gemm_launch_empty", "library", "DTYPES",
+    "gemm_abi_version", "gemm_launch_empty", "gemm_run_splitk_noalloc", "library", "DTYPES",
 ]
 
 GEMM_F16, GEMM_BF16, GEMM_I8_I32 = 0, 1, 2
@@ -30,6 +30,7 @@ STATUS_NAMES = {
     0: "GEMM_OK", 1: "GEMM_ERR_INVALID_ARG", 2: "GEMM_ERR_UNSUPPORTED", 3: "GEMM_ERR_ALIGNMENT",
     4: "GEMM_ERR_NO_DEVICE", 5: "GEMM_ERR_ARCH", 6: "GEMM_ERR_OOM", 7: "GEMM_ERR_TENSORMAP",
     8: "GEMM_ERR_LAUNCH", 9: "GEMM_ERR_DEVICE_TIMEOUT", 10: "GEMM_ERR_CUDA",
+    11: "GEMM_ERR_SCRATCH_LIMIT",
 }
 
 
@@ -80,6 +81,7 @@ def library() -> ctypes.CDLL:
                 "gemm_status_string": ([i32], ctypes.c_char_p),
                 "gemm_abi_version": ([], i32),
                 "gemm_launch_empty": ([i32, vp], i32),
+                "gemm_run_splitk_noalloc": ([i64, i64, i64, i32, i32, vp, vp, vp, vp], i32),
             }
             for name, (args, res) in sig.items():
                 fn = getattr(lib, name)
@@ -138,6 +140,16 @@ def gemm_abi_version() -> int:
 
 def gemm_launch_empty(grid: int, stream=None) -> None:
     _check(library().gemm_launch_empty(int(grid), _stream(stream)), "gemm_launch_empty")
+
+
+def gemm_run_splitk_noalloc(M: int, N: int, K: int, dtype, split_k: int, A, B, C,
+                            stream=None) -> None:
+    """Split-K C = A @ B.T that allocates no device memory: its scratch is a fixed
+    16 MiB array inside the library (for callers that may not allocate; see
+    include/gemm.h for the size limit and the sharing rules)."""
+    _check(library().gemm_run_splitk_noalloc(M, N, K, _dtype_code(dtype), int(split_k), _ptr(A),
+                                             _ptr(B), _ptr(C), _stream(stream)),
+           "gemm_run_splitk_noalloc")
 
 
 def gemm_plan_create(M: int, N: int, K: int, dtype="f16", layout: int = GEMM_LAYOUT_TN) -> int:

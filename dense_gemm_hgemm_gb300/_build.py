@@ -18,7 +18,7 @@ BUILD_DIR = os.path.join(ROOT, "_build")
 LIB_PATH = os.path.join(PKG, "libgemm_gb300.so")
 
 SOURCES = ["gemm_api.cu", "gemm_aux.cu", "gemm_inst_f16.cu", "gemm_inst_bf16.cu",
-           "gemm_inst_i32.cu"]
+           "gemm_inst_i32.cu", "gemm_noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -469,6 +469,9 @@ const char* gemm_status_string(gemm_status_t s) {
         case GEMM_ERR_LAUNCH: return "GEMM_ERR_LAUNCH: kernel launch failed";
         case GEMM_ERR_DEVICE_TIMEOUT: return "GEMM_ERR_DEVICE_TIMEOUT: a kernel wait ran out";
         case GEMM_ERR_CUDA: return "GEMM_ERR_CUDA: CUDA runtime error";
+        case GEMM_ERR_SCRATCH_LIMIT:
+            return "GEMM_ERR_SCRATCH_LIMIT: split-K partials exceed the fixed 16 MiB scratch of "
+                   "gemm_run_splitk_noalloc";
         default: return "unknown gemm_status_t";
     }
 }

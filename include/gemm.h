@@ -69,7 +69,8 @@ typedef enum {
     GEMM_ERR_TENSORMAP = 7,       /* cuTensorMapEncodeTiled rejected a descriptor */
     GEMM_ERR_LAUNCH = 8,          /* kernel launch failed */
     GEMM_ERR_DEVICE_TIMEOUT = 9,  /* a kernel wait ran out (reported by gemm_plan_check) */
-    GEMM_ERR_CUDA = 10            /* any other CUDA runtime error */
+    GEMM_ERR_CUDA = 10,           /* any other CUDA runtime error */
+    GEMM_ERR_SCRATCH_LIMIT = 11   /* gemm_run_splitk_noalloc: problem exceeds its fixed scratch */
 } gemm_status_t;
 
 /*
@@ -171,6 +172,39 @@ int32_t gemm_abi_version(void);
  * launch-latency floor that bounds the smallest GEMMs.
  */
 gemm_status_t gemm_launch_empty(int32_t grid, void *stream);
+
+/*
+ * Split-K GEMM that allocates no device memory (no counterpart on the pages:
+ * this exists for callers that may not allocate -- plugins whose host framework
+ * owns all device memory and offers no allocator, services that reserve their
+ * memory budget up front, loops where cudaMalloc's possible device
+ * synchronisation or failure is not acceptable).
+ *
+ * Computes C = A * B^T exactly as gemm_run does for GEMM_F16 / GEMM_BF16 (same
+ * kernel, 128 x 64 output tiles, K cut into `split_k` slices summed in a fixed
+ * order), with the split-K partials, counters and error word in one fixed
+ * 16 MiB array compiled into the library instead of plan memory.  A, B, C are
+ * caller-owned device pointers with the gemm_run layout and alignment rules;
+ * no plan is needed.  split_k >= 1 (clamped to the number of 64-wide K blocks).
+ *
+ * Limit: with split_k > 1 the partials need ceil(M/128) * ceil(N/64) * split_k
+ * * 32 KiB <= 16 MiB - 32 KiB (at most 511 tile-slices) and at most 4096
+ * tiles; larger problems return GEMM_ERR_SCRATCH_LIMIT.  split_k == 1 needs no
+ * partials.  GEMM_I8_I32 returns GEMM_ERR_UNSUPPORTED.
+ *
+ * The array occupies 16 MiB on every GPU where the library's device code is
+ * loaded, until the process exits.  The first call on a device (that device
+ * current) looks up the array's device address (cudaGetSymbolAddress) and
+ * prepares the kernel; make it before any stream capture.  Every call clears
+ * the array's error word and counters on `stream`; all calls share the one
+ * array, so calls whose work overlaps on the GPU (different streams, or
+ * different host threads) race and must be serialised by the caller.  A wait
+ * that runs out is recorded in the array's error word only (no plan to check).
+ * Calls no cudaMalloc, cudaFree or allocating library routine.
+ */
+gemm_status_t gemm_run_splitk_noalloc(int64_t M, int64_t N, int64_t K, gemm_dtype_t dtype,
+                                      int32_t split_k, const void *A, const void *B, void *C,
+                                      void *stream);
 
 #ifdef __cplusplus
 }
