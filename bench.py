@@ -59,6 +59,8 @@ def parse_args(argv=None):
                     help="only the timed sweep (no e2e, named workloads or CPU baseline)")
     ap.add_argument("--ncu-steps", type=int, default=0,
                     help="run this many untimed steps and exit (for profiler launch lists)")
+    ap.add_argument("--shape", default=None,
+                    help="with --ncu-steps: run only this workload, 'M,N,K,dtype' (profiling)")
     return ap.parse_args(argv)
 
 
@@ -412,6 +414,27 @@ def cpu_oracle_sample(budget_s: float = 15.0, rows: int = 16):
                       "%.1f s" % (rows, done, flops, elapsed)}
 
 
+def profile_one(spec, calls, stream):
+    """`calls` launches of one shape with the table's configuration (for ncu)."""
+    import dense_gemm_hgemm_gb300 as g
+    M, N, K, dtype = spec.split(",")
+    M, N, K = int(M), int(N), int(K)
+    gen = torch.Generator(device="cuda")
+    gen.manual_seed(inputs.shape_seed(M, N, K, dtype))
+    if dtype == "i8":
+        A = torch.randint(-128, 128, (M, K), generator=gen, device="cuda", dtype=torch.int8)
+        B = torch.randint(-128, 128, (N, K), generator=gen, device="cuda", dtype=torch.int8)
+    else:
+        A = torch.randn(M, K, generator=gen, device="cuda").to(inputs.TORCH_DTYPE[dtype])
+        B = torch.randn(N, K, generator=gen, device="cuda").to(inputs.TORCH_DTYPE[dtype])
+    C = torch.empty(M, N, device="cuda", dtype=inputs.OUT_DTYPE[dtype])
+    with g.Plan(M, N, K, dtype) as plan:
+        for _ in range(calls):
+            plan.run(A, B, C, stream)
+        plan.check(stream)
+        print(json.dumps({"shape": [M, N, K, dtype], "config": plan.config, "calls": calls}))
+
+
 def ours(args):
     dist = Dist()
     torch.cuda.set_device(dist.local_rank)
@@ -420,6 +443,9 @@ def ours(args):
     peaks, peak_src = load_peaks()
     stream = torch.cuda.Stream()
     sms = torch.cuda.get_device_properties(dist.local_rank).multi_processor_count
+    if args.ncu_steps and args.shape:
+        profile_one(args.shape, args.ncu_steps, stream)
+        return
     items = make_sweep("cuda")
     flops_step = sum(w.flops for w, *_ in items)
     bytes_step = sum(w.compulsory_bytes for w, *_ in items)

@@ -88,6 +88,7 @@ gemm_status_t normalise_config(int64_t M, int64_t N, int64_t K, gemm_dtype_t dty
     if (c.stages == 0) c.stages = gbg::default_stages(c.block_n);
     if (c.stages != gbg::default_stages(c.block_n)) return GEMM_ERR_INVALID_ARG;
     if (c.split_k < 1 || c.raster_group < 1 || c.max_ctas < 0) return GEMM_ERR_INVALID_ARG;
+    if (c.split_mode != 0 && c.split_mode != 1) return GEMM_ERR_INVALID_ARG;
     const int64_t num_kb = (K + gbg::kBK - 1) / gbg::kBK;
     int64_t s = c.split_k;
     if (num_kb == 0) s = 1;
@@ -98,6 +99,11 @@ gemm_status_t normalise_config(int64_t M, int64_t N, int64_t K, gemm_dtype_t dty
     const int64_t n_blocks = (N + c.block_n - 1) / c.block_n;
     if (m_blocks * n_blocks * s > INT32_MAX) return GEMM_ERR_INVALID_ARG;
     c.split_k = static_cast<int32_t>(s);
+    if (c.split_k == 1) c.split_mode = 0;
+    // Cluster split: the slices of a tile share its 128 rows evenly (S | 128) and
+    // form a portable cluster (S <= 8).
+    if (c.split_mode == 1 && c.split_k != 2 && c.split_k != 4 && c.split_k != 8)
+        return GEMM_ERR_INVALID_ARG;
     if (c.raster_group > m_blocks && m_blocks > 0) c.raster_group = static_cast<int32_t>(m_blocks);
     *out = c;
     *kb_per_split = static_cast<int32_t>(per);
@@ -110,10 +116,11 @@ PlanMemory plan_memory(int64_t M, int64_t N, int64_t K, gemm_dtype_t dtype, cons
     m.error_off = off;
     off += kAlign;
     const int64_t tiles = ((M + gbg::kBM - 1) / gbg::kBM) * ((N + c.block_n - 1) / c.block_n);
+    const bool workspace = c.split_k > 1 && c.split_mode == 0;
     m.counters_off = off;
-    if (c.split_k > 1) off += round_up(static_cast<size_t>(tiles) * 4, kAlign);
+    if (workspace) off += round_up(static_cast<size_t>(tiles) * 4, kAlign);
     m.ws_off = off;
-    if (c.split_k > 1)
+    if (workspace)
         off += round_up(static_cast<size_t>(tiles) * c.split_k * gbg::kBM * c.block_n * 4, kAlign);
     m.a16_off = off;
     if (dtype == GEMM_I8_I32) off += round_up(static_cast<size_t>(M) * K * 2, kAlign);
@@ -244,6 +251,7 @@ gemm_status_t create_plan(int64_t M, int64_t N, int64_t K, gemm_dtype_t dtype,
     kp.m_blocks = static_cast<int32_t>((M + gbg::kBM - 1) / gbg::kBM);
     kp.n_blocks = static_cast<int32_t>((N + cfg.block_n - 1) / cfg.block_n);
     kp.split_k = cfg.split_k;
+    kp.cluster_split = cfg.split_mode == 1 ? 1 : 0;
     kp.kb_per_split = kb_per_split;
     // Integer mode: chunks of 8 k-blocks (512 products of magnitude <= 2^14, so
     // every fp32 partial sum is an integer of magnitude <= 2^23: exact).
@@ -263,6 +271,11 @@ gemm_status_t create_plan(int64_t M, int64_t N, int64_t K, gemm_dtype_t dtype,
 
     const int cap = cfg.max_ctas > 0 ? cfg.max_ctas : sms;
     p->shape.grid = kp.num_units < cap ? kp.num_units : cap;
+    p->shape.cluster = 1;
+    if (kp.cluster_split) {   // one unit per CTA, clusters of split_k CTAs
+        p->shape.grid = kp.num_units;
+        p->shape.cluster = cfg.split_k;
+    }
     if (p->shape.grid < 1) p->shape.grid = 1;
     p->shape.block = gbg::kThreads;
     p->shape.smem_bytes = smem;

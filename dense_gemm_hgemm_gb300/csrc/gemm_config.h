@@ -16,7 +16,7 @@ namespace gbg {
 
 struct TableEntry {
     int32_t M, N, K, dtype;
-    int32_t block_n, split_k, raster_group;
+    int32_t block_n, split_k, raster_group, split_mode;
 };
 
 #include "gemm_config_table.inc"   // static const TableEntry kTunedTable[]; kTunedCount
@@ -35,6 +35,7 @@ inline gemm_config_t model_config(int64_t M, int64_t N, int64_t K, gemm_dtype_t 
     c.max_ctas = 0;
     c.raster_group = 16;
     c.split_k = 1;
+    c.split_mode = 0;
     const int64_t mb = ceil_div(M, kBM);
     const int64_t num_kb = ceil_div(K, kBK);
     const int cands_f[3] = {256, 128, 64};
@@ -53,14 +54,18 @@ inline gemm_config_t model_config(int64_t M, int64_t N, int64_t K, gemm_dtype_t 
             c.block_n = bn;
         }
     }
-    // Few output tiles and a long K: slice K so that more SMs take part.
+    // Few output tiles and a long K: one SM streams only ~110 GB/s, so slice K
+    // over a cluster of 2/4/8 CTAs per tile (reduced in distributed shared memory).
     const int64_t tiles = mb * ceil_div(N, c.block_n);
     if (tiles * 2 <= sms && num_kb >= 8) {
-        int64_t s = sms / tiles;
-        if (s > num_kb / 4) s = num_kb / 4;
-        if (s > 16) s = 16;
-        if (s < 1) s = 1;
-        c.split_k = static_cast<int32_t>(s);
+        for (int s = 8; s >= 2; s /= 2) {
+            const int64_t per = ceil_div(num_kb, s);
+            if (tiles * s <= sms && num_kb >= 2 * s && ceil_div(num_kb, per) == s) {
+                c.split_k = s;
+                c.split_mode = 1;
+                break;
+            }
+        }
     }
     return c;
 }
@@ -74,6 +79,7 @@ inline gemm_config_t select_config(int64_t M, int64_t N, int64_t K, gemm_dtype_t
             c.stages = 0;
             c.split_k = e.split_k;
             c.raster_group = e.raster_group;
+            c.split_mode = e.split_mode;
             c.max_ctas = 0;
             return c;
         }

@@ -22,8 +22,22 @@ cudaError_t launch_one(const LaunchShape& s, const CUtensorMap& a, const CUtenso
     cfg.blockDim = dim3(static_cast<unsigned>(s.block));
     cfg.dynamicSmemBytes = s.smem_bytes;
     cfg.stream = stream;
-    cfg.attrs = nullptr;
-    cfg.numAttrs = 0;
+    // Programmatic dependent launch: this kernel's set-up may overlap the tail
+    // of the previous kernel in the stream (the kernel waits on it with
+    // griddepcontrol.wait before touching global memory).
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    unsigned n = 1;
+    if (s.cluster > 1) {   // split-K slices of a tile as one cluster
+        attr[1].id = cudaLaunchAttributeClusterDimension;
+        attr[1].val.clusterDim.x = static_cast<unsigned>(s.cluster);
+        attr[1].val.clusterDim.y = 1;
+        attr[1].val.clusterDim.z = 1;
+        n = 2;
+    }
+    cfg.attrs = attr;
+    cfg.numAttrs = n;
     return cudaLaunchKernelEx(&cfg, gemm_tn_kernel<BN, STAGES, kOutF16>, a, b, p);
 }
 

@@ -308,6 +308,140 @@ __device__ __forceinline__ void store_ws32(uint32_t* dst, const uint32_t* v) {
                make_uint4(v[g * 4 + 0], v[g * 4 + 1], v[g * 4 + 2], v[g * 4 + 3]));
 }
 
+template <int OUT>
+__device__ __forceinline__ void add_u4(uint32_t* v, const uint4& q) {
+    if constexpr (OUT == kOutI32) {   // integer partials: wrap-around sums (mod 2^32)
+        v[0] += q.x;
+        v[1] += q.y;
+        v[2] += q.z;
+        v[3] += q.w;
+    } else {
+        v[0] = __float_as_uint(__uint_as_float(v[0]) + __uint_as_float(q.x));
+        v[1] = __float_as_uint(__uint_as_float(v[1]) + __uint_as_float(q.y));
+        v[2] = __float_as_uint(__uint_as_float(v[2]) + __uint_as_float(q.z));
+        v[3] = __float_as_uint(__uint_as_float(v[3]) + __uint_as_float(q.w));
+    }
+}
+
+// v = sum over K slices s = 0..S-1 (in that order) of 32 partial values at
+// src + s*slice_stride.  G slices' loads are issued before any is added, so
+// G x 128 bytes per thread are in flight.
+template <int OUT, int G>
+__device__ __forceinline__ void reduce_slices32(const uint32_t* src, int64_t slice_stride,
+                                                int32_t S, uint32_t (&v)[32]) {
+#pragma unroll
+    for (int i = 0; i < 32; ++i) v[i] = 0u;   // +0.0f and integer 0 share the bit pattern
+    for (int32_t s0 = 0; s0 < S; s0 += G) {
+        uint4 q[G][8];
+#pragma unroll
+        for (int t = 0; t < G; ++t) {
+            if (s0 + t < S) {
+                const uint32_t* slice = src + (s0 + t) * slice_stride;
+#pragma unroll
+                for (int g = 0; g < 8; ++g) q[t][g] = ld_cg_u4(slice + g * 4);
+            }
+        }
+#pragma unroll
+        for (int t = 0; t < G; ++t) {
+            if (s0 + t < S) {
+#pragma unroll
+                for (int g = 0; g < 8; ++g) add_u4<OUT>(&v[g * 4], q[t][g]);
+            }
+        }
+    }
+}
+
+// ---- thread-block cluster / distributed shared memory
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+// Shared::cluster address of the same offset in CTA `rank` of this cluster.
+__device__ __forceinline__ uint32_t map_to_rank(uint32_t saddr, uint32_t rank) {
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(saddr), "r"(rank));
+    return r;
+}
+__device__ __forceinline__ uint4 ld_dsmem_u4(uint32_t cluster_addr) {
+    uint4 v;
+    asm volatile("ld.shared::cluster.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "r"(cluster_addr)
+                 : "memory");
+    return v;
+}
+__device__ __forceinline__ void st_shared_u4(uint32_t saddr, uint4 v) {
+    asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(saddr), "r"(v.x), "r"(v.y),
+                 "r"(v.z), "r"(v.w)
+                 : "memory");
+}
+// All threads of all CTAs of the cluster; release/acquire orders shared memory.
+__device__ __forceinline__ void cluster_sync_all() {
+    asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+    asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void fence_proxy_async_smem() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// Partial tile staged in shared memory for the cluster reduction: 128 rows of
+// BN 32-bit values, row stride BN+4 words (keeps the row-per-thread writes of a
+// warp on distinct banks).
+template <int BN>
+__device__ __forceinline__ void stage_row32(uint32_t staging, int row, int col, const uint32_t* v) {
+    const uint32_t base = staging + static_cast<uint32_t>((row * (BN + 4) + col) * 4);
+#pragma unroll
+    for (int g = 0; g < 8; ++g)
+        st_shared_u4(base + g * 16, make_uint4(v[g * 4 + 0], v[g * 4 + 1], v[g * 4 + 2], v[g * 4 + 3]));
+}
+
+// CTA `rank` of the cluster owns rows [rank*128/S, (rank+1)*128/S) of the tile:
+// for each 4-column group it sums the S staged partials in slice order 0..S-1
+// (read from every CTA's shared memory) and stores the converted result.
+template <int BN, int OUT>
+__device__ __forceinline__ void cluster_reduce_store(const KParams& p, const UnitCoord& c,
+                                                     uint32_t staging, int tid, int nthreads) {
+    const int S = p.split_k;
+    const uint32_t rank = cluster_ctarank();
+    const int rows = kBM / S;
+    const int r0 = static_cast<int>(rank) * rows;
+    constexpr int kVec = BN / 4;
+    for (int t = tid; t < rows * kVec; t += nthreads) {
+        const int rr = r0 + t / kVec;
+        const int c4 = (t % kVec) * 4;
+        const int32_t grow = c.m_blk * kBM + rr;
+        const int32_t gcol = c.n_blk * BN + c4;
+        if (grow >= p.M || gcol >= p.N) continue;
+        const uint32_t off = staging + static_cast<uint32_t>((rr * (BN + 4) + c4) * 4);
+        uint4 q[8];
+#pragma unroll
+        for (int s = 0; s < 8; ++s)
+            if (s < S) q[s] = ld_dsmem_u4(map_to_rank(off, static_cast<uint32_t>(s)));
+        uint32_t v[4] = {0u, 0u, 0u, 0u};
+#pragma unroll
+        for (int s = 0; s < 8; ++s)
+            if (s < S) add_u4<OUT>(v, q[s]);
+        const int64_t idx = static_cast<int64_t>(grow) * p.N + gcol;
+        if constexpr (OUT == kOutI32) {
+            *reinterpret_cast<uint4*>(reinterpret_cast<uint32_t*>(p.C) + idx) =
+                make_uint4(v[0], v[1], v[2], v[3]);
+        } else {
+            uint2 h;
+            h.x = pack2<OUT>(__uint_as_float(v[0]), __uint_as_float(v[1]));
+            h.y = pack2<OUT>(__uint_as_float(v[2]), __uint_as_float(v[3]));
+            *reinterpret_cast<uint2*>(reinterpret_cast<uint16_t*>(p.C) + idx) = h;
+        }
+    }
+}
+
+__device__ __forceinline__ void grid_dependency_wait() {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+__device__ __forceinline__ void grid_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // ----------------------------------------------------------------------------
 // the kernel
 // ----------------------------------------------------------------------------
@@ -355,6 +489,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem_base = ctl->tmem_base;
+    // Programmatic dependent launch: the set-up above may overlap the previous
+    // kernel of the stream; no global memory is touched before that kernel has
+    // completed and its writes are visible.  The next kernel may be scheduled
+    // from here on (it waits the same way before reading anything we write).
+    grid_dependency_wait();
+    grid_launch_dependents();
     const Watch watch{&ctl->abort, p.error_word, p.timeout_ns};
 
     if (warp == 0) {
@@ -467,7 +607,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                                            p.n_blocks, p.raster_group);
             const int32_t row = c.m_blk * kBM + row_in_tile;
             const int32_t col0 = c.n_blk * BN;
-            const bool split = p.split_k > 1;
+            const bool split = p.split_k > 1 && !p.cluster_split;
+            const bool cluster = p.cluster_split != 0;
+            if (cluster) fence_proxy_async_smem();   // the ring becomes the staging buffer
             uint32_t* ws_row = nullptr;
             if (split)
                 ws_row = reinterpret_cast<uint32_t*>(p.workspace) +
@@ -504,8 +646,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (!ok) break;
 #pragma unroll
                 for (int j = 0; j < BN / 32; ++j) {
-                    if (split) {
-                        store_ws32(ws_row + j * 32, &sum[j * 32]);
+                    if (cluster) {
+                        stage_row32<BN>(ring, row_in_tile, j * 32, &sum[j * 32]);
+                    } else if (split) {
+                        if (row < p.M) store_ws32(ws_row + j * 32, &sum[j * 32]);
                     } else if (row < p.M) {
                         store_i32_row32(p.C, p.N, row, col0 + j * 32, &sum[j * 32]);
                     }
@@ -524,8 +668,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                     uint32_t v[32];
                     tmem_ld_32x32b_x32(tmem_base + lane_addr + buf * BN + j * 32, v);
                     tmem_ld_wait();
-                    if (split) {
-                        store_ws32(ws_row + j * 32, v);
+                    if (cluster) {
+                        stage_row32<BN>(ring, row_in_tile, j * 32, v);
+                    } else if (split) {
+                        if (row < p.M) store_ws32(ws_row + j * 32, v);
                     } else if (row < p.M) {
                         store_half_row32<OUT>(p.C, p.N, row, col0 + j * 32, v);
                     }
@@ -539,6 +685,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (split) {
                 // Publish this slice; the last slice to arrive sums all slices in
                 // slice order 0..S-1 (fixed order: identical results every run).
+                // Rows beyond M are neither written nor read.
                 __threadfence();
                 named_bar_sync(1, kEpiWarps * 32);
                 if (epi_tid == 0) {
@@ -558,31 +705,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll 1
                     for (int j = 0; j < BN / 32; ++j) {
                         uint32_t v[32];
-                        if constexpr (OUT == kOutI32) {
-#pragma unroll
-                            for (int i = 0; i < 32; ++i) v[i] = 0u;
-                        } else {
-#pragma unroll
-                            for (int i = 0; i < 32; ++i) v[i] = __float_as_uint(0.0f);
-                        }
-                        for (int32_t s = 0; s < p.split_k; ++s) {
-                            const uint32_t* src = tile_ws + s * slice_stride + j * 32;
-#pragma unroll
-                            for (int g = 0; g < 8; ++g) {
-                                const uint4 q = ld_cg_u4(src + g * 4);
-                                if constexpr (OUT == kOutI32) {
-                                    v[g * 4 + 0] += q.x;
-                                    v[g * 4 + 1] += q.y;
-                                    v[g * 4 + 2] += q.z;
-                                    v[g * 4 + 3] += q.w;
-                                } else {
-                                    v[g * 4 + 0] = __float_as_uint(__uint_as_float(v[g * 4 + 0]) + __uint_as_float(q.x));
-                                    v[g * 4 + 1] = __float_as_uint(__uint_as_float(v[g * 4 + 1]) + __uint_as_float(q.y));
-                                    v[g * 4 + 2] = __float_as_uint(__uint_as_float(v[g * 4 + 2]) + __uint_as_float(q.z));
-                                    v[g * 4 + 3] = __float_as_uint(__uint_as_float(v[g * 4 + 3]) + __uint_as_float(q.w));
-                                }
-                            }
-                        }
+                        // integer mode keeps its BN int32 sums live: fewer loads in flight
+                        reduce_slices32<OUT, (OUT == kOutI32 ? 2 : 4)>(tile_ws + j * 32,
+                                                                       slice_stride, p.split_k, v);
                         if constexpr (OUT == kOutI32) {
                             store_i32_row32(p.C, p.N, row, col0 + j * 32, v);
                         } else {
@@ -592,6 +717,18 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             }
         }
+    }
+
+    // ------------------------------------------- split-K reduction in the cluster
+    if (p.cluster_split) {
+        cluster_sync_all();   // every CTA of the cluster has staged its slice
+        if (warp >= 2) {
+            const UnitCoord c = unit_coord(blockIdx.x, p.split_k, p.kb_per_split, p.num_kb,
+                                           p.m_blocks, p.n_blocks, p.raster_group);
+            cluster_reduce_store<BN, OUT>(p, c, ring, static_cast<int>(threadIdx.x) - 64,
+                                          kEpiWarps * 32);
+        }
+        cluster_sync_all();   // no CTA leaves while its shared memory may still be read
     }
 
     // ---------------------------------------------------------------- teardown

@@ -26,6 +26,9 @@ struct KParams {
     int32_t num_kb;         // ceil(K / kBK)
     int32_t m_blocks, n_blocks;
     int32_t split_k;        // K slices per tile
+    int32_t cluster_split;  // 1: the split_k slices of a tile form one thread-block
+                            // cluster and are reduced through distributed shared
+                            // memory (one unit per CTA); 0: workspace + last arriver
     int32_t kb_per_split;   // k-blocks per slice
     int32_t chunk_kb;       // k-blocks per accumulation chunk (integer mode), else >= kb_per_split
     int32_t raster_group;

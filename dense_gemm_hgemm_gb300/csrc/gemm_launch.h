@@ -15,6 +15,7 @@ struct LaunchShape {
     int grid;
     int block;
     size_t smem_bytes;
+    int cluster = 1;   // CTAs per thread-block cluster (x dimension)
 };
 
 // Kernel variant lookup.  `out` is kOutF16 / kOutBF16 / kOutI32.  Returns

@@ -82,6 +82,11 @@ typedef enum {
  *                  in a fixed order, so results are run-to-run identical
  *   raster_group : m-blocks per band of the L2-friendly tile order (>= 1)
  *   max_ctas     : persistent grid cap; 0 = one CTA per SM
+ *   split_mode   : how K slices are combined when split_k > 1:
+ *                  0 = partials in plan memory, summed by the last slice to finish;
+ *                  1 = the slices of a tile run as one thread-block cluster and are
+ *                      summed through distributed shared memory (split_k must
+ *                      come out as 2, 4 or 8; one tile slice per CTA, no scratch)
  */
 typedef struct {
     int32_t block_n;
@@ -89,6 +94,7 @@ typedef struct {
     int32_t split_k;
     int32_t raster_group;
     int32_t max_ctas;
+    int32_t split_mode;
 } gemm_config_t;
 
 typedef struct gemm_plan *gemm_plan_t;

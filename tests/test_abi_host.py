@@ -113,6 +113,18 @@ def test_select_config_splits_k_for_few_tiles(gemm_lib):
     assert c["split_k"] > 1
 
 
+def test_cluster_split_validation(gemm_lib):
+    ok = gemm_lib.gemm_workspace_bytes(128, 128, 4096, "f16",
+                                       {"block_n": 64, "split_k": 4, "split_mode": 1})
+    base = gemm_lib.gemm_workspace_bytes(128, 128, 4096, "f16", {"block_n": 64, "split_k": 1})
+    assert ok == base                      # cluster split needs no plan scratch
+    for bad in ({"block_n": 64, "split_k": 3, "split_mode": 1},      # 128 rows / 3
+                {"block_n": 64, "split_k": 16, "split_mode": 1},     # beyond a portable cluster
+                {"block_n": 64, "split_k": 2, "split_mode": 7}):
+        with pytest.raises(gemm_lib.GemmError):
+            gemm_lib.gemm_workspace_bytes(128, 128, 4096, "f16", bad)
+
+
 @pytest.mark.parametrize("mb,nb,g", [(1, 1, 1), (7, 3, 2), (64, 32, 16), (33, 57, 8), (5, 9, 16)])
 def test_raster_is_a_bijection(gemm_lib, mb, nb, g):
     seen = set()
@@ -157,3 +169,24 @@ def test_product_path_has_no_oracle_or_fallback():
             if f.endswith((".py", ".cu", ".cuh", ".h", ".inc")):
                 text = open(os.path.join(dirpath, f), encoding="utf-8").read()
                 assert not banned.search(text), (f, banned.search(text).group(0))
+
+
+def test_config_table_is_the_emitted_sweep(tmp_path):
+    """csrc/gemm_config_table.inc is exactly what tune.py emits from tuned_configs.json."""
+    from dense_gemm_hgemm_gb300 import tune
+    out = tmp_path / "table.inc"
+    tune.emit(tune.TUNED_JSON, str(out))
+    assert out.read_text() == open(tune.TABLE).read()
+
+
+def test_table_covers_the_sweep_and_named_shapes(gemm_lib):
+    import json
+    from dense_gemm_hgemm_gb300 import tune
+    doc = json.load(open(tune.TUNED_JSON))
+    have = {(r["M"], r["N"], r["K"], r["dtype"]) for r in doc["shapes"]}
+    for w in list(workloads.sweep_shapes()) + list(workloads.NAMED):
+        assert (w.M, w.N, w.K, w.dtype) in have
+    for r in doc["shapes"]:
+        c = gemm_lib.gemm_select_config(r["M"], r["N"], r["K"], r["dtype"], 152)
+        for k, v in r["best"].items():
+            assert c[k] == v or (k == "raster_group" and c[k] <= v), (r, c)

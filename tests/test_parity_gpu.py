@@ -74,6 +74,24 @@ def test_split_k_parity_and_determinism(shape, split):
     assert torch.equal(C1.view(torch.int16), C2.view(torch.int16))
 
 
+@pytest.mark.parametrize("dtype", ["f16", "bf16", "i8"])
+@pytest.mark.parametrize("split", [2, 4, 8])
+@pytest.mark.parametrize("shape", [(128, 128, 4096), (200, 136, 1024), (64, 64, 2048),
+                                   (384, 264, 512)], ids=lambda s: "x".join(map(str, s)))
+def test_cluster_split_k_parity_and_determinism(shape, split, dtype):
+    """Split-K whose slices form one thread-block cluster per tile, reduced in
+    distributed shared memory in slice order."""
+    M, N, K = shape
+    A, B = inputs.make_operands(M, N, K, dtype)
+    for bn in ((64, 128) if dtype == "i8" else (64, 256)):
+        cfg = {"block_n": bn, "split_k": split, "split_mode": 1}
+        C1 = pu.run_gpu(A, B, dtype, cfg, repeats=3)
+        pu.check_full(A, B, dtype, C1, "cluster split %d bn=%d %s %s" % (split, bn, shape, dtype))
+        C2 = pu.run_gpu(A, B, dtype, cfg)
+        assert torch.equal(C1.view(torch.int16) if dtype != "i8" else C1,
+                           C2.view(torch.int16) if dtype != "i8" else C2)
+
+
 def test_default_config_headline_shapes():
     for w in (workloads.SKINNY, workloads.HEADLINE_SWEEP):
         A, B = inputs.make_operands(w.M, w.N, w.K, w.dtype, w.a_scale, w.b_scale)
