@@ -50,8 +50,9 @@ struct gemm_plan {
     void* d_b16;
     const void* map_a_src;      // tensor-map cache keys
     const void* map_b_src;
-    bool map_a_valid, map_b_valid;
-    CUtensorMap map_a, map_b;
+    const void* map_c_src;
+    bool map_a_valid, map_b_valid, map_c_valid;
+    CUtensorMap map_a, map_b, map_c;
 };
 
 namespace {
@@ -158,6 +159,26 @@ gemm_status_t encode_kmajor(CUtensorMap* map, const void* base, int64_t rows, in
     const CUresult r = fn(map, dt, 2, const_cast<void*>(base), dims, strides, box, estr,
                           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? GEMM_OK : GEMM_ERR_TENSORMAP;
+}
+
+// 2-D map over the M x N row-major C for the epilogue's TMA stores: box = one
+// 128-byte row segment (64 16-bit or 32 32-bit values) x 32 rows, 128-byte
+// swizzle (the layout the epilogue writes its store buffers in).
+gemm_status_t encode_output(CUtensorMap* map, void* base, int64_t M, int64_t N, gemm_dtype_t dt) {
+    PFN_cuTensorMapEncodeTiled_v12000 fn = encode_fn();
+    if (!fn) return GEMM_ERR_TENSORMAP;
+    const int esize = dt == GEMM_I8_I32 ? 4 : 2;
+    const CUtensorMapDataType t = dt == GEMM_I8_I32 ? CU_TENSOR_MAP_DATA_TYPE_INT32
+                                  : dt == GEMM_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                                    : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(N), static_cast<cuuint64_t>(M)};
+    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(N) * esize};
+    const cuuint32_t box[2] = {static_cast<cuuint32_t>(128 / esize), 32};
+    const cuuint32_t estr[2] = {1, 1};
+    const CUresult r = fn(map, t, 2, base, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                          CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS ? GEMM_OK : GEMM_ERR_TENSORMAP;
 }
 
@@ -309,12 +330,12 @@ cudaError_t gemm_prepare(int bn, int stages, int out, size_t* smem_bytes) {
 }
 
 cudaError_t gemm_launch(int bn, int stages, int out, const LaunchShape& shape,
-                        const CUtensorMap& a, const CUtensorMap& b, const KParams& p,
-                        cudaStream_t stream) {
+                        const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& c,
+                        const KParams& p, cudaStream_t stream) {
     switch (out) {
-        case kOutF16: return gemm_launch_f16(bn, stages, shape, a, b, p, stream);
-        case kOutBF16: return gemm_launch_bf16(bn, stages, shape, a, b, p, stream);
-        case kOutI32: return gemm_launch_i32(bn, stages, shape, a, b, p, stream);
+        case kOutF16: return gemm_launch_f16(bn, stages, shape, a, b, c, p, stream);
+        case kOutBF16: return gemm_launch_bf16(bn, stages, shape, a, b, c, p, stream);
+        case kOutI32: return gemm_launch_i32(bn, stages, shape, a, b, c, p, stream);
         default: return cudaErrorInvalidValue;
     }
 }
@@ -383,9 +404,16 @@ gemm_status_t gemm_run(gemm_plan_t p, const void* A, const void* B, void* C, voi
             p->map_b_valid = true;
         }
     }
+    if (!p->map_c_valid || p->map_c_src != C) {
+        p->map_c_valid = false;
+        const gemm_status_t st = encode_output(&p->map_c, C, p->M, p->N, p->dtype);
+        if (st != GEMM_OK) return st;
+        p->map_c_src = C;
+        p->map_c_valid = true;
+    }
     p->kp.C = C;
     if (gbg::gemm_launch(p->cfg.block_n, p->cfg.stages, p->out_kind, p->shape, p->map_a, p->map_b,
-                         p->kp, stream) != cudaSuccess) {
+                         p->map_c, p->kp, stream) != cudaSuccess) {
         cudaGetLastError();
         return GEMM_ERR_LAUNCH;
     }

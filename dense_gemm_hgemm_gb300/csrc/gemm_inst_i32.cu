@@ -16,7 +16,7 @@ cudaError_t prepare_one(size_t* smem_bytes) {
 
 template <int BN, int STAGES>
 cudaError_t launch_one(const LaunchShape& s, const CUtensorMap& a, const CUtensorMap& b,
-                       const KParams& p, cudaStream_t stream) {
+                       const CUtensorMap& c, const KParams& p, cudaStream_t stream) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(s.grid));
     cfg.blockDim = dim3(static_cast<unsigned>(s.block));
@@ -38,7 +38,7 @@ cudaError_t launch_one(const LaunchShape& s, const CUtensorMap& a, const CUtenso
     }
     cfg.attrs = attr;
     cfg.numAttrs = n;
-    return cudaLaunchKernelEx(&cfg, gemm_tn_kernel<BN, STAGES, kOutI32>, a, b, p);
+    return cudaLaunchKernelEx(&cfg, gemm_tn_kernel<BN, STAGES, kOutI32>, a, b, c, p);
 }
 
 }  // namespace
@@ -52,9 +52,10 @@ cudaError_t gemm_prepare_i32(int bn, int stages, size_t* smem_bytes) {
 }
 
 cudaError_t gemm_launch_i32(int bn, int stages, const LaunchShape& s, const CUtensorMap& a,
-                             const CUtensorMap& b, const KParams& p, cudaStream_t stream) {
+                             const CUtensorMap& b, const CUtensorMap& c, const KParams& p,
+                             cudaStream_t stream) {
 #define X(B, S) \
-    if (bn == B && stages == S) return launch_one<B, S>(s, a, b, p, stream);
+    if (bn == B && stages == S) return launch_one<B, S>(s, a, b, c, p, stream);
     X(64, 8) X(128, 6)
 #undef X
     return cudaErrorInvalidValue;

@@ -50,8 +50,14 @@ struct SmemLayout {
     static constexpr int kBTileBytes = BN * kBK * 2;
     static constexpr int kStageBytes = kATileBytes + kBTileBytes;
     static constexpr int kRingBytes = STAGES * kStageBytes;
+    // Epilogue staging for TMA stores: per epilogue warp two 32-row x 128-byte
+    // buffers (128-byte swizzle, 1024-byte aligned).
+    static constexpr int kStoreBufBytes = 32 * 128;
+    static constexpr int kStagingBytes = kEpiWarps * 2 * kStoreBufBytes;
     static constexpr int kCtlBytes = 256;
-    static constexpr int kTotal = 1024 /* alignment slack */ + kRingBytes + kCtlBytes;
+    static constexpr int kTotal =
+        1024 /* alignment slack */ + kRingBytes + kStagingBytes + kCtlBytes;
+    static_assert(kTotal <= 232448, "exceeds the 227 KiB a CTA may use");
     static_assert(kBTileBytes % 1024 == 0, "128B-swizzle tiles must stay 1024-byte aligned");
     static_assert(STAGES * 16 + 5 * 8 + 16 <= kCtlBytes, "control block overflow");
 };
@@ -173,6 +179,35 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map
         " [%0], [%1, {%3, %4}], [%2];" ::"r"(dst),
         "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(x), "r"(y)
         : "memory");
+}
+
+// Warm L2 with a tile a later tma_load_2d will read (no shared memory, no barrier).
+__device__ __forceinline__ void tma_prefetch_l2_2d(const CUtensorMap* map, int32_t x, int32_t y) {
+    asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(
+                     reinterpret_cast<uint64_t>(map)),
+                 "r"(x), "r"(y)
+                 : "memory");
+}
+
+// Shared -> global tiled store, tracked by the issuing thread's bulk async-group.
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, uint32_t src, int32_t x,
+                                             int32_t y) {
+    asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];" ::"l"(
+                     reinterpret_cast<uint64_t>(map)),
+                 "r"(src), "r"(x), "r"(y)
+                 : "memory");
+}
+__device__ __forceinline__ void bulk_commit_group() {
+    asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+// Wait until at most N committed groups still read their shared-memory source.
+template <int N>
+__device__ __forceinline__ void bulk_wait_group_read() {
+    asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
+}
+// Wait until all committed groups have completed (writes performed).
+__device__ __forceinline__ void bulk_wait_group_all() {
+    asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
 }
 
 __device__ __forceinline__ void tc_fence_before() {
@@ -442,13 +477,29 @@ __device__ __forceinline__ void grid_launch_dependents() {
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
+// Write `nchunks` 16-byte chunks (4 words each) of row `row` of a 32-row x
+// 128-byte store buffer, starting at logical chunk c0, in the 128-byte swizzle
+// the C tensor map uses (chunk c of row r sits at chunk c ^ (r & 7)): the 8
+// rows of a quarter-warp hit 8 distinct bank groups.
+__device__ __forceinline__ void stage_store_row(uint32_t buf, int row, int c0, const uint32_t* w,
+                                                int nchunks) {
+    const uint32_t row_base = buf + static_cast<uint32_t>(row) * 128u;
+#pragma unroll
+    for (int i = 0; i < nchunks; ++i) {
+        const uint32_t chunk = static_cast<uint32_t>((c0 + i) ^ (row & 7));
+        st_shared_u4(row_base + chunk * 16u,
+                     make_uint4(w[i * 4 + 0], w[i * 4 + 1], w[i * 4 + 2], w[i * 4 + 3]));
+    }
+}
+
 // ----------------------------------------------------------------------------
 // the kernel
 // ----------------------------------------------------------------------------
 template <int BN, int STAGES, int OUT>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_tn_kernel(const __grid_constant__ CUtensorMap tmap_a,
-                   const __grid_constant__ CUtensorMap tmap_b, const KParams p) {
+                   const __grid_constant__ CUtensorMap tmap_b,
+                   const __grid_constant__ CUtensorMap tmap_c, const KParams p) {
     using L = SmemLayout<BN, STAGES>;
     static_assert(BN == 64 || BN == 128 || BN == 256, "tile width");
     static_assert(OUT != kOutI32 || BN <= 128, "integer mode keeps BN int32 sums in registers");
@@ -460,7 +511,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint8_t* smem = smem_raw + ((1024u - (raw_addr & 1023u)) & 1023u);
     const uint32_t ring = smem_addr(smem);                       // A slots, then B slots
     const uint32_t ring_b = ring + STAGES * kATileBytes;
-    SharedCtl<STAGES>* ctl = reinterpret_cast<SharedCtl<STAGES>*>(smem + L::kRingBytes);
+    const uint32_t staging = ring + L::kRingBytes;              // epilogue store buffers
+    SharedCtl<STAGES>* ctl =
+        reinterpret_cast<SharedCtl<STAGES>*>(smem + L::kRingBytes + L::kStagingBytes);
 
     const int warp = __shfl_sync(0xffffffffu, static_cast<int>(threadIdx.x) / 32, 0);
     const int lane = static_cast<int>(threadIdx.x) & 31;
@@ -468,6 +521,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp == 0 && lane == 0) {
         prefetch_tmap(&tmap_a);
         prefetch_tmap(&tmap_b);
+        prefetch_tmap(&tmap_c);
         for (int s = 0; s < STAGES; ++s) {
             mbar_init(smem_addr(&ctl->full[s]), 1);
             mbar_init(smem_addr(&ctl->empty[s]), 1);
@@ -493,6 +547,18 @@ __global__ void __launch_bounds__(kThreads, 1)
     // kernel of the stream; no global memory is touched before that kernel has
     // completed and its writes are visible.  The next kernel may be scheduled
     // from here on (it waits the same way before reading anything we write).
+    if (warp == 0 && lane == 0 && static_cast<int32_t>(blockIdx.x) < p.num_units) {
+        // Warm L2 with this CTA's first k-blocks while the previous kernel drains.
+        // Only L2 is touched (the coherence point); the data is read after the
+        // wait below, so this cannot observe stale values.
+        const UnitCoord c = unit_coord(blockIdx.x, p.split_k, p.kb_per_split, p.num_kb,
+                                       p.m_blocks, p.n_blocks, p.raster_group);
+        const int32_t kb_end = c.kb_begin + STAGES < c.kb_end ? c.kb_begin + STAGES : c.kb_end;
+        for (int32_t kb = c.kb_begin; kb < kb_end; ++kb) {
+            tma_prefetch_l2_2d(&tmap_a, kb * kBK, c.m_blk * kBM);
+            tma_prefetch_l2_2d(&tmap_b, kb * kBK, c.n_blk * BN);
+        }
+    }
     grid_dependency_wait();
     grid_launch_dependents();
     const Watch watch{&ctl->abort, p.error_word, p.timeout_ns};
@@ -600,6 +666,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int row_in_tile = quad * 32 + lane;
         const int epi_tid = (warp - 2) * 32 + lane;   // 0..127
         const uint32_t lane_addr = static_cast<uint32_t>(quad * 32) << 16;
+        // This warp's two TMA-store buffers and which one is next.
+        const uint32_t store_buf0 = staging + static_cast<uint32_t>((warp - 2) * 2 * L::kStoreBufBytes);
+        uint32_t store_sel = 0;
         uint32_t acc_iter = 0;
         bool ok = true;
         for (int32_t u = blockIdx.x; ok && u < p.num_units; u += gridDim.x) {
@@ -650,8 +719,25 @@ __global__ void __launch_bounds__(kThreads, 1)
                         stage_row32<BN>(ring, row_in_tile, j * 32, &sum[j * 32]);
                     } else if (split) {
                         if (row < p.M) store_ws32(ws_row + j * 32, &sum[j * 32]);
-                    } else if (row < p.M) {
-                        store_i32_row32(p.C, p.N, row, col0 + j * 32, &sum[j * 32]);
+                    } else {
+                        // 32 int32 columns = one 128-byte row of a store buffer.  A
+                        // segment wholly outside C is skipped (warp-uniform), so every
+                        // buffer switch matches one committed store group.
+                        const int32_t y = c.m_blk * kBM + quad * 32;
+                        const int32_t x = col0 + j * 32;
+                        if (y < p.M && x < p.N) {
+                            const uint32_t buf = store_buf0 + store_sel * L::kStoreBufBytes;
+                            if (lane == 0) bulk_wait_group_read<1>();
+                            __syncwarp();
+                            stage_store_row(buf, lane, 0, &sum[j * 32], 8);
+                            fence_proxy_async_smem();
+                            __syncwarp();
+                            if (lane == 0) {
+                                tma_store_2d(&tmap_c, buf, x, y);
+                                bulk_commit_group();
+                            }
+                            store_sel ^= 1u;
+                        }
                     }
                 }
             } else {
@@ -663,17 +749,49 @@ __global__ void __launch_bounds__(kThreads, 1)
                     break;
                 }
                 tc_fence_after();
+                if (cluster || split) {
 #pragma unroll 1
-                for (int j = 0; j < BN / 32; ++j) {
-                    uint32_t v[32];
-                    tmem_ld_32x32b_x32(tmem_base + lane_addr + buf * BN + j * 32, v);
-                    tmem_ld_wait();
-                    if (cluster) {
-                        stage_row32<BN>(ring, row_in_tile, j * 32, v);
-                    } else if (split) {
-                        if (row < p.M) store_ws32(ws_row + j * 32, v);
-                    } else if (row < p.M) {
-                        store_half_row32<OUT>(p.C, p.N, row, col0 + j * 32, v);
+                    for (int j = 0; j < BN / 32; ++j) {
+                        uint32_t v[32];
+                        tmem_ld_32x32b_x32(tmem_base + lane_addr + buf * BN + j * 32, v);
+                        tmem_ld_wait();
+                        if (cluster) {
+                            stage_row32<BN>(ring, row_in_tile, j * 32, v);
+                        } else if (row < p.M) {
+                            store_ws32(ws_row + j * 32, v);
+                        }
+                    }
+                } else {
+                    // 64 16-bit columns = one 128-byte store-buffer row per thread;
+                    // segments wholly outside C are skipped (warp-uniform), so every
+                    // buffer switch matches one committed store group.
+                    const int32_t y = c.m_blk * kBM + quad * 32;
+#pragma unroll 1
+                    for (int sc = 0; sc < BN / 64; ++sc) {
+                        const int32_t x = col0 + sc * 64;
+                        if (y >= p.M || x >= p.N) continue;
+                        const uint32_t sbuf = store_buf0 + store_sel * L::kStoreBufBytes;
+                        if (lane == 0) bulk_wait_group_read<1>();
+                        __syncwarp();
+#pragma unroll
+                        for (int h = 0; h < 2; ++h) {
+                            uint32_t v[32];
+                            tmem_ld_32x32b_x32(tmem_base + lane_addr + buf * BN + sc * 64 + h * 32, v);
+                            tmem_ld_wait();
+                            uint32_t w[16];
+#pragma unroll
+                            for (int i = 0; i < 16; ++i)
+                                w[i] = pack2<OUT>(__uint_as_float(v[2 * i]),
+                                                  __uint_as_float(v[2 * i + 1]));
+                            stage_store_row(sbuf, lane, h * 4, w, 4);
+                        }
+                        fence_proxy_async_smem();
+                        __syncwarp();
+                        if (lane == 0) {
+                            tma_store_2d(&tmap_c, sbuf, x, y);
+                            bulk_commit_group();
+                        }
+                        store_sel ^= 1u;
                     }
                 }
                 tc_fence_before();
@@ -717,6 +835,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             }
         }
+    }
+
+    if (warp >= 2) {
+        // Bulk stores of this warp: complete before the CTA (and its shared memory) ends.
+        if ((threadIdx.x & 31) == 0) bulk_wait_group_all();
+        __syncwarp();
     }
 
     // ------------------------------------------- split-K reduction in the cluster

@@ -22,18 +22,18 @@ struct LaunchShape {
 // cudaErrorInvalidValue if no variant exists for (bn, stages, out).
 cudaError_t gemm_prepare(int bn, int stages, int out, size_t* smem_bytes);
 cudaError_t gemm_launch(int bn, int stages, int out, const LaunchShape& shape,
-                        const CUtensorMap& tmap_a, const CUtensorMap& tmap_b, const KParams& p,
-                        cudaStream_t stream);
+                        const CUtensorMap& tmap_a, const CUtensorMap& tmap_b,
+                        const CUtensorMap& tmap_c, const KParams& p, cudaStream_t stream);
 
 // Per-output-type translation units.
 cudaError_t gemm_prepare_f16(int bn, int stages, size_t* smem_bytes);
 cudaError_t gemm_prepare_bf16(int bn, int stages, size_t* smem_bytes);
 cudaError_t gemm_prepare_i32(int bn, int stages, size_t* smem_bytes);
-cudaError_t gemm_launch_f16(int bn, int stages, const LaunchShape&, const CUtensorMap&,
+cudaError_t gemm_launch_f16(int bn, int stages, const LaunchShape&, const CUtensorMap&, const CUtensorMap&,
                             const CUtensorMap&, const KParams&, cudaStream_t);
-cudaError_t gemm_launch_bf16(int bn, int stages, const LaunchShape&, const CUtensorMap&,
+cudaError_t gemm_launch_bf16(int bn, int stages, const LaunchShape&, const CUtensorMap&, const CUtensorMap&,
                              const CUtensorMap&, const KParams&, cudaStream_t);
-cudaError_t gemm_launch_i32(int bn, int stages, const LaunchShape&, const CUtensorMap&,
+cudaError_t gemm_launch_i32(int bn, int stages, const LaunchShape&, const CUtensorMap&, const CUtensorMap&,
                             const CUtensorMap&, const KParams&, cudaStream_t);
 
 // Auxiliary kernels (gemm_aux.cu).

@@ -111,6 +111,18 @@ bool encode_operand(CUtensorMap* map, const void* base, int64_t rows, int64_t K,
               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+bool encode_result(CUtensorMap* map, void* base, int64_t M, int64_t N, CUtensorMapDataType dt) {
+    PFN_cuTensorMapEncodeTiled_v12000 fn = encode_entry();
+    if (!fn) return false;
+    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(N), static_cast<cuuint64_t>(M)};
+    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(N) * 2};
+    const cuuint32_t box[2] = {64, 32};   // 128-byte row segments x 32 rows
+    const cuuint32_t estr[2] = {1, 1};
+    return fn(map, dt, 2, base, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+              CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 }  // namespace
 
 extern "C" gemm_status_t gemm_run_splitk_noalloc(int64_t M, int64_t N, int64_t K,
@@ -174,9 +186,9 @@ extern "C" gemm_status_t gemm_run_splitk_noalloc(int64_t M, int64_t N, int64_t K
 
     const CUtensorMapDataType dt =
         dtype == GEMM_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
-    CUtensorMap map_a, map_b;
+    CUtensorMap map_a, map_b, map_c;
     if (!encode_operand(&map_a, A, M, K, gbg::kBM, dt) ||
-        !encode_operand(&map_b, B, N, K, kBlockN, dt))
+        !encode_operand(&map_b, B, N, K, kBlockN, dt) || !encode_result(&map_c, C, M, N, dt))
         return GEMM_ERR_TENSORMAP;
 
     gbg::KParams kp;
@@ -211,9 +223,9 @@ extern "C" gemm_status_t gemm_run_splitk_noalloc(int64_t M, int64_t N, int64_t K
     const cudaError_t e =
         dtype == GEMM_BF16
             ? cudaLaunchKernelEx(&cfg, gbg::gemm_tn_kernel<kBlockN, kStages, gbg::kOutBF16>, map_a,
-                                 map_b, kp)
+                                 map_b, map_c, kp)
             : cudaLaunchKernelEx(&cfg, gbg::gemm_tn_kernel<kBlockN, kStages, gbg::kOutF16>, map_a,
-                                 map_b, kp);
+                                 map_b, map_c, kp);
     if (e != cudaSuccess) {
         cudaGetLastError();
         return GEMM_ERR_LAUNCH;
