@@ -86,8 +86,15 @@ gemm_status_t normalise_config(int64_t M, int64_t N, int64_t K, gemm_dtype_t dty
                                int32_t* kb_per_split) {
     gemm_config_t c = in;
     if (!valid_block_n(c.block_n, dtype)) return GEMM_ERR_INVALID_ARG;
-    if (c.stages == 0) c.stages = gbg::default_stages(c.block_n);
-    if (c.stages != gbg::default_stages(c.block_n)) return GEMM_ERR_INVALID_ARG;
+    if (c.cta_pair != 0 && c.cta_pair != 1) return GEMM_ERR_INVALID_ARG;
+    if (c.cta_pair) {
+        // SM pair: 256-row tiles, fp16/bf16 only, no K slicing.
+        if (dtype == GEMM_I8_I32 || c.block_n < 128 || c.split_k != 1) return GEMM_ERR_INVALID_ARG;
+    }
+    const int want_stages =
+        c.cta_pair ? gbg::default_pair_stages(c.block_n) : gbg::default_stages(c.block_n);
+    if (c.stages == 0) c.stages = want_stages;
+    if (c.stages != want_stages) return GEMM_ERR_INVALID_ARG;
     if (c.split_k < 1 || c.raster_group < 1 || c.max_ctas < 0) return GEMM_ERR_INVALID_ARG;
     if (c.split_mode != 0 && c.split_mode != 1) return GEMM_ERR_INVALID_ARG;
     const int64_t num_kb = (K + gbg::kBK - 1) / gbg::kBK;
@@ -96,7 +103,8 @@ gemm_status_t normalise_config(int64_t M, int64_t N, int64_t K, gemm_dtype_t dty
     if (s > num_kb && num_kb > 0) s = num_kb;
     const int64_t per = num_kb > 0 ? (num_kb + s - 1) / s : 0;
     if (per > 0) s = (num_kb + per - 1) / per;
-    const int64_t m_blocks = (M + gbg::kBM - 1) / gbg::kBM;
+    const int64_t tile_m = c.cta_pair ? 2 * gbg::kBM : gbg::kBM;
+    const int64_t m_blocks = (M + tile_m - 1) / tile_m;
     const int64_t n_blocks = (N + c.block_n - 1) / c.block_n;
     if (m_blocks * n_blocks * s > INT32_MAX) return GEMM_ERR_INVALID_ARG;
     c.split_k = static_cast<int32_t>(s);
@@ -256,7 +264,12 @@ gemm_status_t create_plan(int64_t M, int64_t N, int64_t K, gemm_dtype_t dtype,
     p->d_b16 = p->dmem + p->mem.b16_off;
 
     size_t smem = 0;
-    if (gbg::gemm_prepare(cfg.block_n, cfg.stages, p->out_kind, &smem) != cudaSuccess) {
+    const cudaError_t prep =
+        cfg.cta_pair ? (p->out_kind == gbg::kOutF16
+                            ? gbg::gemm_prepare_pair_f16(cfg.block_n, cfg.stages, &smem)
+                            : gbg::gemm_prepare_pair_bf16(cfg.block_n, cfg.stages, &smem))
+                     : gbg::gemm_prepare(cfg.block_n, cfg.stages, p->out_kind, &smem);
+    if (prep != cudaSuccess) {
         cudaGetLastError();
         cudaFree(p->dmem);
         delete p;
@@ -269,7 +282,8 @@ gemm_status_t create_plan(int64_t M, int64_t N, int64_t K, gemm_dtype_t dtype,
     kp.N = static_cast<int32_t>(N);
     kp.K = static_cast<int32_t>(K);
     kp.num_kb = static_cast<int32_t>((K + gbg::kBK - 1) / gbg::kBK);
-    kp.m_blocks = static_cast<int32_t>((M + gbg::kBM - 1) / gbg::kBM);
+    const int64_t tile_m = cfg.cta_pair ? 2 * gbg::kBM : gbg::kBM;
+    kp.m_blocks = static_cast<int32_t>((M + tile_m - 1) / tile_m);
     kp.n_blocks = static_cast<int32_t>((N + cfg.block_n - 1) / cfg.block_n);
     kp.split_k = cfg.split_k;
     kp.cluster_split = cfg.split_mode == 1 ? 1 : 0;
@@ -283,7 +297,7 @@ gemm_status_t create_plan(int64_t M, int64_t N, int64_t K, gemm_dtype_t dtype,
     kp.idesc = (1u << 4)                                         // D: fp32
                | (fmt << 7) | (fmt << 10)                        // A, B: fp16 or bf16
                | (static_cast<uint32_t>(cfg.block_n >> 3) << 17)  // N / 8
-               | (static_cast<uint32_t>(gbg::kBM >> 4) << 24);    // M / 16
+               | (static_cast<uint32_t>(tile_m >> 4) << 24);      // M / 16 (128, or 256 for a pair)
     kp.tx_extra = 0;
     kp.workspace = p->d_ws;
     kp.counters = p->d_counters;
@@ -296,6 +310,11 @@ gemm_status_t create_plan(int64_t M, int64_t N, int64_t K, gemm_dtype_t dtype,
     if (kp.cluster_split) {   // one unit per CTA, clusters of split_k CTAs
         p->shape.grid = kp.num_units;
         p->shape.cluster = cfg.split_k;
+    }
+    if (cfg.cta_pair) {       // persistent SM pairs: two CTAs per tile
+        const int pairs_cap = cap / 2 > 0 ? cap / 2 : 1;
+        p->shape.grid = 2 * (kp.num_units < pairs_cap ? kp.num_units : pairs_cap);
+        p->shape.cluster = 2;
     }
     if (p->shape.grid < 1) p->shape.grid = 1;
     p->shape.block = gbg::kThreads;
@@ -398,7 +417,9 @@ gemm_status_t gemm_run(gemm_plan_t p, const void* A, const void* B, void* C, voi
         }
         if (!p->map_b_valid || p->map_b_src != B) {
             p->map_b_valid = false;
-            const gemm_status_t st = encode_kmajor(&p->map_b, B, p->N, p->K, p->cfg.block_n, dt);
+            // an SM pair loads half of the tile's B rows per CTA
+            const int b_rows = p->cfg.cta_pair ? p->cfg.block_n / 2 : p->cfg.block_n;
+            const gemm_status_t st = encode_kmajor(&p->map_b, B, p->N, p->K, b_rows, dt);
             if (st != GEMM_OK) return st;
             p->map_b_src = B;
             p->map_b_valid = true;
@@ -412,8 +433,17 @@ gemm_status_t gemm_run(gemm_plan_t p, const void* A, const void* B, void* C, voi
         p->map_c_valid = true;
     }
     p->kp.C = C;
-    if (gbg::gemm_launch(p->cfg.block_n, p->cfg.stages, p->out_kind, p->shape, p->map_a, p->map_b,
-                         p->map_c, p->kp, stream) != cudaSuccess) {
+    cudaError_t e;
+    if (p->cfg.cta_pair)
+        e = p->out_kind == gbg::kOutF16
+                ? gbg::gemm_launch_pair_f16(p->cfg.block_n, p->cfg.stages, p->shape, p->map_a,
+                                            p->map_b, p->map_c, p->kp, stream)
+                : gbg::gemm_launch_pair_bf16(p->cfg.block_n, p->cfg.stages, p->shape, p->map_a,
+                                             p->map_b, p->map_c, p->kp, stream);
+    else
+        e = gbg::gemm_launch(p->cfg.block_n, p->cfg.stages, p->out_kind, p->shape, p->map_a,
+                             p->map_b, p->map_c, p->kp, stream);
+    if (e != cudaSuccess) {
         cudaGetLastError();
         return GEMM_ERR_LAUNCH;
     }

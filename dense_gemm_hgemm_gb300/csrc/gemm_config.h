@@ -16,7 +16,7 @@ namespace gbg {
 
 struct TableEntry {
     int32_t M, N, K, dtype;
-    int32_t block_n, split_k, raster_group, split_mode;
+    int32_t block_n, split_k, raster_group, split_mode, cta_pair;
 };
 
 #include "gemm_config_table.inc"   // static const TableEntry kTunedTable[]; kTunedCount
@@ -36,6 +36,7 @@ inline gemm_config_t model_config(int64_t M, int64_t N, int64_t K, gemm_dtype_t 
     c.raster_group = 16;
     c.split_k = 1;
     c.split_mode = 0;
+    c.cta_pair = 0;
     const int64_t mb = ceil_div(M, kBM);
     const int64_t num_kb = ceil_div(K, kBK);
     const int cands_f[3] = {256, 128, 64};
@@ -80,6 +81,7 @@ inline gemm_config_t select_config(int64_t M, int64_t N, int64_t K, gemm_dtype_t
             c.split_k = e.split_k;
             c.raster_group = e.raster_group;
             c.split_mode = e.split_mode;
+            c.cta_pair = e.cta_pair;
             c.max_ctas = 0;
             return c;
         }

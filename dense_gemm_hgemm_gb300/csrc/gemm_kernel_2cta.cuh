@@ -1,0 +1,364 @@
+// gemm_kernel_2cta.cuh -- the SM-pair (tcgen05 cta_group::2) variant of the TN GEMM.
+//
+// A thread-block cluster of two CTAs (ranks 0 = leader, 1 = peer, on two SMs)
+// computes a 256 x BN output tile:
+//   * each CTA streams its own 128 rows of A (128 x 64 per stage) and its half
+//     of the tile's B rows (BN/2 x 64 per stage) into its own 128B-swizzled
+//     ring; both CTAs' copies count bytes on the LEADER's `full` barrier;
+//   * one thread of the leader issues tcgen05.mma.cta_group::2 (M=256, N=BN,
+//     K=16): the hardware reads A and B from both CTAs' shared memory and
+//     writes accumulator rows 0-127 to the leader's TMEM, rows 128-255 to the
+//     peer's; tcgen05.commit multicasts ring-slot releases and "accumulator
+//     ready" to the same barriers in both CTAs;
+//   * each CTA's four epilogue warps drain its own TMEM half and TMA-store it,
+//     then arrive (locally or remotely) on the leader's `tmem_empty` barrier.
+// Per SM this moves 32 KiB per 64-wide k-block for 128 x BN x 64 MACs (BN=256)
+// instead of 48 KiB in the one-SM kernel, and the ring holds 6 stages.
+//
+// Same conventions as gemm_kernel.cuh: persistent over tiles (one cluster per SM
+// pair), double-buffered TMEM accumulator, bounded waits with an error word,
+// programmatic dependent launch, L2 prefetch before the dependency wait.
+#pragma once
+
+#include "gemm_kernel.cuh"
+
+namespace gbg {
+
+template <int BN, int STAGES>
+struct SmemLayout2 {
+    static constexpr int kBTileBytes = (BN / 2) * kBK * 2;   // this CTA's half of B
+    static constexpr int kStageBytes = kATileBytes + kBTileBytes;
+    static constexpr int kRingBytes = STAGES * kStageBytes;
+    static constexpr int kStoreBufBytes = 32 * 128;
+    static constexpr int kStagingBytes = kEpiWarps * 2 * kStoreBufBytes;
+    static constexpr int kCtlBytes = 256;
+    static constexpr int kTotal = 1024 + kRingBytes + kStagingBytes + kCtlBytes;
+    static_assert(kBTileBytes % 1024 == 0, "128B-swizzle tiles must stay 1024-byte aligned");
+    static_assert(kTotal <= 232448, "exceeds the 227 KiB a CTA may use");
+};
+
+// Wait-site code for a TMEM address mismatch between the two CTAs of a pair.
+constexpr int32_t kSitePairTmem = 5;
+
+__device__ __forceinline__ void tmem_alloc_pair(uint32_t dst_smem, uint32_t ncols) {
+    asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem),
+                 "r"(ncols)
+                 : "memory");
+}
+__device__ __forceinline__ void tmem_relinquish_pair() {
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc_pair(uint32_t taddr, uint32_t ncols) {
+    asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
+                 : "memory");
+}
+
+// D[tmem of both CTAs] (+)= A[smem of both] * B[smem of both]^T, M=256, N=BN, K=16.
+__device__ __forceinline__ void umma_f16_pair(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                              uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t"
+        ".reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t"
+        "}" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+// Arrive once on the barrier at this shared-memory offset in every CTA of
+// `cta_mask` when all prior tcgen05.mma of this thread are done.
+__device__ __forceinline__ void umma_commit_pair(uint32_t bar, uint16_t cta_mask) {
+    asm volatile(
+        "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
+        " [%0], %1;" ::"r"(bar),
+        "h"(cta_mask)
+        : "memory");
+}
+
+// TMA load into this CTA's shared memory whose bytes are counted on a barrier
+// that may live in the peer CTA (shared::cluster address).
+__device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap* map,
+                                                 uint32_t bar_cluster, int32_t x, int32_t y) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%3, %4}], [%2];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(bar_cluster), "r"(x), "r"(y)
+        : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_remote(uint32_t bar_cluster) {
+    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(bar_cluster)
+                 : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t parity) {
+    uint32_t done;
+    asm volatile(
+        "{\n\t"
+        ".reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t"
+        "}"
+        : "=r"(done)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return done != 0;
+}
+
+// As wait_phase, with cluster-scope acquire (the arrivals come from both CTAs).
+__device__ __forceinline__ bool wait_phase_cluster(uint32_t bar, uint32_t parity, const Watch& w,
+                                                   int32_t site) {
+    if (mbar_try_wait_cluster(bar, parity)) return true;
+    const uint64_t t0 = global_timer_ns();
+    for (uint32_t n = 1;; ++n) {
+        if (mbar_try_wait_cluster(bar, parity)) return true;
+        if ((n & 31u) == 0) {
+            if (*w.abort) return false;
+            if (global_timer_ns() - t0 > w.timeout_ns) {
+                *w.abort = 1;
+                atomicCAS(w.error_word, 0, site);
+                return false;
+            }
+        }
+    }
+}
+
+__device__ __forceinline__ uint32_t ld_dsmem_u32(uint32_t cluster_addr) {
+    uint32_t v;
+    asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(v) : "r"(cluster_addr) : "memory");
+    return v;
+}
+
+template <int BN, int STAGES, int OUT>
+__global__ void __launch_bounds__(kThreads, 1)
+    gemm_tn_pair_kernel(const __grid_constant__ CUtensorMap tmap_a,
+                        const __grid_constant__ CUtensorMap tmap_b,
+                        const __grid_constant__ CUtensorMap tmap_c, const KParams p) {
+    using L = SmemLayout2<BN, STAGES>;
+    static_assert(BN == 128 || BN == 256, "pair tile width");
+    static_assert(OUT == kOutF16 || OUT == kOutBF16, "pair kernel: 16-bit outputs");
+    constexpr uint32_t kTmemCols = 2 * BN;
+    constexpr uint32_t kPairTx = 2 * L::kStageBytes;   // both CTAs' bytes per stage
+
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw_addr = smem_addr(smem_raw);
+    uint8_t* smem = smem_raw + ((1024u - (raw_addr & 1023u)) & 1023u);
+    const uint32_t ring = smem_addr(smem);
+    const uint32_t ring_b = ring + STAGES * kATileBytes;
+    const uint32_t staging = ring + L::kRingBytes;
+    SharedCtl<STAGES>* ctl =
+        reinterpret_cast<SharedCtl<STAGES>*>(smem + L::kRingBytes + L::kStagingBytes);
+
+    const int warp = __shfl_sync(0xffffffffu, static_cast<int>(threadIdx.x) / 32, 0);
+    const int lane = static_cast<int>(threadIdx.x) & 31;
+    const uint32_t rank = cluster_ctarank();          // 0: leader, 1: peer
+    const bool leader = rank == 0;
+    const int32_t pair = static_cast<int32_t>(blockIdx.x >> 1);
+    const int32_t npairs = static_cast<int32_t>(gridDim.x >> 1);
+
+    if (warp == 0 && lane == 0) {
+        prefetch_tmap(&tmap_a);
+        prefetch_tmap(&tmap_b);
+        prefetch_tmap(&tmap_c);
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(smem_addr(&ctl->full[s]), 1);
+            mbar_init(smem_addr(&ctl->empty[s]), 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(smem_addr(&ctl->tmem_full[b]), 1);
+            mbar_init(smem_addr(&ctl->tmem_empty[b]), 2 * kEpiWarps);   // both CTAs' epilogues
+        }
+        mbar_init(smem_addr(&ctl->drain), 1);
+        ctl->abort = 0;
+        ctl->splitk_last = 0;
+        fence_barrier_init();
+    }
+    if (warp == 1) {
+        tmem_alloc_pair(smem_addr(&ctl->tmem_base), kTmemCols);
+        tmem_relinquish_pair();
+    }
+    tc_fence_before();
+    cluster_sync_all();   // barriers of both CTAs initialised, TMEM allocated in both
+    tc_fence_after();
+    const uint32_t tmem_base = ctl->tmem_base;
+    const Watch watch{&ctl->abort, p.error_word, p.timeout_ns};
+    if (!leader && threadIdx.x == 0) {
+        // The leader's MMAs address the peer's TMEM with the leader's address.
+        const uint32_t lead_base = ld_dsmem_u32(map_to_rank(smem_addr(&ctl->tmem_base), 0));
+        if (lead_base != tmem_base) {
+            atomicCAS(p.error_word, 0, kSitePairTmem);
+            ctl->abort = 1;
+        }
+    }
+
+    if (warp == 0 && lane == 0 && pair < p.num_units) {
+        const UnitCoord c = unit_coord(pair, 1, p.kb_per_split, p.num_kb, p.m_blocks, p.n_blocks,
+                                       p.raster_group);
+        const int32_t kb_end = STAGES < c.kb_end ? STAGES : c.kb_end;
+        for (int32_t kb = 0; kb < kb_end; ++kb) {
+            tma_prefetch_l2_2d(&tmap_a, kb * kBK, c.m_blk * 2 * kBM + static_cast<int32_t>(rank) * kBM);
+            tma_prefetch_l2_2d(&tmap_b, kb * kBK, c.n_blk * BN + static_cast<int32_t>(rank) * (BN / 2));
+        }
+    }
+    grid_dependency_wait();
+    grid_launch_dependents();
+
+    if (warp == 0) {
+        // ------------------------------------------------------------ producer (both CTAs)
+        if (elect_one_sync()) {
+            int stage = 0;
+            uint32_t phase = 0;
+            int issued = 0;
+            bool ok = true;
+            for (int32_t u = pair; ok && u < p.num_units; u += npairs) {
+                const UnitCoord c = unit_coord(u, 1, p.kb_per_split, p.num_kb, p.m_blocks,
+                                               p.n_blocks, p.raster_group);
+                const int32_t a_row = c.m_blk * 2 * kBM + static_cast<int32_t>(rank) * kBM;
+                const int32_t b_row = c.n_blk * BN + static_cast<int32_t>(rank) * (BN / 2);
+                for (int32_t kb = c.kb_begin; kb < c.kb_end; ++kb) {
+                    if (!wait_phase(smem_addr(&ctl->empty[stage]), phase ^ 1u, watch,
+                                    kSiteProducerEmpty)) {
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t full_local = smem_addr(&ctl->full[stage]);
+                    if (leader) mbar_arrive_expect_tx(full_local, kPairTx + p.tx_extra);
+                    const uint32_t full_lead = map_to_rank(full_local, 0);
+                    tma_load_2d_pair(ring + stage * kATileBytes, &tmap_a, full_lead, kb * kBK, a_row);
+                    tma_load_2d_pair(ring_b + stage * L::kBTileBytes, &tmap_b, full_lead, kb * kBK,
+                                     b_row);
+                    ++issued;
+                    if (++stage == STAGES) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+            }
+            if (leader) {
+                // Both CTAs' copies count on the leader's barriers: wait for them to
+                // land before the pair can leave (immediate in normal operation).
+                int s = stage;
+                uint32_t ph = phase;
+                const int pending = issued < STAGES ? issued : STAGES;
+                for (int i = 0; i < pending; ++i) {
+                    if (--s < 0) {
+                        s = STAGES - 1;
+                        ph ^= 1u;
+                    }
+                    wait_phase_unwind(smem_addr(&ctl->full[s]), ph, 100000000ull);
+                }
+            }
+            (void)ok;
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        // ------------------------------------------------------------ MMA issuer (leader)
+        if (leader && elect_one_sync()) {
+            int stage = 0;
+            uint32_t phase = 0;
+            uint32_t acc_iter = 0;
+            bool ok = true;
+            for (int32_t u = pair; ok && u < p.num_units; u += npairs) {
+                const UnitCoord c = unit_coord(u, 1, p.kb_per_split, p.num_kb, p.m_blocks,
+                                               p.n_blocks, p.raster_group);
+                const uint32_t buf = acc_iter & 1u;
+                const uint32_t acc_phase = (acc_iter >> 1) & 1u;
+                if (!wait_phase_cluster(smem_addr(&ctl->tmem_empty[buf]), acc_phase ^ 1u, watch,
+                                        kSiteMmaTmemEmpty)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t d_tmem = tmem_base + buf * BN;
+                for (int32_t kb = c.kb_begin; kb < c.kb_end; ++kb) {
+                    if (!wait_phase(smem_addr(&ctl->full[stage]), phase, watch, kSiteMmaFull)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint64_t a_desc = sw128_kmajor_desc(ring + stage * kATileBytes);
+                    const uint64_t b_desc = sw128_kmajor_desc(ring_b + stage * L::kBTileBytes);
+#pragma unroll
+                    for (int k = 0; k < kBK / 16; ++k)
+                        umma_f16_pair(d_tmem, a_desc + 2u * k, b_desc + 2u * k, p.idesc,
+                                      (kb > c.kb_begin || k > 0) ? 1u : 0u);
+                    umma_commit_pair(smem_addr(&ctl->empty[stage]), 0x3);
+                    if (++stage == STAGES) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+                if (!ok) break;
+                umma_commit_pair(smem_addr(&ctl->tmem_full[buf]), 0x3);
+                ++acc_iter;
+            }
+            umma_commit_pair(smem_addr(&ctl->drain), 0x1);
+            wait_phase_unwind(smem_addr(&ctl->drain), 0, 100000000ull);
+        }
+        __syncwarp();
+    } else {
+        // ------------------------------------------------------------ epilogue (both CTAs)
+        const int quad = warp & 3;
+        const uint32_t lane_addr = static_cast<uint32_t>(quad * 32) << 16;
+        const uint32_t store_buf0 = staging + static_cast<uint32_t>((warp - 2) * 2 * L::kStoreBufBytes);
+        uint32_t store_sel = 0;
+        uint32_t acc_iter = 0;
+        for (int32_t u = pair; u < p.num_units; u += npairs) {
+            const UnitCoord c = unit_coord(u, 1, p.kb_per_split, p.num_kb, p.m_blocks, p.n_blocks,
+                                           p.raster_group);
+            const uint32_t buf = acc_iter & 1u;
+            const uint32_t acc_phase = (acc_iter >> 1) & 1u;
+            if (!wait_phase(smem_addr(&ctl->tmem_full[buf]), acc_phase, watch, kSiteEpiTmemFull))
+                break;
+            tc_fence_after();
+            const int32_t y = c.m_blk * 2 * kBM + static_cast<int32_t>(rank) * kBM + quad * 32;
+            const int32_t col0 = c.n_blk * BN;
+#pragma unroll 1
+            for (int sc = 0; sc < BN / 64; ++sc) {
+                const int32_t x = col0 + sc * 64;
+                if (y >= p.M || x >= p.N) continue;   // warp-uniform
+                const uint32_t sbuf = store_buf0 + store_sel * L::kStoreBufBytes;
+                if (lane == 0) bulk_wait_group_read<1>();
+                __syncwarp();
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    uint32_t v[32];
+                    tmem_ld_32x32b_x32(tmem_base + lane_addr + buf * BN + sc * 64 + h * 32, v);
+                    tmem_ld_wait();
+                    uint32_t w[16];
+#pragma unroll
+                    for (int i = 0; i < 16; ++i)
+                        w[i] = pack2<OUT>(__uint_as_float(v[2 * i]), __uint_as_float(v[2 * i + 1]));
+                    stage_store_row(sbuf, lane, h * 4, w, 4);
+                }
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) {
+                    tma_store_2d(&tmap_c, sbuf, x, y);
+                    bulk_commit_group();
+                }
+                store_sel ^= 1u;
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) {
+                const uint32_t bar = smem_addr(&ctl->tmem_empty[buf]);
+                mbar_arrive_remote(map_to_rank(bar, 0));
+            }
+            ++acc_iter;
+        }
+        if (lane == 0) bulk_wait_group_all();
+        __syncwarp();
+    }
+
+    // ---------------------------------------------------------------- teardown
+    tc_fence_before();
+    cluster_sync_all();   // the pair's MMAs, TMEM reads and copies are all finished
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc_pair(tmem_base, kTmemCols);
+    }
+}
+
+}  // namespace gbg

@@ -10,6 +10,8 @@ namespace gbg {
 
 // Default ring depth per tile width (all near 192 KiB of the 227 KiB a CTA may use).
 constexpr int default_stages(int bn) { return bn == 256 ? 4 : (bn == 128 ? 6 : 8); }
+// SM-pair kernel: each CTA holds A 128 x 64 and half of B per stage.
+constexpr int default_pair_stages(int bn) { return bn == 256 ? 6 : 8; }
 
 struct LaunchShape {
     int grid;
@@ -35,6 +37,15 @@ cudaError_t gemm_launch_bf16(int bn, int stages, const LaunchShape&, const CUten
                              const CUtensorMap&, const KParams&, cudaStream_t);
 cudaError_t gemm_launch_i32(int bn, int stages, const LaunchShape&, const CUtensorMap&, const CUtensorMap&,
                             const CUtensorMap&, const KParams&, cudaStream_t);
+
+// SM-pair (cta_group::2) kernels, 16-bit outputs.
+cudaError_t gemm_prepare_pair_f16(int bn, int stages, size_t* smem_bytes);
+cudaError_t gemm_prepare_pair_bf16(int bn, int stages, size_t* smem_bytes);
+cudaError_t gemm_launch_pair_f16(int bn, int stages, const LaunchShape&, const CUtensorMap&,
+                                 const CUtensorMap&, const CUtensorMap&, const KParams&, cudaStream_t);
+cudaError_t gemm_launch_pair_bf16(int bn, int stages, const LaunchShape&, const CUtensorMap&,
+                                  const CUtensorMap&, const CUtensorMap&, const KParams&,
+                                  cudaStream_t);
 
 // Auxiliary kernels (gemm_aux.cu).
 cudaError_t launch_widen_i8(const int8_t* a, int64_t na, const int8_t* b, int64_t nb, void* a16,

@@ -43,6 +43,13 @@ def candidates(M, N, K, dtype, sms):
             per = -(-num_kb // s) if s > 1 else 0
             if s in (2, 4, 8) and -(-num_kb // per) == s:
                 out.append({"block_n": bn, "split_k": s, "raster_group": 16, "split_mode": 1})
+        if dtype != "i8" and bn >= 128 and M > 128:
+            # SM pair: 256-row tiles (raster bands count 256-row blocks)
+            pair_tiles = -(-M // 256) * -(-N // bn)
+            groups = (4, 8, 16) if pair_tiles >= 2 * sms else (8,)
+            for g in groups:
+                out.append({"block_n": bn, "split_k": 1, "raster_group": g, "split_mode": 0,
+                            "cta_pair": 1})
     return out
 
 
@@ -103,7 +110,8 @@ def sweep(out_path, only=None):
                 cold, warm = _time(plan, A, B, C, stream, flush)
             rec["candidates"].append({**cfg, "cold_us": round(cold, 3), "warm_us": round(warm, 3)})
         best = min(rec["candidates"], key=lambda c: (c["cold_us"], c["warm_us"]))
-        rec["best"] = {k: best[k] for k in ("block_n", "split_k", "raster_group", "split_mode")}
+        rec["best"] = {k: best.get(k, 0) for k in ("block_n", "split_k", "raster_group",
+                                                   "split_mode", "cta_pair")}
         rec["model"] = g.gemm_select_config(M, N, K, dtype, sms)
         results.append(rec)
         del A, B, C
@@ -126,15 +134,15 @@ def emit(json_path, table_path=TABLE):
         "// Written by dense_gemm_hgemm_gb300/tune.py from %s" % os.path.basename(json_path),
         "// (%s, %d SMs, %s; %s)." % (doc["gpu"], doc["sms"], doc["when"], doc["regime"]),
         "// Fields: M, N, K, dtype (0 f16, 1 bf16, 2 i8), block_n, split_k, raster_group,",
-        "// split_mode (0 workspace, 1 cluster).",
+        "// split_mode (0 workspace, 1 cluster), cta_pair (0 one SM, 1 SM pair).",
         "static const TableEntry kTunedTable[] = {",
     ]
     n = 0
     for r in doc["shapes"]:
         b = r["best"]
-        lines.append("    {%d, %d, %d, %d, %d, %d, %d, %d}," % (
+        lines.append("    {%d, %d, %d, %d, %d, %d, %d, %d, %d}," % (
             r["M"], r["N"], r["K"], code[r["dtype"]], b["block_n"], b["split_k"],
-            b["raster_group"], b.get("split_mode", 0)))
+            b["raster_group"], b.get("split_mode", 0), b.get("cta_pair", 0)))
         n += 1
     lines.append("};")
     lines.append("static const int kTunedCount = %d;" % n)

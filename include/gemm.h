@@ -87,6 +87,9 @@ typedef enum {
  *                  1 = the slices of a tile run as one thread-block cluster and are
  *                      summed through distributed shared memory (split_k must
  *                      come out as 2, 4 or 8; one tile slice per CTA, no scratch)
+ *   cta_pair     : 1 = 256-row tiles computed by an SM pair (tcgen05 cta_group::2
+ *                  thread-block cluster of two CTAs): fp16/bf16 only, block_n 128
+ *                  or 256, split_k 1; 0 = 128-row tiles on one SM
  */
 typedef struct {
     int32_t block_n;
@@ -95,6 +98,7 @@ typedef struct {
     int32_t raster_group;
     int32_t max_ctas;
     int32_t split_mode;
+    int32_t cta_pair;
 } gemm_config_t;
 
 typedef struct gemm_plan *gemm_plan_t;

@@ -92,6 +92,20 @@ def test_cluster_split_k_parity_and_determinism(shape, split, dtype):
                            C2.view(torch.int16) if dtype != "i8" else C2)
 
 
+@pytest.mark.parametrize("dtype", ["f16", "bf16"])
+@pytest.mark.parametrize("bn", [128, 256])
+@pytest.mark.parametrize("shape", [(256, 128, 64), (64, 136, 128), (300, 264, 1000),
+                                   (1000, 520, 1024), (2048, 1536, 512)],
+                         ids=lambda s: "x".join(map(str, s)))
+def test_pair_kernel_parity(shape, bn, dtype):
+    """256-row tiles on an SM pair (tcgen05 cta_group::2): ragged M (one CTA of
+    the pair entirely beyond M), ragged N, several tiles per pair."""
+    M, N, K = shape
+    A, B = inputs.make_operands(M, N, K, dtype)
+    C = pu.run_gpu(A, B, dtype, {"block_n": bn, "cta_pair": 1}, repeats=2)
+    pu.check_full(A, B, dtype, C, "pair bn=%d %s %s" % (bn, shape, dtype))
+
+
 def test_default_config_headline_shapes():
     for w in (workloads.SKINNY, workloads.HEADLINE_SWEEP):
         A, B = inputs.make_operands(w.M, w.N, w.K, w.dtype, w.a_scale, w.b_scale)
