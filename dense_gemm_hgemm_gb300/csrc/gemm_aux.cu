@@ -46,7 +46,13 @@ __global__ void __launch_bounds__(256) widen_i8_kernel(const int4* __restrict__ 
     }
 }
 
-__global__ void __launch_bounds__(192) empty_kernel() {}
+// Same launch shape and programmatic-dependent-launch protocol as the GEMM
+// kernels, no work: back-to-back launches measure the floor a GEMM launch
+// chain can reach.
+__global__ void __launch_bounds__(192) empty_kernel() {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
 
 __global__ void __launch_bounds__(256) zero_fill_kernel(uint4* __restrict__ dst, int64_t n) {
     const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
@@ -75,8 +81,17 @@ cudaError_t launch_widen_i8(const int8_t* a, int64_t na, const int8_t* b, int64_
 }
 
 cudaError_t launch_empty(int grid, cudaStream_t stream) {
-    empty_kernel<<<grid, 192, 0, stream>>>();
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(grid));
+    cfg.blockDim = dim3(192);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, empty_kernel);
 }
 
 cudaError_t launch_zero_fill(void* dst, int64_t bytes, int num_sms, cudaStream_t stream) {

@@ -838,8 +838,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 
     if (warp >= 2) {
-        // Bulk stores of this warp: complete before the CTA (and its shared memory) ends.
-        if ((threadIdx.x & 31) == 0) bulk_wait_group_all();
+        // This warp's bulk stores must have read their shared-memory source before
+        // the CTA ends; their global writes complete with the grid.
+        if ((threadIdx.x & 31) == 0) bulk_wait_group_read<0>();
         __syncwarp();
     }
 

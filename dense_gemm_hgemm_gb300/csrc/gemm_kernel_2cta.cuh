@@ -348,7 +348,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             ++acc_iter;
         }
-        if (lane == 0) bulk_wait_group_all();
+        if (lane == 0) bulk_wait_group_read<0>();   // sources read; writes complete with the grid
         __syncwarp();
     }
 

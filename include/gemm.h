@@ -177,9 +177,10 @@ const char *gemm_status_string(gemm_status_t status);
 int32_t gemm_abi_version(void);
 
 /*
- * Measurement aid: queue one empty kernel of `grid` CTAs x 192 threads (the
- * GEMM kernel's block size) on `stream`.  Back-to-back launches of it give the
- * launch-latency floor that bounds the smallest GEMMs.
+ * Measurement aid: queue one empty kernel of `grid` CTAs x 192 threads on
+ * `stream`, launched like the GEMM kernels (same block size, programmatic
+ * dependent launch, grid-dependency wait).  Back-to-back launches of it give
+ * the launch-latency floor that bounds the smallest GEMMs.
  */
 gemm_status_t gemm_launch_empty(int32_t grid, void *stream);
 
