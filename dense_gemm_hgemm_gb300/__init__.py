@@ -18,6 +18,7 @@ __all__ = [
     "GEMM_F16", "GEMM_BF16", "GEMM_I8_I32", "GEMM_LAYOUT_TN", "GemmError", "Plan",
     "build_library", "gemm_plan_create", "gemm_plan_create_with_config", "gemm_run",
     "gemm_plan_check", "gemm_plan_destroy", "gemm_plan_get_config", "gemm_plan_set_timeout",
+    "gemm_plan_set_wait_test",
     "gemm_select_config", "gemm_tile_coords", "gemm_workspace_bytes", "gemm_status_string",
     "gemm_abi_version", "gemm_launch_empty", "gemm_run_splitk_noalloc", "library", "DTYPES",
 ]
@@ -75,6 +76,7 @@ def library() -> ctypes.CDLL:
                 "gemm_plan_destroy": ([vp], i32),
                 "gemm_plan_get_config": ([vp, cfgp], i32),
                 "gemm_plan_set_timeout": ([vp, ctypes.c_uint64], i32),
+                "gemm_plan_set_wait_test": ([vp, ctypes.c_uint32], i32),
                 "gemm_select_config": ([i64, i64, i64, i32, i32, cfgp], i32),
                 "gemm_tile_coords": ([i64, i64, i32, i64, ctypes.POINTER(i64),
                                       ctypes.POINTER(i64)], i32),
@@ -193,6 +195,10 @@ def gemm_plan_set_timeout(plan: int, ns: int) -> None:
     _check(library().gemm_plan_set_timeout(plan, int(ns)), "gemm_plan_set_timeout")
 
 
+def gemm_plan_set_wait_test(plan: int, extra_bytes: int) -> None:
+    _check(library().gemm_plan_set_wait_test(plan, int(extra_bytes)), "gemm_plan_set_wait_test")
+
+
 def gemm_select_config(M, N, K, dtype, num_sms: int) -> dict:
     c = gemm_config_t()
     _check(library().gemm_select_config(M, N, K, _dtype_code(dtype), num_sms, ctypes.byref(c)),
@@ -236,6 +242,9 @@ class Plan:
 
     def set_timeout(self, ns: int) -> None:
         gemm_plan_set_timeout(self.handle, ns)
+
+    def set_wait_test(self, extra_bytes: int) -> None:
+        gemm_plan_set_wait_test(self.handle, extra_bytes)
 
     def close(self) -> None:
         if self.handle:

@@ -492,6 +492,12 @@ gemm_status_t gemm_plan_set_timeout(gemm_plan_t p, uint64_t ns) {
     return GEMM_OK;
 }
 
+gemm_status_t gemm_plan_set_wait_test(gemm_plan_t p, uint32_t extra_bytes) {
+    if (!p || extra_bytes > 4096 || (extra_bytes & 15u)) return GEMM_ERR_INVALID_ARG;
+    p->kp.tx_extra = extra_bytes;
+    return GEMM_OK;
+}
+
 gemm_status_t gemm_select_config(int64_t M, int64_t N, int64_t K, gemm_dtype_t dtype,
                                  int32_t num_sms, gemm_config_t* config) {
     if (!config || num_sms < 1) return GEMM_ERR_INVALID_ARG;

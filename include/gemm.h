@@ -151,6 +151,16 @@ gemm_status_t gemm_plan_get_config(gemm_plan_t plan, gemm_config_t *config);
 gemm_status_t gemm_plan_set_timeout(gemm_plan_t plan, uint64_t ns);
 
 /*
+ * Test hook for failure reporting: make every shared-memory ring slot of this
+ * plan's GEMM kernel wait for `extra_bytes` more than its copies deliver, so
+ * the slot never completes, the kernel's bounded wait runs out (see
+ * gemm_plan_set_timeout), the kernel unwinds and frees its resources, and
+ * gemm_plan_check reports GEMM_ERR_DEVICE_TIMEOUT.  The GPU context stays
+ * usable.  0 restores normal operation.  Output C is undefined while it is set.
+ */
+gemm_status_t gemm_plan_set_wait_test(gemm_plan_t plan, uint32_t extra_bytes);
+
+/*
  * Host-only query (no device work): the configuration the table picks for a
  * shape on a GPU with `num_sms` SMs, after validating the shape as
  * gemm_plan_create does.
