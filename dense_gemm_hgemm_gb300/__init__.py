@@ -46,7 +46,7 @@ class gemm_config_t(ctypes.Structure):
     _fields_ = [("block_n", ctypes.c_int32), ("stages", ctypes.c_int32),
                 ("split_k", ctypes.c_int32), ("raster_group", ctypes.c_int32),
                 ("max_ctas", ctypes.c_int32), ("split_mode", ctypes.c_int32),
-                ("cta_pair", ctypes.c_int32)]
+                ("cta_pair", ctypes.c_int32), ("direct_store", ctypes.c_int32)]
 
     def as_dict(self):
         return {f: int(getattr(self, f)) for f, _ in self._fields_}
@@ -132,6 +132,7 @@ def _config(cfg) -> gemm_config_t:
     c.max_ctas = int(cfg.get("max_ctas", 0))
     c.split_mode = int(cfg.get("split_mode", 0))
     c.cta_pair = int(cfg.get("cta_pair", 0))
+    c.direct_store = int(cfg.get("direct_store", 0))
     return c
 
 

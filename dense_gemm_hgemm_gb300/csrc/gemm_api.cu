@@ -87,6 +87,8 @@ gemm_status_t normalise_config(int64_t M, int64_t N, int64_t K, gemm_dtype_t dty
     gemm_config_t c = in;
     if (!valid_block_n(c.block_n, dtype)) return GEMM_ERR_INVALID_ARG;
     if (c.cta_pair != 0 && c.cta_pair != 1) return GEMM_ERR_INVALID_ARG;
+    if (c.direct_store != 0 && c.direct_store != 1) return GEMM_ERR_INVALID_ARG;
+    if (c.direct_store && c.cta_pair) return GEMM_ERR_INVALID_ARG;
     if (c.cta_pair) {
         // SM pair: 256-row tiles, fp16/bf16 only, no K slicing.
         if (dtype == GEMM_I8_I32 || c.block_n < 128 || c.split_k != 1) return GEMM_ERR_INVALID_ARG;
@@ -292,6 +294,7 @@ gemm_status_t create_plan(int64_t M, int64_t N, int64_t K, gemm_dtype_t dtype,
     // every fp32 partial sum is an integer of magnitude <= 2^23: exact).
     kp.chunk_kb = dtype == GEMM_I8_I32 ? 8 : (kb_per_split > 0 ? kb_per_split : 1);
     kp.raster_group = cfg.raster_group;
+    kp.direct_store = cfg.direct_store;
     kp.num_units = kp.m_blocks * kp.n_blocks * kp.split_k;
     const uint32_t fmt = dtype == GEMM_BF16 ? 1u : 0u;
     kp.idesc = (1u << 4)                                         // D: fp32

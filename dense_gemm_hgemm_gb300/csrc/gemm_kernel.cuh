@@ -719,6 +719,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                         stage_row32<BN>(ring, row_in_tile, j * 32, &sum[j * 32]);
                     } else if (split) {
                         if (row < p.M) store_ws32(ws_row + j * 32, &sum[j * 32]);
+                    } else if (p.direct_store) {
+                        if (row < p.M) store_i32_row32(p.C, p.N, row, col0 + j * 32, &sum[j * 32]);
                     } else {
                         // 32 int32 columns = one 128-byte row of a store buffer.  A
                         // segment wholly outside C is skipped (warp-uniform), so every
@@ -749,7 +751,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     break;
                 }
                 tc_fence_after();
-                if (cluster || split) {
+                if (cluster || split || p.direct_store) {
 #pragma unroll 1
                     for (int j = 0; j < BN / 32; ++j) {
                         uint32_t v[32];
@@ -758,7 +760,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                         if (cluster) {
                             stage_row32<BN>(ring, row_in_tile, j * 32, v);
                         } else if (row < p.M) {
-                            store_ws32(ws_row + j * 32, v);
+                            if (split)
+                                store_ws32(ws_row + j * 32, v);
+                            else
+                                store_half_row32<OUT>(p.C, p.N, row, col0 + j * 32, v);
                         }
                     }
                 } else {

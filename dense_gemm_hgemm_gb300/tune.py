@@ -7,10 +7,13 @@ candidate on the target GPU and keeping the fastest.
   python -m dense_gemm_hgemm_gb300.tune --out tuned.json      # on the GPU
   python -m dense_gemm_hgemm_gb300.tune --emit tuned.json     # writes the .inc
 
-Timing regime: each call with L2 flushed first (a 256 MB write on the same
-stream), CUDA events around the call, median of repeats -- the situation of a
-shape inside the 343-shape benchmark step, where every shape's operands come
-from HBM.  Warm back-to-back µs/call is recorded alongside.
+Timing regime ("seq"): the shape's operands exist in R separate copies; L2 is
+flushed (a 256 MB write on the same stream), then R calls run back to back,
+each on its own copy, between two CUDA events; µs/call = elapsed / R, median of
+5 such batches.  Every call reads cold operands and overlaps its launch with the
+previous call (programmatic dependent launch) -- the situation of a shape inside
+the 343-shape benchmark step.  Warm back-to-back µs/call (same buffers, L2
+resident) is recorded alongside.
 """
 from __future__ import annotations
 
@@ -40,6 +43,9 @@ def candidates(M, N, K, dtype, sms):
                 groups = (4, 8, 16, 32)
             for g in groups:
                 out.append({"block_n": bn, "split_k": s, "raster_group": g, "split_mode": 0})
+            if s == 1 and K <= 1024:
+                out.append({"block_n": bn, "split_k": 1, "raster_group": 16, "split_mode": 0,
+                            "direct_store": 1})
             per = -(-num_kb // s) if s > 1 else 0
             if s in (2, 4, 8) and -(-num_kb // per) == s:
                 out.append({"block_n": bn, "split_k": s, "raster_group": 16, "split_mode": 1})
@@ -53,28 +59,30 @@ def candidates(M, N, K, dtype, sms):
     return out
 
 
-def _time(plan, A, B, C, stream, flush, reps_cold=7, reps_warm=20):
+def _time(plan, copies, stream, flush, batches=5, reps_warm=20):
     import torch
+    A0, B0, C0 = copies[0]
     for _ in range(3):
-        plan.run(A, B, C, stream)
+        plan.run(A0, B0, C0, stream)
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
-    cold = []
-    for _ in range(reps_cold):
+    seq = []
+    for _ in range(batches):
         with torch.cuda.stream(stream):
             flush.add_(1)
         e0.record(stream)
-        plan.run(A, B, C, stream)
+        for A, B, C in copies:
+            plan.run(A, B, C, stream)
         e1.record(stream)
         torch.cuda.synchronize()
-        cold.append(e0.elapsed_time(e1) * 1e3)
+        seq.append(e0.elapsed_time(e1) * 1e3 / len(copies))
     e0.record(stream)
     for _ in range(reps_warm):
-        plan.run(A, B, C, stream)
+        plan.run(A0, B0, C0, stream)
     e1.record(stream)
     torch.cuda.synchronize()
     plan.check(stream)
-    return statistics.median(cold), e0.elapsed_time(e1) * 1e3 / reps_warm
+    return statistics.median(seq), e0.elapsed_time(e1) * 1e3 / reps_warm
 
 
 def sweep(out_path, only=None):
@@ -97,31 +105,59 @@ def sweep(out_path, only=None):
     for M, N, K, dtype in shapes:
         gen = torch.Generator(device="cuda")
         gen.manual_seed(inputs.shape_seed(M, N, K, dtype))
-        if dtype == "i8":
-            A = torch.randint(-128, 128, (M, K), generator=gen, device="cuda", dtype=torch.int8)
-            B = torch.randint(-128, 128, (N, K), generator=gen, device="cuda", dtype=torch.int8)
-        else:
-            A = torch.randn(M, K, generator=gen, device="cuda").to(inputs.TORCH_DTYPE[dtype])
-            B = torch.randn(N, K, generator=gen, device="cuda").to(inputs.TORCH_DTYPE[dtype])
-        C = torch.empty(M, N, device="cuda", dtype=inputs.OUT_DTYPE[dtype])
-        rec = {"M": M, "N": N, "K": K, "dtype": dtype, "candidates": []}
+        esz = 1 if dtype == "i8" else 2
+        nbytes = (M * K + N * K) * esz + M * N * (4 if dtype == "i8" else 2)
+        reps = max(2, min(16, (2 << 30) // nbytes))      # copies: at most ~2 GB
+        copies = []
+        for _ in range(reps):
+            if dtype == "i8":
+                A = torch.randint(-128, 128, (M, K), generator=gen, device="cuda", dtype=torch.int8)
+                B = torch.randint(-128, 128, (N, K), generator=gen, device="cuda", dtype=torch.int8)
+            else:
+                A = torch.randn(M, K, generator=gen, device="cuda").to(inputs.TORCH_DTYPE[dtype])
+                B = torch.randn(N, K, generator=gen, device="cuda").to(inputs.TORCH_DTYPE[dtype])
+            copies.append((A, B, torch.empty(M, N, device="cuda", dtype=inputs.OUT_DTYPE[dtype])))
+        rec = {"M": M, "N": N, "K": K, "dtype": dtype, "copies": reps, "candidates": []}
         for cfg in candidates(M, N, K, dtype, sms):
             with g.Plan(M, N, K, dtype, cfg) as plan:
-                cold, warm = _time(plan, A, B, C, stream, flush)
-            rec["candidates"].append({**cfg, "cold_us": round(cold, 3), "warm_us": round(warm, 3)})
-        best = min(rec["candidates"], key=lambda c: (c["cold_us"], c["warm_us"]))
+                seq, warm = _time(plan, copies, stream, flush)
+            rec["candidates"].append({**cfg, "seq_us": round(seq, 3), "warm_us": round(warm, 3)})
+        best = min(rec["candidates"], key=lambda c: (c["seq_us"], c["warm_us"]))
         rec["best"] = {k: best.get(k, 0) for k in ("block_n", "split_k", "raster_group",
-                                                   "split_mode", "cta_pair")}
+                                                   "split_mode", "cta_pair", "direct_store")}
         rec["model"] = g.gemm_select_config(M, N, K, dtype, sms)
         results.append(rec)
-        del A, B, C
+        del copies
     doc = {"gpu": props.name, "sms": sms, "when": time.strftime("%Y-%m-%dT%H:%M:%SZ", time.gmtime()),
            "seconds": round(time.time() - t_start, 1),
-           "regime": "L2 flushed before each call; median of 7; warm = back-to-back mean of 20",
+           "regime": "seq: L2 flushed, R cold copies back to back, median of 5 batches; "
+                     "warm = same buffers back to back, mean of 20",
            "shapes": results}
     with open(out_path, "w") as f:
         json.dump(doc, f, indent=1)
     print("tuned %d shapes in %.1f s -> %s" % (len(results), doc["seconds"], out_path))
+
+
+def compact(full_json, out_json=TUNED_JSON):
+    """Keep, per shape, the chosen configuration and its timings (the committed record)."""
+    with open(full_json) as f:
+        doc = json.load(f)
+    head = {k: doc[k] for k in ("gpu", "sms", "when", "seconds", "regime")}
+    head["note"] = "best candidate per shape (by seq_us, then warm_us); from a full sweep output"
+    rows = []
+    for r in doc["shapes"]:
+        key = lambda c: (c["seq_us"], c["warm_us"])
+        b = min(r["candidates"], key=key)
+        plain = [c for c in r["candidates"] if c["split_k"] == 1 and not c.get("cta_pair")
+                 and not c.get("direct_store")]
+        rows.append({"M": r["M"], "N": r["N"], "K": r["K"], "dtype": r["dtype"],
+                     "best": r["best"], "seq_us": b["seq_us"], "warm_us": b["warm_us"],
+                     "plain_seq_us": min(plain, key=key)["seq_us"] if plain else None,
+                     "candidates": len(r["candidates"])})
+    with open(out_json, "w") as f:
+        f.write("{\n" + ",\n".join('"%s": %s' % (k, json.dumps(v)) for k, v in head.items()))
+        f.write(',\n"shapes": [\n' + ",\n".join(json.dumps(x) for x in rows) + "\n]}\n")
+    print("wrote %d shapes to %s" % (len(rows), out_json))
 
 
 def emit(json_path, table_path=TABLE):
@@ -134,15 +170,17 @@ def emit(json_path, table_path=TABLE):
         "// Written by dense_gemm_hgemm_gb300/tune.py from %s" % os.path.basename(json_path),
         "// (%s, %d SMs, %s; %s)." % (doc["gpu"], doc["sms"], doc["when"], doc["regime"]),
         "// Fields: M, N, K, dtype (0 f16, 1 bf16, 2 i8), block_n, split_k, raster_group,",
-        "// split_mode (0 workspace, 1 cluster), cta_pair (0 one SM, 1 SM pair).",
+        "// split_mode (0 workspace, 1 cluster), cta_pair (0 one SM, 1 SM pair),",
+        "// direct_store (0 TMA store, 1 per-thread stores).",
         "static const TableEntry kTunedTable[] = {",
     ]
     n = 0
     for r in doc["shapes"]:
         b = r["best"]
-        lines.append("    {%d, %d, %d, %d, %d, %d, %d, %d, %d}," % (
+        lines.append("    {%d, %d, %d, %d, %d, %d, %d, %d, %d, %d}," % (
             r["M"], r["N"], r["K"], code[r["dtype"]], b["block_n"], b["split_k"],
-            b["raster_group"], b.get("split_mode", 0), b.get("cta_pair", 0)))
+            b["raster_group"], b.get("split_mode", 0), b.get("cta_pair", 0),
+            b.get("direct_store", 0)))
         n += 1
     lines.append("};")
     lines.append("static const int kTunedCount = %d;" % n)
@@ -155,12 +193,16 @@ def main(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--out", default=None, help="run the sweep on the GPU and write this JSON")
     ap.add_argument("--emit", default=None, help="write the C table from this JSON")
+    ap.add_argument("--compact", default=None,
+                    help="write tuned_configs.json (chosen configs) from a full sweep JSON")
     args = ap.parse_args(argv)
     if args.out:
         sweep(args.out)
+    if args.compact:
+        compact(args.compact)
     if args.emit:
         emit(args.emit)
-    if not args.out and not args.emit:
+    if not args.out and not args.emit and not args.compact:
         ap.print_help()
         return 2
     return 0

@@ -90,6 +90,9 @@ typedef enum {
  *   cta_pair     : 1 = 256-row tiles computed by an SM pair (tcgen05 cta_group::2
  *                  thread-block cluster of two CTAs): fp16/bf16 only, block_n 128
  *                  or 256, split_k 1; 0 = 128-row tiles on one SM
+ *   direct_store : epilogue store path: 0 = TMA tensor stores from a swizzled
+ *                  shared-memory buffer; 1 = 16-byte global stores from each
+ *                  thread's row (one-SM kernel only)
  */
 typedef struct {
     int32_t block_n;
@@ -99,6 +102,7 @@ typedef struct {
     int32_t max_ctas;
     int32_t split_mode;
     int32_t cta_pair;
+    int32_t direct_store;
 } gemm_config_t;
 
 typedef struct gemm_plan *gemm_plan_t;
