@@ -106,6 +106,18 @@ def test_pair_kernel_parity(shape, bn, dtype):
     pu.check_full(A, B, dtype, C, "pair bn=%d %s %s" % (bn, shape, dtype))
 
 
+@pytest.mark.parametrize("dtype", ["f16", "bf16", "i8"])
+@pytest.mark.parametrize("shape", [(64, 4096, 64), (130, 72, 208), (257, 520, 1040)],
+                         ids=lambda s: "x".join(map(str, s)))
+def test_direct_store_epilogue_parity(shape, dtype):
+    """The per-thread 16-byte store epilogue (instead of TMA stores)."""
+    M, N, K = shape
+    A, B = inputs.make_operands(M, N, K, dtype)
+    for bn in ((64, 128) if dtype == "i8" else (64, 128, 256)):
+        C = pu.run_gpu(A, B, dtype, {"block_n": bn, "direct_store": 1})
+        pu.check_full(A, B, dtype, C, "direct store bn=%d %s %s" % (bn, shape, dtype))
+
+
 def test_default_config_headline_shapes():
     for w in (workloads.SKINNY, workloads.HEADLINE_SWEEP):
         A, B = inputs.make_operands(w.M, w.N, w.K, w.dtype, w.a_scale, w.b_scale)
