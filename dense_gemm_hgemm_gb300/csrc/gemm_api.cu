@@ -91,7 +91,8 @@ gemm_status_t normalise_config(int64_t M, int64_t N, int64_t K, gemm_dtype_t dty
     if (c.direct_store && c.cta_pair) return GEMM_ERR_INVALID_ARG;
     if (c.cta_pair) {
         // SM pair: 256-row tiles, fp16/bf16 only, no K slicing.
-        if (dtype == GEMM_I8_I32 || c.block_n < 128 || c.split_k != 1) return GEMM_ERR_INVALID_ARG;
+        if (c.block_n < 128 || c.split_k != 1) return GEMM_ERR_INVALID_ARG;
+        if (dtype == GEMM_I8_I32 && c.block_n != 128) return GEMM_ERR_INVALID_ARG;
     }
     const int want_stages =
         c.cta_pair ? gbg::default_pair_stages(c.block_n) : gbg::default_stages(c.block_n);
@@ -269,7 +270,9 @@ gemm_status_t create_plan(int64_t M, int64_t N, int64_t K, gemm_dtype_t dtype,
     const cudaError_t prep =
         cfg.cta_pair ? (p->out_kind == gbg::kOutF16
                             ? gbg::gemm_prepare_pair_f16(cfg.block_n, cfg.stages, &smem)
-                            : gbg::gemm_prepare_pair_bf16(cfg.block_n, cfg.stages, &smem))
+                        : p->out_kind == gbg::kOutBF16
+                            ? gbg::gemm_prepare_pair_bf16(cfg.block_n, cfg.stages, &smem)
+                            : gbg::gemm_prepare_pair_i32(cfg.block_n, cfg.stages, &smem))
                      : gbg::gemm_prepare(cfg.block_n, cfg.stages, p->out_kind, &smem);
     if (prep != cudaSuccess) {
         cudaGetLastError();
@@ -290,9 +293,10 @@ gemm_status_t create_plan(int64_t M, int64_t N, int64_t K, gemm_dtype_t dtype,
     kp.split_k = cfg.split_k;
     kp.cluster_split = cfg.split_mode == 1 ? 1 : 0;
     kp.kb_per_split = kb_per_split;
-    // Integer mode: chunks of 8 k-blocks (512 products of magnitude <= 2^14, so
-    // every fp32 partial sum is an integer of magnitude <= 2^23: exact).
-    kp.chunk_kb = dtype == GEMM_I8_I32 ? 8 : (kb_per_split > 0 ? kb_per_split : 1);
+    // Integer mode: chunks of 16 k-blocks (1024 products of magnitude <= 2^14, so
+    // every fp32 partial sum is an integer of magnitude <= 2^24: exactly
+    // representable, hence exact).
+    kp.chunk_kb = dtype == GEMM_I8_I32 ? 16 : (kb_per_split > 0 ? kb_per_split : 1);
     kp.raster_group = cfg.raster_group;
     kp.direct_store = cfg.direct_store;
     kp.num_units = kp.m_blocks * kp.n_blocks * kp.split_k;
@@ -326,7 +330,8 @@ gemm_status_t create_plan(int64_t M, int64_t N, int64_t K, gemm_dtype_t dtype,
     if (dtype == GEMM_I8_I32 && M > 0 && N > 0 && K > 0) {
         st = encode_kmajor(&p->map_a, p->d_a16, M, K, gbg::kBM, CU_TENSOR_MAP_DATA_TYPE_FLOAT16);
         if (st == GEMM_OK)
-            st = encode_kmajor(&p->map_b, p->d_b16, N, K, cfg.block_n, CU_TENSOR_MAP_DATA_TYPE_FLOAT16);
+            st = encode_kmajor(&p->map_b, p->d_b16, N, K, cfg.cta_pair ? cfg.block_n / 2 : cfg.block_n,
+                               CU_TENSOR_MAP_DATA_TYPE_FLOAT16);
         if (st != GEMM_OK) {
             cudaFree(p->dmem);
             delete p;
@@ -441,8 +446,11 @@ gemm_status_t gemm_run(gemm_plan_t p, const void* A, const void* B, void* C, voi
         e = p->out_kind == gbg::kOutF16
                 ? gbg::gemm_launch_pair_f16(p->cfg.block_n, p->cfg.stages, p->shape, p->map_a,
                                             p->map_b, p->map_c, p->kp, stream)
-                : gbg::gemm_launch_pair_bf16(p->cfg.block_n, p->cfg.stages, p->shape, p->map_a,
-                                             p->map_b, p->map_c, p->kp, stream);
+            : p->out_kind == gbg::kOutBF16
+                ? gbg::gemm_launch_pair_bf16(p->cfg.block_n, p->cfg.stages, p->shape, p->map_a,
+                                             p->map_b, p->map_c, p->kp, stream)
+                : gbg::gemm_launch_pair_i32(p->cfg.block_n, p->cfg.stages, p->shape, p->map_a,
+                                            p->map_b, p->map_c, p->kp, stream);
     else
         e = gbg::gemm_launch(p->cfg.block_n, p->cfg.stages, p->out_kind, p->shape, p->map_a,
                              p->map_b, p->map_c, p->kp, stream);

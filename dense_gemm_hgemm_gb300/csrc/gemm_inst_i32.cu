@@ -1,6 +1,7 @@
 // gemm_inst_i32.cu -- instantiations and launchers of the TN GEMM kernel with
 // i32 output.  Variants: (tile width BN, ring depth STAGES).
 #include "gemm_kernel.cuh"
+#include "gemm_kernel_2cta.cuh"
 #include "gemm_launch.h"
 
 namespace gbg {
@@ -41,7 +42,47 @@ cudaError_t launch_one(const LaunchShape& s, const CUtensorMap& a, const CUtenso
     return cudaLaunchKernelEx(&cfg, gemm_tn_kernel<BN, STAGES, kOutI32>, a, b, c, p);
 }
 
+template <int BN, int STAGES>
+cudaError_t prepare_pair(size_t* smem_bytes) {
+    const size_t bytes = SmemLayout2<BN, STAGES>::kTotal;
+    *smem_bytes = bytes;
+    return cudaFuncSetAttribute(gemm_tn_pair_kernel<BN, STAGES, kOutI32>,
+                                cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(bytes));
+}
+
+template <int BN, int STAGES>
+cudaError_t launch_pair(const LaunchShape& s, const CUtensorMap& a, const CUtensorMap& b,
+                        const CUtensorMap& c, const KParams& p, cudaStream_t stream) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(s.grid));
+    cfg.blockDim = dim3(static_cast<unsigned>(s.block));
+    cfg.dynamicSmemBytes = s.smem_bytes;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    attr[1].id = cudaLaunchAttributeClusterDimension;   // the SM pair
+    attr[1].val.clusterDim.x = 2;
+    attr[1].val.clusterDim.y = 1;
+    attr[1].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 2;
+    return cudaLaunchKernelEx(&cfg, gemm_tn_pair_kernel<BN, STAGES, kOutI32>, a, b, c, p);
+}
+
 }  // namespace
+
+cudaError_t gemm_prepare_pair_i32(int bn, int stages, size_t* smem_bytes) {
+    if (bn == 128 && stages == 8) return prepare_pair<128, 8>(smem_bytes);
+    return cudaErrorInvalidValue;
+}
+
+cudaError_t gemm_launch_pair_i32(int bn, int stages, const LaunchShape& s, const CUtensorMap& a,
+                                 const CUtensorMap& b, const CUtensorMap& c, const KParams& p,
+                                 cudaStream_t stream) {
+    if (bn == 128 && stages == 8) return launch_pair<128, 8>(s, a, b, c, p, stream);
+    return cudaErrorInvalidValue;
+}
 
 cudaError_t gemm_prepare_i32(int bn, int stages, size_t* smem_bytes) {
 #define X(B, S) \

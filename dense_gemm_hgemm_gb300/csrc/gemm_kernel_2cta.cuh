@@ -137,7 +137,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         const __grid_constant__ CUtensorMap tmap_c, const KParams p) {
     using L = SmemLayout2<BN, STAGES>;
     static_assert(BN == 128 || BN == 256, "pair tile width");
-    static_assert(OUT == kOutF16 || OUT == kOutBF16, "pair kernel: 16-bit outputs");
+    static_assert(OUT != kOutI32 || BN == 128, "integer mode keeps BN int32 sums in registers");
     constexpr uint32_t kTmemCols = 2 * BN;
     constexpr uint32_t kPairTx = 2 * L::kStageBytes;   // both CTAs' bytes per stage
 
@@ -262,36 +262,41 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int32_t u = pair; ok && u < p.num_units; u += npairs) {
                 const UnitCoord c = unit_coord(u, 1, p.kb_per_split, p.num_kb, p.m_blocks,
                                                p.n_blocks, p.raster_group);
-                const uint32_t buf = acc_iter & 1u;
-                const uint32_t acc_phase = (acc_iter >> 1) & 1u;
-                if (!wait_phase_cluster(smem_addr(&ctl->tmem_empty[buf]), acc_phase ^ 1u, watch,
-                                        kSiteMmaTmemEmpty)) {
-                    ok = false;
-                    break;
-                }
-                tc_fence_after();
-                const uint32_t d_tmem = tmem_base + buf * BN;
-                for (int32_t kb = c.kb_begin; kb < c.kb_end; ++kb) {
-                    if (!wait_phase(smem_addr(&ctl->full[stage]), phase, watch, kSiteMmaFull)) {
+                // One accumulation per chunk of k-blocks (the whole K range except in
+                // integer mode, where a chunk keeps every fp32 partial sum exact).
+                for (int32_t k0 = c.kb_begin; ok && k0 < c.kb_end; k0 += p.chunk_kb) {
+                    const int32_t k1 = (k0 + p.chunk_kb < c.kb_end) ? k0 + p.chunk_kb : c.kb_end;
+                    const uint32_t buf = acc_iter & 1u;
+                    const uint32_t acc_phase = (acc_iter >> 1) & 1u;
+                    if (!wait_phase_cluster(smem_addr(&ctl->tmem_empty[buf]), acc_phase ^ 1u,
+                                            watch, kSiteMmaTmemEmpty)) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
-                    const uint64_t a_desc = sw128_kmajor_desc(ring + stage * kATileBytes);
-                    const uint64_t b_desc = sw128_kmajor_desc(ring_b + stage * L::kBTileBytes);
+                    const uint32_t d_tmem = tmem_base + buf * BN;
+                    for (int32_t kb = k0; kb < k1; ++kb) {
+                        if (!wait_phase(smem_addr(&ctl->full[stage]), phase, watch, kSiteMmaFull)) {
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after();
+                        const uint64_t a_desc = sw128_kmajor_desc(ring + stage * kATileBytes);
+                        const uint64_t b_desc = sw128_kmajor_desc(ring_b + stage * L::kBTileBytes);
 #pragma unroll
-                    for (int k = 0; k < kBK / 16; ++k)
-                        umma_f16_pair(d_tmem, a_desc + 2u * k, b_desc + 2u * k, p.idesc,
-                                      (kb > c.kb_begin || k > 0) ? 1u : 0u);
-                    umma_commit_pair(smem_addr(&ctl->empty[stage]), 0x3);
-                    if (++stage == STAGES) {
-                        stage = 0;
-                        phase ^= 1u;
+                        for (int k = 0; k < kBK / 16; ++k)
+                            umma_f16_pair(d_tmem, a_desc + 2u * k, b_desc + 2u * k, p.idesc,
+                                          (kb > k0 || k > 0) ? 1u : 0u);
+                        umma_commit_pair(smem_addr(&ctl->empty[stage]), 0x3);
+                        if (++stage == STAGES) {
+                            stage = 0;
+                            phase ^= 1u;
+                        }
                     }
+                    if (!ok) break;
+                    umma_commit_pair(smem_addr(&ctl->tmem_full[buf]), 0x3);
+                    ++acc_iter;
                 }
-                if (!ok) break;
-                umma_commit_pair(smem_addr(&ctl->tmem_full[buf]), 0x3);
-                ++acc_iter;
             }
             umma_commit_pair(smem_addr(&ctl->drain), 0x1);
             wait_phase_unwind(smem_addr(&ctl->drain), 0, 100000000ull);
@@ -304,16 +309,65 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t store_buf0 = staging + static_cast<uint32_t>((warp - 2) * 2 * L::kStoreBufBytes);
         uint32_t store_sel = 0;
         uint32_t acc_iter = 0;
-        for (int32_t u = pair; u < p.num_units; u += npairs) {
+        bool ok = true;
+        for (int32_t u = pair; ok && u < p.num_units; u += npairs) {
             const UnitCoord c = unit_coord(u, 1, p.kb_per_split, p.num_kb, p.m_blocks, p.n_blocks,
                                            p.raster_group);
+            const int32_t y = c.m_blk * 2 * kBM + static_cast<int32_t>(rank) * kBM + quad * 32;
+            const int32_t col0 = c.n_blk * BN;
+            if constexpr (OUT == kOutI32) {
+                // Integer mode: round each exact fp32 chunk to int32 and add (mod 2^32).
+                uint32_t sum[BN];
+#pragma unroll
+                for (int i = 0; i < BN; ++i) sum[i] = 0u;
+                for (int32_t k0 = c.kb_begin; k0 < c.kb_end; k0 += p.chunk_kb) {
+                    const uint32_t buf = acc_iter & 1u;
+                    const uint32_t acc_phase = (acc_iter >> 1) & 1u;
+                    if (!wait_phase(smem_addr(&ctl->tmem_full[buf]), acc_phase, watch,
+                                    kSiteEpiTmemFull)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+#pragma unroll
+                    for (int j = 0; j < BN / 32; ++j) {
+                        uint32_t v[32];
+                        tmem_ld_32x32b_x32(tmem_base + lane_addr + buf * BN + j * 32, v);
+                        tmem_ld_wait();
+#pragma unroll
+                        for (int i = 0; i < 32; ++i)
+                            sum[j * 32 + i] +=
+                                static_cast<uint32_t>(__float2int_rn(__uint_as_float(v[i])));
+                    }
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive_remote(map_to_rank(smem_addr(&ctl->tmem_empty[buf]), 0));
+                    ++acc_iter;
+                }
+                if (!ok) break;
+#pragma unroll
+                for (int j = 0; j < BN / 32; ++j) {
+                    const int32_t x = col0 + j * 32;   // 32 int32 = one 128-byte buffer row
+                    if (y >= p.M || x >= p.N) continue;   // warp-uniform
+                    const uint32_t sbuf = store_buf0 + store_sel * L::kStoreBufBytes;
+                    if (lane == 0) bulk_wait_group_read<1>();
+                    __syncwarp();
+                    stage_store_row(sbuf, lane, 0, &sum[j * 32], 8);
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) {
+                        tma_store_2d(&tmap_c, sbuf, x, y);
+                        bulk_commit_group();
+                    }
+                    store_sel ^= 1u;
+                }
+                continue;
+            }
             const uint32_t buf = acc_iter & 1u;
             const uint32_t acc_phase = (acc_iter >> 1) & 1u;
             if (!wait_phase(smem_addr(&ctl->tmem_full[buf]), acc_phase, watch, kSiteEpiTmemFull))
                 break;
             tc_fence_after();
-            const int32_t y = c.m_blk * 2 * kBM + static_cast<int32_t>(rank) * kBM + quad * 32;
-            const int32_t col0 = c.n_blk * BN;
 #pragma unroll 1
             for (int sc = 0; sc < BN / 64; ++sc) {
                 const int32_t x = col0 + sc * 64;

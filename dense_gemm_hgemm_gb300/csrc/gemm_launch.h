@@ -43,6 +43,9 @@ cudaError_t gemm_prepare_pair_f16(int bn, int stages, size_t* smem_bytes);
 cudaError_t gemm_prepare_pair_bf16(int bn, int stages, size_t* smem_bytes);
 cudaError_t gemm_launch_pair_f16(int bn, int stages, const LaunchShape&, const CUtensorMap&,
                                  const CUtensorMap&, const CUtensorMap&, const KParams&, cudaStream_t);
+cudaError_t gemm_prepare_pair_i32(int bn, int stages, size_t* smem_bytes);
+cudaError_t gemm_launch_pair_i32(int bn, int stages, const LaunchShape&, const CUtensorMap&,
+                                 const CUtensorMap&, const CUtensorMap&, const KParams&, cudaStream_t);
 cudaError_t gemm_launch_pair_bf16(int bn, int stages, const LaunchShape&, const CUtensorMap&,
                                   const CUtensorMap&, const CUtensorMap&, const KParams&,
                                   cudaStream_t);

@@ -49,7 +49,7 @@ def candidates(M, N, K, dtype, sms):
             per = -(-num_kb // s) if s > 1 else 0
             if s in (2, 4, 8) and -(-num_kb // per) == s:
                 out.append({"block_n": bn, "split_k": s, "raster_group": 16, "split_mode": 1})
-        if dtype != "i8" and bn >= 128 and M > 128:
+        if (bn == 128 or (dtype != "i8" and bn == 256)) and M > 128:
             # SM pair: 256-row tiles (raster bands count 256-row blocks)
             pair_tiles = -(-M // 256) * -(-N // bn)
             groups = (4, 8, 16) if pair_tiles >= 2 * sms else (8,)
@@ -85,7 +85,7 @@ def _time(plan, copies, stream, flush, batches=5, reps_warm=20):
     return statistics.median(seq), e0.elapsed_time(e1) * 1e3 / reps_warm
 
 
-def sweep(out_path, only=None):
+def sweep(out_path, only=None, dtype=None):
     import torch
 
     import dense_gemm_hgemm_gb300 as g
@@ -100,6 +100,8 @@ def sweep(out_path, only=None):
                if (w.M, w.N, w.K, w.dtype) not in shapes]
     if only:
         shapes = [s for s in shapes if s in only]
+    if dtype:
+        shapes = [s for s in shapes if s[3] == dtype]
     results = []
     t_start = time.time()
     for M, N, K, dtype in shapes:
@@ -193,11 +195,12 @@ def main(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--out", default=None, help="run the sweep on the GPU and write this JSON")
     ap.add_argument("--emit", default=None, help="write the C table from this JSON")
+    ap.add_argument("--only", default=None, help="with --out: only shapes of this dtype")
     ap.add_argument("--compact", default=None,
                     help="write tuned_configs.json (chosen configs) from a full sweep JSON")
     args = ap.parse_args(argv)
     if args.out:
-        sweep(args.out)
+        sweep(args.out, dtype=args.only)
     if args.compact:
         compact(args.compact)
     if args.emit:

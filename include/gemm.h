@@ -88,8 +88,8 @@ typedef enum {
  *                      summed through distributed shared memory (split_k must
  *                      come out as 2, 4 or 8; one tile slice per CTA, no scratch)
  *   cta_pair     : 1 = 256-row tiles computed by an SM pair (tcgen05 cta_group::2
- *                  thread-block cluster of two CTAs): fp16/bf16 only, block_n 128
- *                  or 256, split_k 1; 0 = 128-row tiles on one SM
+ *                  thread-block cluster of two CTAs): block_n 128 or 256 (int8:
+ *                  128), split_k 1; 0 = 128-row tiles on one SM
  *   direct_store : epilogue store path: 0 = TMA tensor stores from a swizzled
  *                  shared-memory buffer; 1 = 16-byte global stores from each
  *                  thread's row (one-SM kernel only)

@@ -195,7 +195,7 @@ def test_table_covers_the_sweep_and_named_shapes(gemm_lib):
 def test_pair_config_validation(gemm_lib):
     ok = gemm_lib.gemm_workspace_bytes(4096, 4096, 4096, "f16", {"block_n": 256, "cta_pair": 1})
     assert ok > 0
-    for dtype, bad in (("i8", {"block_n": 128, "cta_pair": 1}),
+    for dtype, bad in (("i8", {"block_n": 256, "cta_pair": 1}),
                        ("f16", {"block_n": 64, "cta_pair": 1}),
                        ("f16", {"block_n": 256, "cta_pair": 1, "split_k": 2}),
                        ("f16", {"block_n": 256, "cta_pair": 1, "stages": 4}),

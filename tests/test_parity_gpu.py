@@ -150,6 +150,44 @@ def test_int8_extremes_k4096():
     pu.check_full(A, B, "i8", pu.run_gpu(A, B, "i8", {"block_n": 128}), "i8 extremes")
 
 
+@pytest.mark.parametrize("shape", [(256, 128, 1024), (300, 264, 1040), (1000, 520, 4096)],
+                         ids=lambda s: "x".join(map(str, s)))
+def test_int8_pair_kernel_bit_exact(shape):
+    """Integer mode on an SM pair: chunked exact fp32 accumulation drained to int32."""
+    M, N, K = shape
+    A, B = inputs.make_operands(M, N, K, "i8")
+    C = pu.run_gpu(A, B, "i8", {"block_n": 128, "cta_pair": 1}, repeats=2)
+    pu.check_full(A, B, "i8", C, "i8 pair %s" % (shape,))
+
+
+@pytest.mark.parametrize("cfg", [{"block_n": 64}, {"block_n": 128}, {"block_n": 128, "cta_pair": 1}],
+                         ids=["bn64", "bn128", "pair"])
+def test_int8_small_addend_at_top_of_range(cfg):
+    """Per 1024-long K chunk: 1023 products of 2^14 then one product of 1, i.e. a
+    partial sum of 2^24 - 2^14 + 1 that needs all 24 significand bits of the fp32
+    accumulator (a narrower internal adder drops the +1); other rows mix signs."""
+    K = 4096
+    A = torch.full((256, K), -128, dtype=torch.int8)
+    B = torch.full((128, K), -128, dtype=torch.int8)
+    for c in range(K // 1024):
+        A[:, c * 1024 + 1023] = 1
+        B[:, c * 1024 + 1023] = 1
+    A[1::2, ::2] = 127                       # odd rows: alternating large mixed-sign products
+    C = pu.run_gpu(A, B, "i8", cfg).cpu()
+    assert torch.all(C[0::2] == 4 * (1023 * 16384 + 1))
+    pu.check_full(A, B, "i8", C, "small addend %s" % cfg)
+
+
+def test_int8_pair_kernel_extremes():
+    K = 4096
+    A = torch.full((384, K), -128, dtype=torch.int8)
+    B = torch.full((256, K), -128, dtype=torch.int8)
+    B[1::2] = 127
+    C = pu.run_gpu(A, B, "i8", {"block_n": 128, "cta_pair": 1}).cpu()
+    assert torch.all(C[:, 0::2] == K * 16384)
+    assert torch.all(C[:, 1::2] == -128 * 127 * K)
+
+
 def test_int8_split_k():
     A, B = inputs.make_operands(128, 128, 4096, "i8")
     C = pu.run_gpu(A, B, "i8", {"block_n": 64, "split_k": 4})
