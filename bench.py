@@ -384,7 +384,7 @@ def named_workloads(stream, peaks, floor_us, sms):
     return out
 
 
-def cpu_oracle_sample(budget_s: float = 15.0, rows: int = 16):
+def cpu_oracle_sample(budget_s: float = 15.0, rows: int = 64):
     """Time the CPU oracle on rows [0, rows) of the sweep's shapes, in seeded
     random shape order, until `budget_s` seconds of work; TFLOP/s achieved."""
     import numpy as np
@@ -518,10 +518,14 @@ def ours(args):
         head = workloads.HEADLINE_SWEEP.name.replace("hgemm_tn_", "sweep_").replace("_f16", "_f16")
         line["sweep_roofline"] = {
             "launch_floor_us": round(floor, 3),
-            "t_meas_us_sum": round(t_meas, 1), "t_roof_us_sum": round(t_roof, 1),
-            "frac": round(t_roof / t_meas, 4), "by_bound": classes,
+            "t_roof_us_sum": round(t_roof, 1),
+            "frac_of_timed_step": round(t_roof / (ms_step * 1e3), 4),
+            "t_meas_us_sum_isolated": round(t_meas, 1),
+            "frac_isolated": round(t_roof / t_meas, 4), "by_bound_isolated": classes,
             "rule": "per shape t_roof = max(2MNK/bf16 burst peak, compulsory bytes/HBM, "
-                    "empty-kernel launch floor); per-launch device times from events",
+                    "launch floor of an empty kernel launched like the GEMM); "
+                    "frac_of_timed_step = sum t_roof / timed ms_per_step; *_isolated = each "
+                    "launch timed alone between events (no launch overlap)",
             "headline_128x2048x128_us_in_sweep": round(times.get("sweep_128x2048x128_f16", 0) * 1e3, 3),
         }
         e2e_ms, h2d, d2h = e2e_sweep(items, stream, steps=max(3, min(20, args.steps)))
