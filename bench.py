@@ -384,6 +384,47 @@ def named_workloads(stream, peaks, floor_us, sms):
     return out
 
 
+def server_mode(stream, calls=2000):
+    """Back-to-back 64x4096x64 fp16 GEMMs (the pages' inference-server shape):
+    calls/s issued one gemm_run at a time, and replayed from a captured CUDA graph."""
+    import dense_gemm_hgemm_gb300 as g
+    w = workloads.SKINNY
+    gen = torch.Generator(device="cuda")
+    gen.manual_seed(inputs.shape_seed(w.M, w.N, w.K, w.dtype))
+    A = torch.randn(w.M, w.K, generator=gen, device="cuda").half()
+    B = torch.randn(w.N, w.K, generator=gen, device="cuda").half()
+    C = torch.empty(w.M, w.N, device="cuda", dtype=torch.float16)
+    out = {}
+    with g.Plan(w.M, w.N, w.K, w.dtype) as plan:
+        for _ in range(50):
+            plan.run(A, B, C, stream)
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        for _ in range(calls):
+            plan.run(A, B, C, stream)
+        torch.cuda.synchronize()
+        out["eager_calls_per_s"] = round(calls / (time.perf_counter() - t0), 1)
+        per_graph = 100
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=stream):
+            for _ in range(per_graph):
+                plan.run(A, B, C, torch.cuda.current_stream())
+        for _ in range(3):
+            graph.replay()
+        torch.cuda.synchronize()
+        reps = max(1, calls // per_graph)
+        t0 = time.perf_counter()
+        for _ in range(reps):
+            graph.replay()
+        torch.cuda.synchronize()
+        out["graph_calls_per_s"] = round(reps * per_graph / (time.perf_counter() - t0), 1)
+        plan.check(stream)
+    out["shape"] = [w.M, w.N, w.K, w.dtype]
+    out["note"] = ("host wall clock over %d calls; eager = one gemm_run (ctypes) per call, "
+                   "graph = %d captured calls per replay" % (calls, per_graph))
+    return out
+
+
 def cpu_oracle_sample(budget_s: float = 15.0, rows: int = 64):
     """Time the CPU oracle on rows [0, rows) of the sweep's shapes, in seeded
     random shape order, until `budget_s` seconds of work; TFLOP/s achieved."""
@@ -537,6 +578,7 @@ def ours(args):
         del items
         torch.cuda.empty_cache()
         line["named"] = named_workloads(stream, peaks, floor, sms)
+        line["server_mode"] = server_mode(stream)
         line["cpu_baseline"] = cpu_oracle_sample()
     if dist.rank == 0:
         print(json.dumps(line), flush=True)

@@ -56,6 +56,14 @@ inline gemm_config_t model_config(int64_t M, int64_t N, int64_t K, gemm_dtype_t 
             c.block_n = bn;
         }
     }
+    // Many 256-row tiles: SM pairs (each SM streams half of B; measured ~15%
+    // faster than one-SM tiles on the large shapes of the sweep).
+    if (dtype != GEMM_I8_I32 && mb >= 2 && ceil_div(M, 2 * kBM) * ceil_div(N, 256) >= sms) {
+        c.block_n = 256;
+        c.cta_pair = 1;
+        c.raster_group = 8;
+        return c;
+    }
     // Few output tiles and a long K: one SM streams only ~110 GB/s, so slice K
     // over a cluster of 2/4/8 CTAs per tile (reduced in distributed shared memory).
     const int64_t tiles = mb * ceil_div(N, c.block_n);
