@@ -378,6 +378,26 @@ def named_workloads(stream, peaks, floor_us, sms):
         if w.dtype == "i8":
             out[w.name]["note"] = ("int8 runs on the fp16 tensor path (sm_103a has no tcgen05 "
                                    "kind::i8); peak is the fp16/bf16 rate")
+        if w is workloads.FFN_BF16:
+            # The same shape with the linear-layer epilogue fused: C = GELU(A B^T + bias).
+            bias = torch.randn(w.N, generator=gen, device="cuda").float()
+            with g.Plan(w.M, w.N, w.K, w.dtype) as plan:
+                for _ in range(5):
+                    plan.run(A, B, C, stream, bias=bias, act=g.ACT_GELU)
+                samples = []
+                for _ in range(5):
+                    e0.record(stream)
+                    for _ in range(reps):
+                        plan.run(A, B, C, stream, bias=bias, act=g.ACT_GELU)
+                    e1.record(stream)
+                    torch.cuda.synchronize()
+                    samples.append(e0.elapsed_time(e1) * 1e3 / reps)
+                plan.check(stream)
+            us2 = statistics.median(samples)
+            out[w.name + "_bias_gelu"] = {
+                "M": w.M, "N": w.N, "K": w.K, "dtype": w.dtype, "epilogue": "bias + GELU fused",
+                "us_per_call": round(us2, 3), "TFLOPS": round(w.flops / (us2 * 1e-6) / 1e12, 2),
+                "overhead_vs_plain": round(us2 / us - 1.0, 4)}
         del A, B, C
     del flush
     torch.cuda.empty_cache()

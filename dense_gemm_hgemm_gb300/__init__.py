@@ -17,6 +17,7 @@ from ._build import LIB_PATH, build_library
 __all__ = [
     "GEMM_F16", "GEMM_BF16", "GEMM_I8_I32", "GEMM_LAYOUT_TN", "GemmError", "Plan",
     "build_library", "gemm_plan_create", "gemm_plan_create_with_config", "gemm_run",
+    "gemm_run_bias_act", "ACTIVATIONS",
     "gemm_plan_check", "gemm_plan_destroy", "gemm_plan_get_config", "gemm_plan_set_timeout",
     "gemm_plan_set_wait_test",
     "gemm_select_config", "gemm_tile_coords", "gemm_workspace_bytes", "gemm_status_string",
@@ -72,6 +73,7 @@ def library() -> ctypes.CDLL:
                 "gemm_plan_create_with_config": ([i64, i64, i64, i32, i32, cfgp,
                                                   ctypes.POINTER(vp)], i32),
                 "gemm_run": ([vp, vp, vp, vp, vp], i32),
+                "gemm_run_bias_act": ([vp, vp, vp, vp, vp, i32, vp], i32),
                 "gemm_plan_check": ([vp, vp], i32),
                 "gemm_plan_destroy": ([vp], i32),
                 "gemm_plan_get_config": ([vp, cfgp], i32),
@@ -178,6 +180,17 @@ def gemm_run(plan: int, A, B, C, stream=None) -> None:
     _check(library().gemm_run(plan, _ptr(A), _ptr(B), _ptr(C), _stream(stream)), "gemm_run")
 
 
+ACT_NONE, ACT_RELU, ACT_GELU, ACT_SILU = 0, 1, 2, 3
+ACTIVATIONS = {"none": ACT_NONE, "relu": ACT_RELU, "gelu": ACT_GELU, "silu": ACT_SILU}
+
+
+def gemm_run_bias_act(plan: int, A, B, C, bias=None, act=ACT_NONE, stream=None) -> None:
+    """C = act(A @ B.T + bias) with the bias (N fp32 values or None) and activation fused."""
+    a = ACTIVATIONS[act] if isinstance(act, str) else int(act)
+    _check(library().gemm_run_bias_act(plan, _ptr(A), _ptr(B), _ptr(C), _ptr(bias), a,
+                                       _stream(stream)), "gemm_run_bias_act")
+
+
 def gemm_plan_check(plan: int, stream=None) -> None:
     _check(library().gemm_plan_check(plan, _stream(stream)), "gemm_plan_check")
 
@@ -235,8 +248,11 @@ class Plan:
     def config(self) -> dict:
         return gemm_plan_get_config(self.handle)
 
-    def run(self, A, B, C, stream=None) -> None:
-        gemm_run(self.handle, A, B, C, stream)
+    def run(self, A, B, C, stream=None, bias=None, act=ACT_NONE) -> None:
+        if bias is None and act in (ACT_NONE, "none"):
+            gemm_run(self.handle, A, B, C, stream)
+        else:
+            gemm_run_bias_act(self.handle, A, B, C, bias, act, stream)
 
     def check(self, stream=None) -> None:
         gemm_plan_check(self.handle, stream)

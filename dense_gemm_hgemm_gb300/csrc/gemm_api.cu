@@ -384,7 +384,16 @@ gemm_status_t gemm_plan_create_with_config(int64_t M, int64_t N, int64_t K, gemm
 }
 
 gemm_status_t gemm_run(gemm_plan_t p, const void* A, const void* B, void* C, void* stream_ptr) {
+    return gemm_run_bias_act(p, A, B, C, nullptr, GEMM_ACT_NONE, stream_ptr);
+}
+
+gemm_status_t gemm_run_bias_act(gemm_plan_t p, const void* A, const void* B, void* C,
+                                const float* bias, gemm_activation_t act, void* stream_ptr) {
     if (!p) return GEMM_ERR_INVALID_ARG;
+    if (act < GEMM_ACT_NONE || act > GEMM_ACT_SILU) return GEMM_ERR_INVALID_ARG;
+    if (p->dtype == GEMM_I8_I32 && (bias != nullptr || act != GEMM_ACT_NONE))
+        return GEMM_ERR_UNSUPPORTED;
+    if (reinterpret_cast<uintptr_t>(bias) & 15u) return GEMM_ERR_ALIGNMENT;
     if (p->M == 0 || p->N == 0) return GEMM_OK;
     if (!C || (p->K > 0 && (!A || !B))) return GEMM_ERR_INVALID_ARG;
     if ((reinterpret_cast<uintptr_t>(A) | reinterpret_cast<uintptr_t>(B) |
@@ -400,7 +409,11 @@ gemm_status_t gemm_run(gemm_plan_t p, const void* A, const void* B, void* C, voi
     const int64_t out_bytes = p->M * p->N * (p->dtype == GEMM_I8_I32 ? 4 : 2);
 
     if (p->K == 0) {
-        if (gbg::launch_zero_fill(C, out_bytes, p->num_sms, stream) != cudaSuccess) {
+        const cudaError_t e =
+            bias ? gbg::launch_fill_bias_act(C, p->M, p->N, bias, static_cast<int>(act),
+                                             p->dtype == GEMM_BF16 ? 1 : 0, p->num_sms, stream)
+                 : gbg::launch_zero_fill(C, out_bytes, p->num_sms, stream);   // act(0) = 0
+        if (e != cudaSuccess) {
             cudaGetLastError();
             return GEMM_ERR_LAUNCH;
         }
@@ -441,6 +454,8 @@ gemm_status_t gemm_run(gemm_plan_t p, const void* A, const void* B, void* C, voi
         p->map_c_valid = true;
     }
     p->kp.C = C;
+    p->kp.bias = bias;
+    p->kp.act = static_cast<int32_t>(act);
     cudaError_t e;
     if (p->cfg.cta_pair)
         e = p->out_kind == gbg::kOutF16

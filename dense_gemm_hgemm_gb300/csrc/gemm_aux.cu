@@ -1,10 +1,12 @@
 // gemm_aux.cu -- small HBM-bound kernels around the GEMM:
 //   * widen_i8: int8 operands -> fp16 copies (every int8 value is exact in fp16),
 //     the input side of the integer mode of the tensor-core kernel;
-//   * zero_fill: C = 0 for K == 0 (the empty sum);
+//   * zero_fill: C = 0 for K == 0 (the empty sum); fill_bias_act: C = act(bias)
+//     for K == 0 with a bias;
 //   * empty: a kernel with no body, for measuring the launch-latency floor.
 // Both are grid-stride loops over 16-byte vectors sized to a whole number of
 // waves of the SMs.
+#include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <stdint.h>
 
@@ -60,6 +62,30 @@ __global__ void __launch_bounds__(256) zero_fill_kernel(uint4* __restrict__ dst,
         dst[i] = make_uint4(0u, 0u, 0u, 0u);
 }
 
+// K == 0 with a bias: every row of C is act(bias) (the empty sum is 0).
+__device__ __forceinline__ float act_of(float x, int act) {
+    switch (act) {
+        case 1: return fmaxf(x, 0.0f);
+        case 2: return 0.5f * x * (1.0f + erff(x * 0.70710678118654752f));
+        case 3: return x / (1.0f + expf(-x));
+        default: return x;
+    }
+}
+
+__global__ void __launch_bounds__(256) fill_bias_act_kernel(void* __restrict__ C, int64_t M,
+                                                            int64_t N, const float* __restrict__ bias,
+                                                            int act, int bf16) {
+    const int64_t total = M * N;
+    const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+    for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < total; i += stride) {
+        const float v = act_of(bias[i % N], act);
+        if (bf16)
+            reinterpret_cast<__nv_bfloat16*>(C)[i] = __float2bfloat16_rn(v);
+        else
+            reinterpret_cast<__half*>(C)[i] = __float2half_rn(v);
+    }
+}
+
 int grid_for(int64_t work_items, int num_sms) {
     const int64_t per_wave = static_cast<int64_t>(num_sms) * 8;    // 8 x 256 threads per SM
     int64_t blocks = (work_items + 255) / 256;
@@ -92,6 +118,12 @@ cudaError_t launch_empty(int grid, cudaStream_t stream) {
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     return cudaLaunchKernelEx(&cfg, empty_kernel);
+}
+
+cudaError_t launch_fill_bias_act(void* C, int64_t M, int64_t N, const float* bias, int act,
+                                 int bf16, int num_sms, cudaStream_t stream) {
+    fill_bias_act_kernel<<<grid_for(M * N, num_sms), 256, 0, stream>>>(C, M, N, bias, act, bf16);
+    return cudaGetLastError();
 }
 
 cudaError_t launch_zero_fill(void* dst, int64_t bytes, int num_sms, cudaStream_t stream) {

@@ -303,6 +303,34 @@ __device__ __forceinline__ uint32_t pack2(float lo, float hi) {
     }
 }
 
+// Fused epilogue of a linear layer, in fp32 before the output conversion:
+// x = act(x + bias[col]).
+__device__ __forceinline__ float activation(float x, int32_t act) {
+    switch (act) {
+        case 1: return fmaxf(x, 0.0f);
+        case 2: return 0.5f * x * (1.0f + erff(x * 0.70710678118654752f));   // x * Phi(x)
+        case 3: return x / (1.0f + expf(-x));
+        default: return x;
+    }
+}
+
+// v holds fp32 bits for columns [col, col + 4*G); N % 8 == 0, so a group of 4
+// columns is entirely inside or outside C.
+template <int G>
+__device__ __forceinline__ void apply_bias_act(uint32_t* v, const KParams& p, int32_t col) {
+    if (p.bias == nullptr && p.act == 0) return;
+#pragma unroll
+    for (int g = 0; g < G; ++g) {
+        float4 b = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (p.bias != nullptr && col + g * 4 < p.N)
+            b = __ldg(reinterpret_cast<const float4*>(p.bias + col + g * 4));
+        v[g * 4 + 0] = __float_as_uint(activation(__uint_as_float(v[g * 4 + 0]) + b.x, p.act));
+        v[g * 4 + 1] = __float_as_uint(activation(__uint_as_float(v[g * 4 + 1]) + b.y, p.act));
+        v[g * 4 + 2] = __float_as_uint(activation(__uint_as_float(v[g * 4 + 2]) + b.z, p.act));
+        v[g * 4 + 3] = __float_as_uint(activation(__uint_as_float(v[g * 4 + 3]) + b.w, p.act));
+    }
+}
+
 // Store 32 fp32 values (as bits) of row `row`, columns [col, col+32) as fp16/bf16.
 template <int OUT>
 __device__ __forceinline__ void store_half_row32(void* C, int32_t N, int32_t row, int32_t col,
@@ -458,6 +486,7 @@ __device__ __forceinline__ void cluster_reduce_store(const KParams& p, const Uni
         for (int s = 0; s < 8; ++s)
             if (s < S) add_u4<OUT>(v, q[s]);
         const int64_t idx = static_cast<int64_t>(grow) * p.N + gcol;
+        if constexpr (OUT != kOutI32) apply_bias_act<1>(v, p, gcol);
         if constexpr (OUT == kOutI32) {
             *reinterpret_cast<uint4*>(reinterpret_cast<uint32_t*>(p.C) + idx) =
                 make_uint4(v[0], v[1], v[2], v[3]);
@@ -760,10 +789,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                         if (cluster) {
                             stage_row32<BN>(ring, row_in_tile, j * 32, v);
                         } else if (row < p.M) {
-                            if (split)
+                            if (split) {
                                 store_ws32(ws_row + j * 32, v);
-                            else
+                            } else {
+                                apply_bias_act<8>(v, p, col0 + j * 32);
                                 store_half_row32<OUT>(p.C, p.N, row, col0 + j * 32, v);
+                            }
                         }
                     }
                 } else {
@@ -783,6 +814,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                             uint32_t v[32];
                             tmem_ld_32x32b_x32(tmem_base + lane_addr + buf * BN + sc * 64 + h * 32, v);
                             tmem_ld_wait();
+                            apply_bias_act<8>(v, p, x + h * 32);
                             uint32_t w[16];
 #pragma unroll
                             for (int i = 0; i < 16; ++i)
@@ -834,6 +866,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         if constexpr (OUT == kOutI32) {
                             store_i32_row32(p.C, p.N, row, col0 + j * 32, v);
                         } else {
+                            apply_bias_act<8>(v, p, col0 + j * 32);
                             store_half_row32<OUT>(p.C, p.N, row, col0 + j * 32, v);
                         }
                     }

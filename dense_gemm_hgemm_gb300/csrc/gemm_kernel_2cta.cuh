@@ -380,6 +380,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     uint32_t v[32];
                     tmem_ld_32x32b_x32(tmem_base + lane_addr + buf * BN + sc * 64 + h * 32, v);
                     tmem_ld_wait();
+                    apply_bias_act<8>(v, p, x + h * 32);
                     uint32_t w[16];
 #pragma unroll
                     for (int i = 0; i < 16; ++i)

@@ -36,6 +36,8 @@ struct KParams {
     int32_t num_units;      // m_blocks * n_blocks * split_k
     uint32_t idesc;         // tcgen05 instruction descriptor
     uint32_t tx_extra;      // extra bytes each ring slot expects (0 in normal operation)
+    const float* bias;      // per-column bias (N fp32 values) or null
+    int32_t act;            // 0 none, 1 ReLU, 2 GELU (erf), 3 SiLU: C = act(A B^T + bias)
     void* C;
     void* workspace;        // split-K partials: [num_units][kBM][BN] fp32 (int32 in integer mode)
     uint32_t* counters;     // split-K arrival counter per tile (self-resetting)

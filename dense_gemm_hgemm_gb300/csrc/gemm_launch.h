@@ -55,5 +55,7 @@ cudaError_t launch_widen_i8(const int8_t* a, int64_t na, const int8_t* b, int64_
                             void* b16, int num_sms, cudaStream_t stream);
 cudaError_t launch_zero_fill(void* dst, int64_t bytes, int num_sms, cudaStream_t stream);
 cudaError_t launch_empty(int grid, cudaStream_t stream);
+cudaError_t launch_fill_bias_act(void* C, int64_t M, int64_t N, const float* bias, int act,
+                                 int bf16, int num_sms, cudaStream_t stream);
 
 }  // namespace gbg

@@ -107,6 +107,14 @@ typedef struct {
 
 typedef struct gemm_plan *gemm_plan_t;
 
+/* Activation of the fused epilogue (gemm_run_bias_act). */
+typedef enum {
+    GEMM_ACT_NONE = 0,
+    GEMM_ACT_RELU = 1,   /* max(x, 0) */
+    GEMM_ACT_GELU = 2,   /* x * Phi(x), Phi = standard normal CDF (erf form) */
+    GEMM_ACT_SILU = 3    /* x / (1 + exp(-x)) */
+} gemm_activation_t;
+
 /*
  * Create a plan.  Validates the arguments (sizes >= 0; K a multiple of 8 for
  * fp16/bf16 and of 16 for int8 so that A and B rows are 16-byte aligned; N a
@@ -134,6 +142,20 @@ gemm_status_t gemm_plan_create_with_config(int64_t M, int64_t N, int64_t K, gemm
  * gemm_plan_check or the CUDA stream.
  */
 gemm_status_t gemm_run(gemm_plan_t plan, const void *A, const void *B, void *C, void *stream);
+
+/*
+ * Linear-layer epilogue fused into the GEMM (fp16/bf16 plans):
+ *     C[i][j] = act(sum_k A[i][k] * B[j][k] + bias[j])
+ * evaluated in fp32 before the conversion to the output type.  bias: device
+ * pointer to N fp32 values, 16-byte aligned, or NULL (no bias); act: a
+ * gemm_activation_t.  Otherwise as gemm_run.  The pages list the order of
+ * fused operations among the tuning dimensions of the HGEMM kernels ("RL驱动
+ * CUDA L2 GEMM内核自动调优", paragraph on tile size and fusion order) without
+ * naming them; bias + activation is what follows FFN-shaped GEMMs.
+ * int8 plans return GEMM_ERR_UNSUPPORTED unless bias is NULL and act is NONE.
+ */
+gemm_status_t gemm_run_bias_act(gemm_plan_t plan, const void *A, const void *B, void *C,
+                                const float *bias, gemm_activation_t act, void *stream);
 
 /*
  * Synchronise `stream`, then read and clear the plan's device error word.

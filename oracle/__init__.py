@@ -75,6 +75,10 @@ def _load():
             lib.oracle_gemm_tn_i8_sampled.argtypes = [p, p, i64, i64, i64, p, p, i64, p, p,
                                                       ctypes.c_int]
             lib.oracle_gemm_tn_i8_sampled.restype = ctypes.c_int
+            lib.oracle_epilogue.argtypes = [p, i64, i64, p, ctypes.c_int]
+            lib.oracle_epilogue.restype = ctypes.c_int
+            lib.oracle_epilogue_sampled.argtypes = [p, p, i64, p, ctypes.c_int]
+            lib.oracle_epilogue_sampled.restype = ctypes.c_int
             _lib = lib
     return _lib
 
@@ -162,3 +166,28 @@ def gemm_tn_i8_sampled(A, B, rows, cols, threads: int = 0):
     if rc != 0:
         raise RuntimeError("oracle_gemm_tn_i8_sampled failed")
     return o64, o32
+
+
+ACT_NONE, ACT_RELU, ACT_GELU, ACT_SILU = 0, 1, 2, 3
+
+
+def epilogue(C: np.ndarray, bias, act: int) -> np.ndarray:
+    """act(C + bias[None, :]) in fp64 on a copy of the fp64 GEMM result C[M,N]."""
+    out = np.array(C, dtype=np.float64, copy=True, order="C")
+    b = None if bias is None else np.ascontiguousarray(bias, dtype=np.float32)
+    rc = _load().oracle_epilogue(_ptr(out), out.shape[0], out.shape[1],
+                                 None if b is None else _ptr(b), act)
+    if rc != 0:
+        raise RuntimeError("oracle_epilogue failed")
+    return out
+
+
+def epilogue_sampled(vals: np.ndarray, cols, bias, act: int) -> np.ndarray:
+    out = np.array(vals, dtype=np.float64, copy=True)
+    cols = np.ascontiguousarray(cols, dtype=np.int64)
+    b = None if bias is None else np.ascontiguousarray(bias, dtype=np.float32)
+    rc = _load().oracle_epilogue_sampled(_ptr(out), _ptr(cols), out.size,
+                                         None if b is None else _ptr(b), act)
+    if rc != 0:
+        raise RuntimeError("oracle_epilogue_sampled failed")
+    return out

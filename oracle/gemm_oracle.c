@@ -199,3 +199,41 @@ int oracle_gemm_tn_i8_sampled(const int8_t *A, const int8_t *B, int64_t M, int64
     }
     return 0;
 }
+
+/*
+ * Fused epilogue of a linear layer: C[i][j] = act(C[i][j] + bias[j]) in fp64, applied to
+ * the GEMM result above (bias: N values, may be NULL).  act: 0 none, 1 ReLU max(x, 0),
+ * 2 GELU x * Phi(x) with Phi the standard normal CDF = (1 + erf(x / sqrt 2)) / 2,
+ * 3 SiLU x / (1 + exp(-x)).  The GEMM post on RL-driven tuning counts the order of fused
+ * operations among its tuning dimensions (paragraph on tile size and fusion order) without
+ * naming the operations; these are the ones that follow FFN-shaped GEMMs.
+ */
+static double apply_act(double x, int act)
+{
+    switch (act) {
+        case 1: return x > 0.0 ? x : 0.0;
+        case 2: return 0.5 * x * (1.0 + erf(x / sqrt(2.0)));
+        case 3: return x / (1.0 + exp(-x));
+        default: return x;
+    }
+}
+
+int oracle_epilogue(double *C, int64_t M, int64_t N, const float *bias, int act)
+{
+    if (M < 0 || N < 0 || act < 0 || act > 3) return -1;
+    for (int64_t i = 0; i < M; ++i)
+        for (int64_t j = 0; j < N; ++j) {
+            const double x = C[i * N + j] + (bias ? (double)bias[j] : 0.0);
+            C[i * N + j] = apply_act(x, act);
+        }
+    return 0;
+}
+
+/* The same at sampled positions: out[t] = act(C[rows[t]][cols[t]] + bias[cols[t]]). */
+int oracle_epilogue_sampled(double *vals, const int64_t *cols, int64_t n, const float *bias, int act)
+{
+    if (n < 0 || act < 0 || act > 3) return -1;
+    for (int64_t t = 0; t < n; ++t)
+        vals[t] = apply_act(vals[t] + (bias ? (double)bias[cols[t]] : 0.0), act);
+    return 0;
+}

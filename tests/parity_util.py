@@ -93,3 +93,16 @@ def check_sampled(A: torch.Tensor, B: torch.Tensor, dtype: str, C_gpu: torch.Ten
         return 0.0
     ref = oracle.gemm_tn_half_sampled(bits(A), bits(B), fmt(dtype), rows.numpy(), cols.numpy())
     return assert_close_half(got.float().numpy(), ref, K, where)
+
+
+def run_gpu_epilogue(A, B, dtype, config, bias, act):
+    """C = act(A @ B.T + bias) through gemm_run_bias_act."""
+    import dense_gemm_hgemm_gb300 as g
+    M, K = A.shape
+    N = B.shape[0]
+    C = torch.empty(M, N, dtype=inputs.OUT_DTYPE[dtype], device="cuda")
+    db = None if bias is None else bias.cuda()
+    with g.Plan(M, N, K, dtype, config) as plan:
+        plan.run(A.cuda(), B.cuda(), C, bias=db, act=act)
+        plan.check()
+    return C

@@ -337,3 +337,42 @@ def test_oracle_mutants_are_caught(tmp_path, name):
         Be = inputs.make_operands(7, 7, 7, "f16" if fmt == 0 else "bf16")[1]
         caught |= not np.array_equal(gemm(_bits(Ae), _bits(Be), fmt), Be.double().numpy().T)
     assert caught, name
+
+
+# ---------------------------------------------------------------------------
+# fused epilogue act(C + bias): closed forms
+# ---------------------------------------------------------------------------
+
+def test_epilogue_closed_forms(oracle_mod):
+    C = np.array([[0.0, 1.0, -1.0, 2.0]])
+    bias = np.array([0.0, 0.0, 0.0, -2.0], np.float32)
+    assert np.array_equal(oracle_mod.epilogue(C, bias, 0), [[0.0, 1.0, -1.0, 0.0]])
+    assert np.array_equal(oracle_mod.epilogue(C, None, 1), [[0.0, 1.0, 0.0, 2.0]])
+    g = oracle_mod.epilogue(C, None, 2)[0]
+    # GELU(x) = x * Phi(x): Phi(0) = 1/2, Phi(1) = 0.8413447460685429 (standard normal table)
+    assert g[0] == 0.0 and abs(g[1] - 0.8413447460685429) < 1e-15
+    assert abs(g[2] - (-1.0) * (1 - 0.8413447460685429)) < 1e-15
+    s = oracle_mod.epilogue(C, None, 3)[0]
+    # SiLU(x) = x * sigmoid(x): sigmoid(1) = e / (1 + e)
+    assert s[0] == 0.0 and abs(s[1] - np.e / (1 + np.e)) < 1e-15
+    assert abs(s[2] - (-1.0) / (1 + np.e)) < 1e-15      # sigmoid(-1) = 1/(1+e)
+
+
+def test_epilogue_bias_is_per_column(oracle_mod):
+    C = np.zeros((3, 4))
+    bias = np.array([1, -2, 3, -4], np.float32)
+    out = oracle_mod.epilogue(C, bias, 1)
+    assert np.array_equal(out, np.tile([[1.0, 0.0, 3.0, 0.0]], (3, 1)))
+    vals = oracle_mod.epilogue_sampled(np.zeros(4), [3, 2, 1, 0], bias, 0)
+    assert np.array_equal(vals, [-4.0, 3.0, -2.0, 1.0])
+
+
+def test_epilogue_symmetries(oracle_mod):
+    x = np.linspace(-6, 6, 241)[None, :]
+    g = oracle_mod.epilogue(x, None, 2)[0]
+    # GELU(x) - GELU(-x) = x  (since Phi(x) + Phi(-x) = 1)
+    assert np.allclose(g - g[::-1], x[0], atol=1e-14, rtol=0)
+    s = oracle_mod.epilogue(x, None, 3)[0]
+    assert np.allclose(s - s[::-1], x[0], atol=1e-14, rtol=0)   # sigmoid(x) + sigmoid(-x) = 1
+    with pytest.raises(RuntimeError):
+        oracle_mod.epilogue(x, None, 9)
