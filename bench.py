@@ -59,6 +59,8 @@ def parse_args(argv=None):
                     help="only the timed sweep (no e2e, named workloads or CPU baseline)")
     ap.add_argument("--ncu-steps", type=int, default=0,
                     help="run this many untimed steps and exit (for profiler launch lists)")
+    ap.add_argument("--tma-sweep", action="store_true",
+                    help="run the TMA load-mode x FMA-intensity experiment and print its table")
     ap.add_argument("--shape", default=None,
                     help="with --ncu-steps: run only this workload, 'M,N,K,dtype' (profiling)")
     return ap.parse_args(argv)
@@ -661,8 +663,47 @@ def reference(args):
     print(json.dumps(line), flush=True)
 
 
+def tma_sweep():
+    """The tutorial page's experiment on this GPU: n = 4 Mi floats, 4 KiB tiles, 64 tiles per
+    256-thread block; CUDA-event median of 25 launches per (mode, fma_iters)."""
+    import dense_gemm_hgemm_gb300 as g
+    g.build_library()
+    n = 4_194_304
+    x = torch.randn(n, device="cuda")
+    y = torch.empty_like(x)
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    stream = torch.cuda.Stream()
+    modes = ("sync", "bulk1d", "tensor2d", "pipe2")
+    rows = []
+    for iters in (1, 2, 4, 8, 16, 32, 64, 128, 256):
+        rec = {"fma_iters": iters}
+        for m in modes:
+            for _ in range(3):
+                g.tma_intensity_run(m, iters, 0.999, 0.001, x, y, 2048, err, stream)
+            ts = []
+            for _ in range(25):
+                e0 = torch.cuda.Event(enable_timing=True)
+                e1 = torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                g.tma_intensity_run(m, iters, 0.999, 0.001, x, y, 2048, err, stream)
+                e1.record(stream)
+                torch.cuda.synchronize()
+                ts.append(e0.elapsed_time(e1))
+            rec[m + "_ms"] = round(statistics.median(ts), 5)
+        for m in modes[1:]:
+            rec["speedup_" + m] = round(rec["sync_ms"] / rec[m + "_ms"], 3)
+        rows.append(rec)
+    assert int(err.item()) == 0
+    print(json.dumps({"experiment": "tma_intensity", "gpu": torch.cuda.get_device_name(0),
+                      "n": n, "tile_bytes": 4096, "tiles_per_block": 64, "block": 256,
+                      "blocks": n // 65536, "timing": "CUDA-event median of 25", "rows": rows}))
+
+
 def main(argv=None):
     args = parse_args(argv)
+    if args.tma_sweep:
+        tma_sweep()
+        return
     if args.warmup < 3 and not args.ncu_steps:
         print("warning: fewer than 3 warm-up steps", file=sys.stderr)
     if args.impl == "reference":

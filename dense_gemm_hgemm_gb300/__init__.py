@@ -17,7 +17,7 @@ from ._build import LIB_PATH, build_library
 __all__ = [
     "GEMM_F16", "GEMM_BF16", "GEMM_I8_I32", "GEMM_LAYOUT_TN", "GemmError", "Plan",
     "build_library", "gemm_plan_create", "gemm_plan_create_with_config", "gemm_run",
-    "gemm_run_bias_act", "ACTIVATIONS",
+    "gemm_run_bias_act", "ACTIVATIONS", "tma_intensity_run", "TMA_MODES",
     "gemm_plan_check", "gemm_plan_destroy", "gemm_plan_get_config", "gemm_plan_set_timeout",
     "gemm_plan_set_wait_test",
     "gemm_select_config", "gemm_tile_coords", "gemm_workspace_bytes", "gemm_status_string",
@@ -87,6 +87,8 @@ def library() -> ctypes.CDLL:
                 "gemm_abi_version": ([], i32),
                 "gemm_launch_empty": ([i32, vp], i32),
                 "gemm_run_splitk_noalloc": ([i64, i64, i64, i32, i32, vp, vp, vp, vp], i32),
+                "tma_intensity_run": ([i32, i32, ctypes.c_float, ctypes.c_float, vp, vp, i64, i32,
+                                       vp, vp], i32),
             }
             for name, (args, res) in sig.items():
                 fn = getattr(lib, name)
@@ -158,6 +160,18 @@ def gemm_run_splitk_noalloc(M: int, N: int, K: int, dtype, split_k: int, A, B, C
     _check(library().gemm_run_splitk_noalloc(M, N, K, _dtype_code(dtype), int(split_k), _ptr(A),
                                              _ptr(B), _ptr(C), _stream(stream)),
            "gemm_run_splitk_noalloc")
+
+
+TMA_MODES = {"sync": 0, "bulk1d": 1, "tensor2d": 2, "pipe2": 3}
+
+
+def tma_intensity_run(mode, fma_iters: int, a: float, b: float, x, y, cols: int = 2048,
+                      error_word=None, stream=None) -> None:
+    """The TMA load-mode x FMA-intensity experiment (see include/tma_intensity.h)."""
+    m = TMA_MODES[mode] if isinstance(mode, str) else int(mode)
+    _check(library().tma_intensity_run(m, int(fma_iters), float(a), float(b), _ptr(x), _ptr(y),
+                                       x.numel() if hasattr(x, "numel") else int(x), int(cols),
+                                       _ptr(error_word), _stream(stream)), "tma_intensity_run")
 
 
 def gemm_plan_create(M: int, N: int, K: int, dtype="f16", layout: int = GEMM_LAYOUT_TN) -> int:

@@ -18,7 +18,7 @@ BUILD_DIR = os.path.join(ROOT, "_build")
 LIB_PATH = os.path.join(PKG, "libgemm_gb300.so")
 
 SOURCES = ["gemm_api.cu", "gemm_aux.cu", "gemm_inst_f16.cu", "gemm_inst_bf16.cu",
-           "gemm_inst_i32.cu", "gemm_noalloc.cu"]
+           "gemm_inst_i32.cu", "gemm_noalloc.cu", "tma_intensity.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 
@@ -34,7 +34,7 @@ def _flags(extra=()):
 
 def _deps():
     files = [os.path.join(CSRC, f) for f in os.listdir(CSRC)]
-    files.append(os.path.join(INCLUDE, "gemm.h"))
+    files += [os.path.join(INCLUDE, f) for f in os.listdir(INCLUDE)]
     files.append(os.path.abspath(__file__))
     return files
 

@@ -79,6 +79,9 @@ def _load():
             lib.oracle_epilogue.restype = ctypes.c_int
             lib.oracle_epilogue_sampled.argtypes = [p, p, i64, p, ctypes.c_int]
             lib.oracle_epilogue_sampled.restype = ctypes.c_int
+            lib.oracle_fma_chain.argtypes = [p, p, i64, ctypes.c_int, ctypes.c_float,
+                                             ctypes.c_float]
+            lib.oracle_fma_chain.restype = ctypes.c_int
             _lib = lib
     return _lib
 
@@ -190,4 +193,14 @@ def epilogue_sampled(vals: np.ndarray, cols, bias, act: int) -> np.ndarray:
                                          None if b is None else _ptr(b), act)
     if rc != 0:
         raise RuntimeError("oracle_epilogue_sampled failed")
+    return out
+
+
+def fma_chain(x: np.ndarray, iters: int, a: float, b: float) -> np.ndarray:
+    """y = x, then iters times y = fma(y, a, b) in fp32 (single rounding), elementwise."""
+    x = np.ascontiguousarray(x, dtype=np.float32)
+    out = np.empty_like(x)
+    rc = _load().oracle_fma_chain(_ptr(x), _ptr(out), x.size, iters, a, b)
+    if rc != 0:
+        raise RuntimeError("oracle_fma_chain failed")
     return out

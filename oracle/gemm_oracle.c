@@ -237,3 +237,22 @@ int oracle_epilogue_sampled(double *vals, const int64_t *cols, int64_t n, const 
         vals[t] = apply_act(vals[t] + (bias ? (double)bias[cols[t]] : 0.0), act);
     return 0;
 }
+
+/*
+ * TMA intensity experiment ("B-08. Hopper TMA：从单线程 Bulk Copy 到吞吐墙", sections 5 and
+ * 5.2): every element x of the input passes through `iters` fused multiply-adds,
+ * y <- fma(y, a, b) starting from y = x, and lands at the same index of the output.  The
+ * page fixes the workload (4 KiB tiles, a sweep over the FMA count) but not the arithmetic
+ * constants; a and b are arguments.  fmaf is the single-rounding fp32 fused multiply-add of
+ * C99, so the result is bit-defined.
+ */
+int oracle_fma_chain(const float *in, float *out, int64_t n, int iters, float a, float b)
+{
+    if (n < 0 || iters < 0) return -1;
+    for (int64_t t = 0; t < n; ++t) {
+        float y = in[t];
+        for (int i = 0; i < iters; ++i) y = fmaf(y, a, b);
+        out[t] = y;
+    }
+    return 0;
+}

@@ -12,9 +12,12 @@ HAS_GPU = torch.cuda.is_available()
 
 
 def _declared_functions():
-    text = open(os.path.join(ROOT, "include", "gemm.h"), encoding="utf-8").read()
-    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
-    return sorted(set(re.findall(r"\b(gemm_[a-z_0-9]+)\s*\(", text)))
+    names = set()
+    for h in os.listdir(os.path.join(ROOT, "include")):
+        text = open(os.path.join(ROOT, "include", h), encoding="utf-8").read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        names |= set(re.findall(r"\b((?:gemm|tma)_[a-z_0-9]+)\s*\(", text))
+    return sorted(names)
 
 
 def test_header_declares_the_boundary():

@@ -376,3 +376,20 @@ def test_epilogue_symmetries(oracle_mod):
     assert np.allclose(s - s[::-1], x[0], atol=1e-14, rtol=0)   # sigmoid(x) + sigmoid(-x) = 1
     with pytest.raises(RuntimeError):
         oracle_mod.epilogue(x, None, 9)
+
+
+# ---------------------------------------------------------------------------
+# fma chain of the TMA intensity experiment
+# ---------------------------------------------------------------------------
+
+def test_fma_chain_closed_form_and_single_rounding(oracle_mod):
+    x = np.array([0.0, 1.0, -2.0, 3.5], np.float32)
+    assert np.array_equal(oracle_mod.fma_chain(x, 0, 0.5, 1.0), x)
+    # a = 1/2, b = 1: exact in fp32, y_k = 2 + (x - 2) / 2^k
+    for k in (1, 2, 5):
+        assert np.array_equal(oracle_mod.fma_chain(x, k, 0.5, 1.0),
+                              (2.0 + (x.astype(np.float64) - 2.0) / 2 ** k).astype(np.float32))
+    # fused: fma(1 + 2^-23, 1 - 2^-23, -1) = -2^-46 exactly (a separate multiply rounds it to 0)
+    one_p = np.float32(1 + 2 ** -23)
+    y = oracle_mod.fma_chain(np.array([one_p], np.float32), 1, float(np.float32(1 - 2 ** -23)), -1.0)
+    assert y[0] == np.float32(-(2.0 ** -46))
