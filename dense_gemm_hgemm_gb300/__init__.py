@@ -15,7 +15,8 @@ import threading
 from ._build import LIB_PATH, build_library
 
 __all__ = [
-    "GEMM_F16", "GEMM_BF16", "GEMM_I8_I32", "GEMM_LAYOUT_TN", "GemmError", "Plan",
+    "GEMM_F16", "GEMM_BF16", "GEMM_I8_I32", "GEMM_LAYOUT_TN", "GEMM_LAYOUT_NN", "GEMM_LAYOUT_TT",
+    "GEMM_LAYOUT_NT", "LAYOUTS", "GemmError", "Plan",
     "build_library", "gemm_plan_create", "gemm_plan_create_with_config", "gemm_run",
     "gemm_run_bias_act", "ACTIVATIONS", "tma_intensity_run", "TMA_MODES",
     "gemm_plan_check", "gemm_plan_destroy", "gemm_plan_get_config", "gemm_plan_set_timeout",
@@ -25,7 +26,8 @@ __all__ = [
 ]
 
 GEMM_F16, GEMM_BF16, GEMM_I8_I32 = 0, 1, 2
-GEMM_LAYOUT_TN = 0
+GEMM_LAYOUT_TN, GEMM_LAYOUT_NN, GEMM_LAYOUT_TT, GEMM_LAYOUT_NT = 0, 1, 2, 3
+LAYOUTS = {"TN": GEMM_LAYOUT_TN, "NN": GEMM_LAYOUT_NN, "TT": GEMM_LAYOUT_TT, "NT": GEMM_LAYOUT_NT}
 DTYPES = {"f16": GEMM_F16, "bf16": GEMM_BF16, "i8": GEMM_I8_I32}
 
 STATUS_NAMES = {
@@ -253,10 +255,11 @@ def gemm_workspace_bytes(M, N, K, dtype, config) -> int:
 class Plan:
     """Owning wrapper of a plan handle: ``with Plan(M, N, K, "f16") as p: p.run(A, B, C)``."""
 
-    def __init__(self, M: int, N: int, K: int, dtype="f16", config=None):
+    def __init__(self, M: int, N: int, K: int, dtype="f16", config=None, layout=GEMM_LAYOUT_TN):
         self.M, self.N, self.K, self.dtype = M, N, K, dtype
-        self.handle = (gemm_plan_create(M, N, K, dtype) if config is None
-                       else gemm_plan_create_with_config(M, N, K, dtype, config))
+        lay = LAYOUTS[layout] if isinstance(layout, str) else int(layout)
+        self.handle = (gemm_plan_create(M, N, K, dtype, lay) if config is None
+                       else gemm_plan_create_with_config(M, N, K, dtype, config, lay))
 
     @property
     def config(self) -> dict:

@@ -35,6 +35,7 @@ struct PlanMemory {
 struct gemm_plan {
     int64_t M, N, K;
     gemm_dtype_t dtype;
+    gemm_layout_t layout;
     gemm_config_t cfg;          // effective configuration
     int device;
     int num_sms;
@@ -57,16 +58,21 @@ struct gemm_plan {
 
 namespace {
 
+bool a_mn_major(gemm_layout_t l) { return l == GEMM_LAYOUT_TT || l == GEMM_LAYOUT_NT; }
+bool b_mn_major(gemm_layout_t l) { return l == GEMM_LAYOUT_NN || l == GEMM_LAYOUT_NT; }
+
 gemm_status_t validate_shape(int64_t M, int64_t N, int64_t K, gemm_dtype_t dtype,
                              gemm_layout_t layout) {
     if (dtype != GEMM_F16 && dtype != GEMM_BF16 && dtype != GEMM_I8_I32) return GEMM_ERR_UNSUPPORTED;
-    if (layout != GEMM_LAYOUT_TN) return GEMM_ERR_UNSUPPORTED;
+    if (layout < GEMM_LAYOUT_TN || layout > GEMM_LAYOUT_NT) return GEMM_ERR_UNSUPPORTED;
     if (M < 0 || N < 0 || K < 0) return GEMM_ERR_INVALID_ARG;
     if (M > INT32_MAX || N > INT32_MAX || K > INT32_MAX) return GEMM_ERR_INVALID_ARG;
     const bool i8 = dtype == GEMM_I8_I32;
-    // Row strides must be multiples of 16 bytes: K * in_bytes for A and B,
-    // N * out_bytes for C.
-    if (K % (i8 ? 16 : 8) != 0) return GEMM_ERR_ALIGNMENT;
+    // Stored rows must be multiples of 16 bytes: the contiguous extent of A
+    // (K, or M when A is stored K x M) and of B (K, or N), and N * out_bytes for C.
+    const int64_t in_mult = i8 ? 16 : 8;
+    if ((a_mn_major(layout) ? M : K) % in_mult != 0) return GEMM_ERR_ALIGNMENT;
+    if ((b_mn_major(layout) ? N : K) % in_mult != 0) return GEMM_ERR_ALIGNMENT;
     if (N % (i8 ? 4 : 8) != 0) return GEMM_ERR_ALIGNMENT;
     // Work-decomposition indices are 32-bit.
     const int64_t tiles = ((M + gbg::kBM - 1) / gbg::kBM) * ((N + 63) / 64);
@@ -193,6 +199,30 @@ gemm_status_t encode_output(CUtensorMap* map, void* base, int64_t M, int64_t N, 
     return r == CUDA_SUCCESS ? GEMM_OK : GEMM_ERR_TENSORMAP;
 }
 
+// Map over an operand stored K x rows (rows contiguous): boxes of 64 rows-elements
+// (128 bytes) x 64 K-rows with 128-byte swizzle, the M/N-major tile blocks the
+// kernels' descriptors expect.
+gemm_status_t encode_mnmajor(CUtensorMap* map, const void* base, int64_t rows, int64_t K,
+                             CUtensorMapDataType dt) {
+    PFN_cuTensorMapEncodeTiled_v12000 fn = encode_fn();
+    if (!fn) return GEMM_ERR_TENSORMAP;
+    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(rows), static_cast<cuuint64_t>(K)};
+    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(rows) * 2};
+    const cuuint32_t box[2] = {64, static_cast<cuuint32_t>(gbg::kBK)};
+    const cuuint32_t estr[2] = {1, 1};
+    const CUresult r = fn(map, dt, 2, const_cast<void*>(base), dims, strides, box, estr,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? GEMM_OK : GEMM_ERR_TENSORMAP;
+}
+
+// Map for operand A (rows = M) or B (rows = N) in the plan's storage.
+gemm_status_t encode_operand_map(CUtensorMap* map, const void* base, int64_t rows, int64_t K,
+                                 int box_rows, bool mn_major, CUtensorMapDataType dt) {
+    return mn_major ? encode_mnmajor(map, base, rows, K, dt)
+                    : encode_kmajor(map, base, rows, K, box_rows, dt);
+}
+
 CUtensorMapDataType operand_type(gemm_dtype_t dt) {
     return dt == GEMM_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
 }
@@ -244,6 +274,7 @@ gemm_status_t create_plan(int64_t M, int64_t N, int64_t K, gemm_dtype_t dtype,
     p->N = N;
     p->K = K;
     p->dtype = dtype;
+    p->layout = layout;
     p->cfg = cfg;
     p->device = dev;
     p->num_sms = sms;
@@ -299,10 +330,14 @@ gemm_status_t create_plan(int64_t M, int64_t N, int64_t K, gemm_dtype_t dtype,
     kp.chunk_kb = dtype == GEMM_I8_I32 ? 16 : (kb_per_split > 0 ? kb_per_split : 1);
     kp.raster_group = cfg.raster_group;
     kp.direct_store = cfg.direct_store;
+    kp.a_mn_major = a_mn_major(layout) ? 1 : 0;
+    kp.b_mn_major = b_mn_major(layout) ? 1 : 0;
     kp.num_units = kp.m_blocks * kp.n_blocks * kp.split_k;
     const uint32_t fmt = dtype == GEMM_BF16 ? 1u : 0u;
     kp.idesc = (1u << 4)                                         // D: fp32
                | (fmt << 7) | (fmt << 10)                        // A, B: fp16 or bf16
+               | (static_cast<uint32_t>(kp.a_mn_major) << 15)    // A M-major
+               | (static_cast<uint32_t>(kp.b_mn_major) << 16)    // B N-major
                | (static_cast<uint32_t>(cfg.block_n >> 3) << 17)  // N / 8
                | (static_cast<uint32_t>(tile_m >> 4) << 24);      // M / 16 (128, or 256 for a pair)
     kp.tx_extra = 0;
@@ -328,10 +363,12 @@ gemm_status_t create_plan(int64_t M, int64_t N, int64_t K, gemm_dtype_t dtype,
     p->shape.smem_bytes = smem;
 
     if (dtype == GEMM_I8_I32 && M > 0 && N > 0 && K > 0) {
-        st = encode_kmajor(&p->map_a, p->d_a16, M, K, gbg::kBM, CU_TENSOR_MAP_DATA_TYPE_FLOAT16);
+        st = encode_operand_map(&p->map_a, p->d_a16, M, K, gbg::kBM, a_mn_major(layout),
+                                CU_TENSOR_MAP_DATA_TYPE_FLOAT16);
         if (st == GEMM_OK)
-            st = encode_kmajor(&p->map_b, p->d_b16, N, K, cfg.cta_pair ? cfg.block_n / 2 : cfg.block_n,
-                               CU_TENSOR_MAP_DATA_TYPE_FLOAT16);
+            st = encode_operand_map(&p->map_b, p->d_b16, N, K,
+                                    cfg.cta_pair ? cfg.block_n / 2 : cfg.block_n,
+                                    b_mn_major(layout), CU_TENSOR_MAP_DATA_TYPE_FLOAT16);
         if (st != GEMM_OK) {
             cudaFree(p->dmem);
             delete p;
@@ -431,7 +468,8 @@ gemm_status_t gemm_run_bias_act(gemm_plan_t p, const void* A, const void* B, voi
         const CUtensorMapDataType dt = operand_type(p->dtype);
         if (!p->map_a_valid || p->map_a_src != A) {
             p->map_a_valid = false;
-            const gemm_status_t st = encode_kmajor(&p->map_a, A, p->M, p->K, gbg::kBM, dt);
+            const gemm_status_t st =
+                encode_operand_map(&p->map_a, A, p->M, p->K, gbg::kBM, a_mn_major(p->layout), dt);
             if (st != GEMM_OK) return st;
             p->map_a_src = A;
             p->map_a_valid = true;
@@ -440,7 +478,8 @@ gemm_status_t gemm_run_bias_act(gemm_plan_t p, const void* A, const void* B, voi
             p->map_b_valid = false;
             // an SM pair loads half of the tile's B rows per CTA
             const int b_rows = p->cfg.cta_pair ? p->cfg.block_n / 2 : p->cfg.block_n;
-            const gemm_status_t st = encode_kmajor(&p->map_b, B, p->N, p->K, b_rows, dt);
+            const gemm_status_t st =
+                encode_operand_map(&p->map_b, B, p->N, p->K, b_rows, b_mn_major(p->layout), dt);
             if (st != GEMM_OK) return st;
             p->map_b_src = B;
             p->map_b_valid = true;

@@ -261,6 +261,45 @@ __device__ __forceinline__ uint64_t sw128_kmajor_desc(uint32_t saddr) {
            | (static_cast<uint64_t>(2) << 61);               // swizzle mode: 128 B
 }
 
+// Shared-memory descriptor for an MN-major operand tile written by TMA as
+// 64-element (128-byte) wide blocks of 64 K-rows (8 KiB each, 128-byte swizzle):
+// 8-row K groups 1024 bytes apart (stride byte offset), 64-element MN blocks
+// 8 KiB apart (leading byte offset).
+__device__ __forceinline__ uint64_t sw128_mnmajor_desc(uint32_t saddr) {
+    return static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4)
+           | (static_cast<uint64_t>(8192 >> 4) << 16)       // leading byte offset: next 64 MN
+           | (static_cast<uint64_t>(1024 >> 4) << 32)       // stride byte offset: next 8 K rows
+           | (static_cast<uint64_t>(1) << 46)
+           | (static_cast<uint64_t>(2) << 61);
+}
+__device__ __forceinline__ uint64_t operand_desc(uint32_t saddr, int32_t mn_major) {
+    return mn_major ? sw128_mnmajor_desc(saddr) : sw128_kmajor_desc(saddr);
+}
+// Descriptor advance per K=16 MMA: 32 bytes along a K-major row, or 16 rows of
+// 128 bytes of an MN-major tile (start address is encoded >> 4).
+__device__ __forceinline__ uint32_t desc_k_step(int32_t mn_major) { return mn_major ? 128u : 2u; }
+
+// One operand tile (`rows` rows of M or N by 64 K) of k-block kb into `dst`:
+// K-major = one box {64 K, rows}; MN-major = rows/64 boxes {64 MN, 64 K}, 8 KiB apart.
+__device__ __forceinline__ void load_operand(uint32_t dst, const CUtensorMap* map, uint32_t bar,
+                                             int32_t kb, int32_t row0, int32_t rows,
+                                             int32_t mn_major) {
+    if (!mn_major) {
+        tma_load_2d(dst, map, bar, kb * kBK, row0);
+        return;
+    }
+    for (int32_t i = 0; i < rows / 64; ++i)
+        tma_load_2d(dst + static_cast<uint32_t>(i) * 8192u, map, bar, row0 + i * 64, kb * kBK);
+}
+__device__ __forceinline__ void prefetch_operand(const CUtensorMap* map, int32_t kb, int32_t row0,
+                                                 int32_t rows, int32_t mn_major) {
+    if (!mn_major) {
+        tma_prefetch_l2_2d(map, kb * kBK, row0);
+        return;
+    }
+    for (int32_t i = 0; i < rows / 64; ++i) tma_prefetch_l2_2d(map, row0 + i * 64, kb * kBK);
+}
+
 // 32 lanes x 32 consecutive 32-bit TMEM columns -> 32 registers per thread.
 __device__ __forceinline__ void tmem_ld_32x32b_x32(uint32_t taddr, uint32_t (&r)[32]) {
     asm volatile(
@@ -584,8 +623,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                                        p.m_blocks, p.n_blocks, p.raster_group);
         const int32_t kb_end = c.kb_begin + STAGES < c.kb_end ? c.kb_begin + STAGES : c.kb_end;
         for (int32_t kb = c.kb_begin; kb < kb_end; ++kb) {
-            tma_prefetch_l2_2d(&tmap_a, kb * kBK, c.m_blk * kBM);
-            tma_prefetch_l2_2d(&tmap_b, kb * kBK, c.n_blk * BN);
+            prefetch_operand(&tmap_a, kb, c.m_blk * kBM, kBM, p.a_mn_major);
+            prefetch_operand(&tmap_b, kb, c.n_blk * BN, BN, p.b_mn_major);
         }
     }
     grid_dependency_wait();
@@ -610,9 +649,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                         break;
                     }
                     mbar_arrive_expect_tx(full, kStageTx + p.tx_extra);
-                    tma_load_2d(ring + stage * kATileBytes, &tmap_a, full, kb * kBK, c.m_blk * kBM);
-                    tma_load_2d(ring_b + stage * L::kBTileBytes, &tmap_b, full, kb * kBK,
-                                c.n_blk * BN);
+                    load_operand(ring + stage * kATileBytes, &tmap_a, full, kb, c.m_blk * kBM, kBM,
+                                 p.a_mn_major);
+                    load_operand(ring_b + stage * L::kBTileBytes, &tmap_b, full, kb, c.n_blk * BN,
+                                 BN, p.b_mn_major);
                     ++issued;
                     if (++stage == STAGES) {
                         stage = 0;
@@ -665,12 +705,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                             break;
                         }
                         tc_fence_after();
-                        const uint64_t a_desc = sw128_kmajor_desc(ring + stage * kATileBytes);
-                        const uint64_t b_desc = sw128_kmajor_desc(ring_b + stage * L::kBTileBytes);
+                        const uint64_t a_desc = operand_desc(ring + stage * kATileBytes, p.a_mn_major);
+                        const uint64_t b_desc =
+                            operand_desc(ring_b + stage * L::kBTileBytes, p.b_mn_major);
+                        const uint32_t a_step = desc_k_step(p.a_mn_major);
+                        const uint32_t b_step = desc_k_step(p.b_mn_major);
 #pragma unroll
                         for (int k = 0; k < kBK / 16; ++k) {
-                            // +32 bytes along K per instruction (encoded >> 4)
-                            umma_f16(d_tmem, a_desc + 2u * k, b_desc + 2u * k, p.idesc,
+                            umma_f16(d_tmem, a_desc + a_step * k, b_desc + b_step * k, p.idesc,
                                      (kb > k0 || k > 0) ? 1u : 0u);
                         }
                         umma_commit(smem_addr(&ctl->empty[stage]));

@@ -87,6 +87,19 @@ __device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap
         : "memory");
 }
 
+// load_operand for the pair kernel (bytes counted on the leader's barrier).
+__device__ __forceinline__ void load_operand_pair(uint32_t dst, const CUtensorMap* map,
+                                                  uint32_t bar_cluster, int32_t kb, int32_t row0,
+                                                  int32_t rows, int32_t mn_major) {
+    if (!mn_major) {
+        tma_load_2d_pair(dst, map, bar_cluster, kb * kBK, row0);
+        return;
+    }
+    for (int32_t i = 0; i < rows / 64; ++i)
+        tma_load_2d_pair(dst + static_cast<uint32_t>(i) * 8192u, map, bar_cluster, row0 + i * 64,
+                         kb * kBK);
+}
+
 __device__ __forceinline__ void mbar_arrive_remote(uint32_t bar_cluster) {
     asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(bar_cluster)
                  : "memory");
@@ -197,8 +210,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                                        p.raster_group);
         const int32_t kb_end = STAGES < c.kb_end ? STAGES : c.kb_end;
         for (int32_t kb = 0; kb < kb_end; ++kb) {
-            tma_prefetch_l2_2d(&tmap_a, kb * kBK, c.m_blk * 2 * kBM + static_cast<int32_t>(rank) * kBM);
-            tma_prefetch_l2_2d(&tmap_b, kb * kBK, c.n_blk * BN + static_cast<int32_t>(rank) * (BN / 2));
+            prefetch_operand(&tmap_a, kb, c.m_blk * 2 * kBM + static_cast<int32_t>(rank) * kBM, kBM,
+                             p.a_mn_major);
+            prefetch_operand(&tmap_b, kb, c.n_blk * BN + static_cast<int32_t>(rank) * (BN / 2),
+                             BN / 2, p.b_mn_major);
         }
     }
     grid_dependency_wait();
@@ -225,9 +240,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const uint32_t full_local = smem_addr(&ctl->full[stage]);
                     if (leader) mbar_arrive_expect_tx(full_local, kPairTx + p.tx_extra);
                     const uint32_t full_lead = map_to_rank(full_local, 0);
-                    tma_load_2d_pair(ring + stage * kATileBytes, &tmap_a, full_lead, kb * kBK, a_row);
-                    tma_load_2d_pair(ring_b + stage * L::kBTileBytes, &tmap_b, full_lead, kb * kBK,
-                                     b_row);
+                    load_operand_pair(ring + stage * kATileBytes, &tmap_a, full_lead, kb, a_row, kBM,
+                                      p.a_mn_major);
+                    load_operand_pair(ring_b + stage * L::kBTileBytes, &tmap_b, full_lead, kb, b_row,
+                                      BN / 2, p.b_mn_major);
                     ++issued;
                     if (++stage == STAGES) {
                         stage = 0;
@@ -281,11 +297,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                             break;
                         }
                         tc_fence_after();
-                        const uint64_t a_desc = sw128_kmajor_desc(ring + stage * kATileBytes);
-                        const uint64_t b_desc = sw128_kmajor_desc(ring_b + stage * L::kBTileBytes);
+                        const uint64_t a_desc = operand_desc(ring + stage * kATileBytes, p.a_mn_major);
+                        const uint64_t b_desc =
+                            operand_desc(ring_b + stage * L::kBTileBytes, p.b_mn_major);
+                        const uint32_t a_step = desc_k_step(p.a_mn_major);
+                        const uint32_t b_step = desc_k_step(p.b_mn_major);
 #pragma unroll
                         for (int k = 0; k < kBK / 16; ++k)
-                            umma_f16_pair(d_tmem, a_desc + 2u * k, b_desc + 2u * k, p.idesc,
+                            umma_f16_pair(d_tmem, a_desc + a_step * k, b_desc + b_step * k, p.idesc,
                                           (kb > k0 || k > 0) ? 1u : 0u);
                         umma_commit_pair(smem_addr(&ctl->empty[stage]), 0x3);
                         if (++stage == STAGES) {

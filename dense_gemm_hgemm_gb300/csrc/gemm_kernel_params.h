@@ -33,6 +33,8 @@ struct KParams {
     int32_t chunk_kb;       // k-blocks per accumulation chunk (integer mode), else >= kb_per_split
     int32_t raster_group;
     int32_t direct_store;   // 1: epilogue stores C with 16-byte st.global per thread; 0: TMA stores
+    int32_t a_mn_major;     // 1: A stored K x M (M contiguous); 0: M x K (K contiguous)
+    int32_t b_mn_major;     // 1: B stored K x N (N contiguous); 0: N x K (K contiguous)
     int32_t num_units;      // m_blocks * n_blocks * split_k
     uint32_t idesc;         // tcgen05 instruction descriptor
     uint32_t tx_extra;      // extra bytes each ring slot expects (0 in normal operation)

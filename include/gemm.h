@@ -9,7 +9,9 @@
  * along K: the "row-major A, column-major B" layout of the HGEMM kernels in
  * "RL驱动CUDA L2 GEMM内核自动调优：A100/H100 tile size与融合优化", paragraph on tile
  * size and data layout) and C an M x N row-major matrix that is overwritten
- * (no alpha/beta, C is never read).
+ * (no alpha/beta, C is never read).  Other operand storages (B stored K x N, A
+ * stored K x M) are selected with gemm_layout_t: the kernels then load
+ * M/N-contiguous tiles and use M/N-major shared-memory matrix descriptors.
  *
  *   GEMM_F16    : fp16 A, B;  fp32 accumulation;  fp16 C (round to nearest even)
  *   GEMM_BF16   : bf16 A, B;  fp32 accumulation;  bf16 C (round to nearest even)
@@ -54,8 +56,15 @@ typedef enum {
     GEMM_I8_I32 = 2
 } gemm_dtype_t;
 
+/*
+ * Operand storage.  C is always M x N row-major; the math is always
+ * C[i][j] = sum_k a(i,k) * b(k,j) with a, b the logical M x K and K x N operands.
+ */
 typedef enum {
-    GEMM_LAYOUT_TN = 0   /* A[M,K] row-major, B[N,K] row-major, C[M,N] row-major */
+    GEMM_LAYOUT_TN = 0,  /* A stored M x K, B stored N x K (both K contiguous): C = A * B^T */
+    GEMM_LAYOUT_NN = 1,  /* A stored M x K, B stored K x N (N contiguous):      C = A * B   */
+    GEMM_LAYOUT_TT = 2,  /* A stored K x M (M contiguous), B stored N x K:      C = A^T * B^T */
+    GEMM_LAYOUT_NT = 3   /* A stored K x M, B stored K x N:                     C = A^T * B */
 } gemm_layout_t;
 
 typedef enum {
@@ -116,10 +125,11 @@ typedef enum {
 } gemm_activation_t;
 
 /*
- * Create a plan.  Validates the arguments (sizes >= 0; K a multiple of 8 for
- * fp16/bf16 and of 16 for int8 so that A and B rows are 16-byte aligned; N a
- * multiple of 8 for fp16/bf16 and of 4 for int8 so that C rows are 16-byte
- * aligned), checks the current device is an sm_103 part, picks the kernel
+ * Create a plan.  Validates the arguments (sizes >= 0; every stored row of A,
+ * B and C a multiple of 16 bytes: for fp16/bf16 the contiguous dimension of A
+ * and of B (K for TN, M or N for the other layouts) a multiple of 8 and N a
+ * multiple of 8; for int8 multiples of 16 and N of 4), checks the current
+ * device is an sm_103 part, picks the kernel
  * configuration from the built-in table and allocates the plan's scratch
  * memory.  On success *plan receives a handle that gemm_plan_destroy frees.
  * Row-stride rule: "TMA/2D tensor" alignment of "B-08. Hopper TMA：从单线程 Bulk

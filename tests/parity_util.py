@@ -106,3 +106,24 @@ def run_gpu_epilogue(A, B, dtype, config, bias, act):
         plan.run(A.cuda(), B.cuda(), C, bias=db, act=act)
         plan.check()
     return C
+
+
+def stored(A: torch.Tensor, B: torch.Tensor, layout: str):
+    """A[M,K], B[N,K] (the logical TN operands) in the storage of `layout`."""
+    a = A.T.contiguous() if layout in ("TT", "NT") else A
+    b = B.T.contiguous() if layout in ("NN", "NT") else B
+    return a, b
+
+
+def run_gpu_layout(A, B, dtype, config, layout):
+    """C = A @ B.T computed from A, B stored as `layout` prescribes."""
+    import dense_gemm_hgemm_gb300 as g
+    M, K = A.shape
+    N = B.shape[0]
+    a, b = stored(A, B, layout)
+    C = torch.empty(M, N, dtype=inputs.OUT_DTYPE[dtype], device="cuda")
+    with g.Plan(M, N, K, dtype, config, layout=layout) as plan:
+        plan.run(a.cuda(), b.cuda(), C)
+        plan.run(a.cuda(), b.cuda(), C)
+        plan.check()
+    return C

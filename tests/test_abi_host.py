@@ -61,7 +61,10 @@ def _create_status(g, M, N, K, dtype, layout=0):
 
 @pytest.mark.parametrize("args,expect", [
     ((64, 64, 64, 7, 0), 2),        # unknown dtype
-    ((64, 64, 64, 0, 1), 2),        # unknown layout
+    ((64, 64, 64, 0, 4), 2),        # unknown layout
+    ((60, 64, 64, 0, 2), 3),        # A stored K x M: M*2 bytes not a multiple of 16
+    ((64, 60, 64, 0, 1), 3),        # B stored K x N: N*2 bytes not a multiple of 16
+    ((64, 64, 60, 0, 3), 0 if HAS_GPU else 4),   # NT: K is never a stored row; passes validation
     ((-1, 64, 64, 0, 0), 1),        # negative M
     ((64, -8, 64, 0, 0), 1),
     ((64, 64, -8, 1, 0), 1),
