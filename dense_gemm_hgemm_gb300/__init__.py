@@ -19,7 +19,8 @@ __all__ = [
     "GEMM_LAYOUT_NT", "LAYOUTS", "GemmError", "Plan",
     "build_library", "gemm_plan_create", "gemm_plan_create_with_config", "gemm_run",
     "gemm_run_bias_act", "ACTIVATIONS", "tma_intensity_run", "TMA_MODES",
-    "gemm_plan_check", "gemm_plan_destroy", "gemm_plan_get_config", "gemm_plan_set_timeout",
+    "gemm_plan_check", "gemm_plan_destroy", "gemm_plan_get_config", "gemm_plan_get_launch",
+    "gemm_plan_set_timeout",
     "gemm_plan_set_wait_test",
     "gemm_select_config", "gemm_tile_coords", "gemm_workspace_bytes", "gemm_status_string",
     "gemm_abi_version", "gemm_launch_empty", "gemm_run_splitk_noalloc", "library", "DTYPES",
@@ -49,7 +50,8 @@ class gemm_config_t(ctypes.Structure):
     _fields_ = [("block_n", ctypes.c_int32), ("stages", ctypes.c_int32),
                 ("split_k", ctypes.c_int32), ("raster_group", ctypes.c_int32),
                 ("max_ctas", ctypes.c_int32), ("split_mode", ctypes.c_int32),
-                ("cta_pair", ctypes.c_int32), ("direct_store", ctypes.c_int32)]
+                ("cta_pair", ctypes.c_int32), ("direct_store", ctypes.c_int32),
+                ("multicast", ctypes.c_int32), ("l2_prefetch", ctypes.c_int32)]
 
     def as_dict(self):
         return {f: int(getattr(self, f)) for f, _ in self._fields_}
@@ -79,6 +81,8 @@ def library() -> ctypes.CDLL:
                 "gemm_plan_check": ([vp, vp], i32),
                 "gemm_plan_destroy": ([vp], i32),
                 "gemm_plan_get_config": ([vp, cfgp], i32),
+                "gemm_plan_get_launch": ([vp, ctypes.POINTER(i32), ctypes.POINTER(i32),
+                                          ctypes.POINTER(i32)], i32),
                 "gemm_plan_set_timeout": ([vp, ctypes.c_uint64], i32),
                 "gemm_plan_set_wait_test": ([vp, ctypes.c_uint32], i32),
                 "gemm_select_config": ([i64, i64, i64, i32, i32, cfgp], i32),
@@ -139,6 +143,8 @@ def _config(cfg) -> gemm_config_t:
     c.split_mode = int(cfg.get("split_mode", 0))
     c.cta_pair = int(cfg.get("cta_pair", 0))
     c.direct_store = int(cfg.get("direct_store", 0))
+    c.multicast = int(cfg.get("multicast", 0))
+    c.l2_prefetch = int(cfg.get("l2_prefetch", 0))
     return c
 
 
@@ -221,6 +227,14 @@ def gemm_plan_get_config(plan: int) -> dict:
     return c.as_dict()
 
 
+def gemm_plan_get_launch(plan: int) -> dict:
+    """{"grid", "cluster", "max_active_clusters"} of the plan's GEMM kernel launch."""
+    g, c, n = ctypes.c_int32(), ctypes.c_int32(), ctypes.c_int32()
+    _check(library().gemm_plan_get_launch(plan, ctypes.byref(g), ctypes.byref(c), ctypes.byref(n)),
+           "gemm_plan_get_launch")
+    return {"grid": g.value, "cluster": c.value, "max_active_clusters": n.value}
+
+
 def gemm_plan_set_timeout(plan: int, ns: int) -> None:
     _check(library().gemm_plan_set_timeout(plan, int(ns)), "gemm_plan_set_timeout")
 
@@ -264,6 +278,10 @@ class Plan:
     @property
     def config(self) -> dict:
         return gemm_plan_get_config(self.handle)
+
+    @property
+    def launch(self) -> dict:
+        return gemm_plan_get_launch(self.handle)
 
     def run(self, A, B, C, stream=None, bias=None, act=ACT_NONE) -> None:
         if bias is None and act in (ACT_NONE, "none"):

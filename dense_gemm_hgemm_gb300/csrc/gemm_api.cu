@@ -95,10 +95,14 @@ gemm_status_t normalise_config(int64_t M, int64_t N, int64_t K, gemm_dtype_t dty
     if (c.cta_pair != 0 && c.cta_pair != 1) return GEMM_ERR_INVALID_ARG;
     if (c.direct_store != 0 && c.direct_store != 1) return GEMM_ERR_INVALID_ARG;
     if (c.direct_store && c.cta_pair) return GEMM_ERR_INVALID_ARG;
+    if (c.multicast == 1) c.multicast = 0;   // 0 and 1 both mean off
+    if (c.multicast != 0 && c.multicast != 2 && c.multicast != 4) return GEMM_ERR_INVALID_ARG;
+    if (c.l2_prefetch < 0 || c.l2_prefetch > 64) return GEMM_ERR_INVALID_ARG;
     if (c.cta_pair) {
-        // SM pair: 256-row tiles, fp16/bf16 only, no K slicing.
-        if (c.block_n < 128 || c.split_k != 1) return GEMM_ERR_INVALID_ARG;
+        // SM pair: 256-row tiles; K is sliced only across the pairs of a cluster.
+        if (c.block_n < 128) return GEMM_ERR_INVALID_ARG;
         if (dtype == GEMM_I8_I32 && c.block_n != 128) return GEMM_ERR_INVALID_ARG;
+        if (c.split_k != 1 && c.split_mode != 1) return GEMM_ERR_INVALID_ARG;
     }
     const int want_stages =
         c.cta_pair ? gbg::default_pair_stages(c.block_n) : gbg::default_stages(c.block_n);
@@ -118,10 +122,13 @@ gemm_status_t normalise_config(int64_t M, int64_t N, int64_t K, gemm_dtype_t dty
     if (m_blocks * n_blocks * s > INT32_MAX) return GEMM_ERR_INVALID_ARG;
     c.split_k = static_cast<int32_t>(s);
     if (c.split_k == 1) c.split_mode = 0;
+    if (c.multicast > 1 && (c.split_k != 1 || c.cta_pair)) return GEMM_ERR_INVALID_ARG;
     // Cluster split: the slices of a tile share its 128 rows evenly (S | 128) and
     // form a portable cluster (S <= 8).
     if (c.split_mode == 1 && c.split_k != 2 && c.split_k != 4 && c.split_k != 8)
         return GEMM_ERR_INVALID_ARG;
+    // ... and with SM pairs the cluster holds 2 * split_k CTAs
+    if (c.split_mode == 1 && c.cta_pair && c.split_k > 4) return GEMM_ERR_INVALID_ARG;
     if (c.raster_group > m_blocks && m_blocks > 0) c.raster_group = static_cast<int32_t>(m_blocks);
     *out = c;
     *kb_per_split = static_cast<int32_t>(per);
@@ -252,6 +259,8 @@ gemm_status_t create_plan(int64_t M, int64_t N, int64_t K, gemm_dtype_t dtype,
     *out = nullptr;
     gemm_status_t st = validate_shape(M, N, K, dtype, layout);
     if (st != GEMM_OK) return st;
+    // A stored K x M is copied in 64-column blocks: at most two multicast slices
+    if (user_cfg && user_cfg->multicast > 2 && a_mn_major(layout)) return GEMM_ERR_INVALID_ARG;
     if (user_cfg) {
         gemm_config_t tmp;
         int32_t per;
@@ -263,6 +272,7 @@ gemm_status_t create_plan(int64_t M, int64_t N, int64_t K, gemm_dtype_t dtype,
     if (st != GEMM_OK) return st;
 
     gemm_config_t want = user_cfg ? *user_cfg : gbg::select_config(M, N, K, dtype, sms);
+    if (want.multicast > 2 && a_mn_major(layout)) want.multicast = 2;
     gemm_config_t cfg;
     int32_t kb_per_split = 0;
     st = normalise_config(M, N, K, dtype, want, &cfg, &kb_per_split);
@@ -332,7 +342,12 @@ gemm_status_t create_plan(int64_t M, int64_t N, int64_t K, gemm_dtype_t dtype,
     kp.direct_store = cfg.direct_store;
     kp.a_mn_major = a_mn_major(layout) ? 1 : 0;
     kp.b_mn_major = b_mn_major(layout) ? 1 : 0;
-    kp.num_units = kp.m_blocks * kp.n_blocks * kp.split_k;
+    kp.mcast = cfg.multicast > 1 ? cfg.multicast : 1;
+    kp.l2_prefetch = cfg.l2_prefetch;
+    // with A multicast a unit is a group of `mcast` adjacent n-blocks
+    kp.num_units = kp.mcast > 1 ? kp.m_blocks * ((kp.n_blocks + kp.mcast - 1) / kp.mcast)
+                                : kp.m_blocks * kp.n_blocks * kp.split_k;
+    gbg::set_divisors(&kp);
     const uint32_t fmt = dtype == GEMM_BF16 ? 1u : 0u;
     kp.idesc = (1u << 4)                                         // D: fp32
                | (fmt << 7) | (fmt << 10)                        // A, B: fp16 or bf16
@@ -353,7 +368,15 @@ gemm_status_t create_plan(int64_t M, int64_t N, int64_t K, gemm_dtype_t dtype,
         p->shape.grid = kp.num_units;
         p->shape.cluster = cfg.split_k;
     }
-    if (cfg.cta_pair) {       // persistent SM pairs: two CTAs per tile
+    if (kp.mcast > 1) {       // persistent clusters of mcast CTAs per tile group
+        const int groups_cap = cap / kp.mcast > 0 ? cap / kp.mcast : 1;
+        p->shape.grid = kp.mcast * (kp.num_units < groups_cap ? kp.num_units : groups_cap);
+        p->shape.cluster = kp.mcast;
+    }
+    if (cfg.cta_pair && kp.cluster_split) {   // one unit per pair, split_k pairs per cluster
+        p->shape.grid = 2 * kp.num_units;
+        p->shape.cluster = 2 * cfg.split_k;
+    } else if (cfg.cta_pair) {                 // persistent SM pairs: two CTAs per tile
         const int pairs_cap = cap / 2 > 0 ? cap / 2 : 1;
         p->shape.grid = 2 * (kp.num_units < pairs_cap ? kp.num_units : pairs_cap);
         p->shape.cluster = 2;
@@ -361,9 +384,18 @@ gemm_status_t create_plan(int64_t M, int64_t N, int64_t K, gemm_dtype_t dtype,
     if (p->shape.grid < 1) p->shape.grid = 1;
     p->shape.block = gbg::kThreads;
     p->shape.smem_bytes = smem;
+    if (kp.mcast > 1) {   // no more persistent clusters than fit on the GPU at once
+        int fit = 0;
+        if (gbg::gemm_max_clusters(cfg.block_n, cfg.stages, p->out_kind, 0, p->shape, &fit) ==
+                cudaSuccess && fit > 0) {
+            if (p->shape.grid > fit * kp.mcast) p->shape.grid = fit * kp.mcast;
+        } else {
+            cudaGetLastError();
+        }
+    }
 
     if (dtype == GEMM_I8_I32 && M > 0 && N > 0 && K > 0) {
-        st = encode_operand_map(&p->map_a, p->d_a16, M, K, gbg::kBM, a_mn_major(layout),
+        st = encode_operand_map(&p->map_a, p->d_a16, M, K, gbg::kBM / kp.mcast, a_mn_major(layout),
                                 CU_TENSOR_MAP_DATA_TYPE_FLOAT16);
         if (st == GEMM_OK)
             st = encode_operand_map(&p->map_b, p->d_b16, N, K,
@@ -391,6 +423,27 @@ cudaError_t gemm_prepare(int bn, int stages, int out, size_t* smem_bytes) {
         case kOutI32: return gemm_prepare_i32(bn, stages, smem_bytes);
         default: return cudaErrorInvalidValue;
     }
+}
+
+cudaError_t gemm_max_clusters(int bn, int stages, int out, int pair, const LaunchShape& shape,
+                              int* n) {
+    const void* fn = out == kOutF16    ? gemm_kernel_ptr_f16(bn, stages, pair)
+                     : out == kOutBF16 ? gemm_kernel_ptr_bf16(bn, stages, pair)
+                     : out == kOutI32  ? gemm_kernel_ptr_i32(bn, stages, pair)
+                                       : nullptr;
+    if (!fn) return cudaErrorInvalidValue;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(shape.grid));
+    cfg.blockDim = dim3(static_cast<unsigned>(shape.block));
+    cfg.dynamicSmemBytes = shape.smem_bytes;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = static_cast<unsigned>(shape.cluster);
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaOccupancyMaxActiveClusters(n, fn, &cfg);
 }
 
 cudaError_t gemm_launch(int bn, int stages, int out, const LaunchShape& shape,
@@ -469,7 +522,8 @@ gemm_status_t gemm_run_bias_act(gemm_plan_t p, const void* A, const void* B, voi
         if (!p->map_a_valid || p->map_a_src != A) {
             p->map_a_valid = false;
             const gemm_status_t st =
-                encode_operand_map(&p->map_a, A, p->M, p->K, gbg::kBM, a_mn_major(p->layout), dt);
+                encode_operand_map(&p->map_a, A, p->M, p->K, gbg::kBM / p->kp.mcast,
+                                   a_mn_major(p->layout), dt);
             if (st != GEMM_OK) return st;
             p->map_a_src = A;
             p->map_a_valid = true;
@@ -551,6 +605,27 @@ gemm_status_t gemm_plan_get_config(gemm_plan_t p, gemm_config_t* config) {
     return GEMM_OK;
 }
 
+gemm_status_t gemm_plan_get_launch(gemm_plan_t p, int32_t* grid, int32_t* cluster,
+                                   int32_t* max_active_clusters) {
+    if (!p) return GEMM_ERR_INVALID_ARG;
+    if (grid) *grid = p->shape.grid;
+    if (cluster) *cluster = p->shape.cluster;
+    if (max_active_clusters) {
+        int n = 0;
+        int prev = 0;
+        cudaGetDevice(&prev);
+        if (prev != p->device) cudaSetDevice(p->device);
+        if (gbg::gemm_max_clusters(p->cfg.block_n, p->cfg.stages, p->out_kind, p->cfg.cta_pair,
+                                   p->shape, &n) != cudaSuccess) {
+            cudaGetLastError();
+            n = 0;
+        }
+        if (prev != p->device) cudaSetDevice(prev);
+        *max_active_clusters = n;
+    }
+    return GEMM_OK;
+}
+
 gemm_status_t gemm_plan_set_timeout(gemm_plan_t p, uint64_t ns) {
     if (!p) return GEMM_ERR_INVALID_ARG;
     p->kp.timeout_ns = ns ? ns : kDefaultTimeoutNs;
@@ -577,9 +652,13 @@ gemm_status_t gemm_tile_coords(int64_t m_blocks, int64_t n_blocks, int32_t raste
     if (!m_blk || !n_blk || m_blocks < 1 || n_blocks < 1 || raster_group < 1 || tile < 0 ||
         m_blocks * n_blocks > INT32_MAX || tile >= m_blocks * n_blocks)
         return GEMM_ERR_INVALID_ARG;
+    // the kernels' multiply-shift evaluation of the raster (a band taller than
+    // the grid is the whole grid)
+    const int32_t g = raster_group < m_blocks ? raster_group : static_cast<int32_t>(m_blocks);
+    const gbg::RasterDiv rd = gbg::make_raster_div(static_cast<int32_t>(m_blocks),
+                                                   static_cast<int32_t>(n_blocks), g);
     int32_t m = 0, n = 0;
-    gbg::raster_tile(static_cast<int32_t>(m_blocks), static_cast<int32_t>(n_blocks), raster_group,
-                     static_cast<int32_t>(tile), &m, &n);
+    gbg::raster_tile_fast(static_cast<int32_t>(m_blocks), rd, static_cast<int32_t>(tile), &m, &n);
     *m_blk = m;
     *n_blk = n;
     return GEMM_OK;

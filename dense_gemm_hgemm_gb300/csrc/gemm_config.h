@@ -16,7 +16,7 @@ namespace gbg {
 
 struct TableEntry {
     int32_t M, N, K, dtype;
-    int32_t block_n, split_k, raster_group, split_mode, cta_pair, direct_store;
+    int32_t block_n, split_k, raster_group, split_mode, cta_pair, direct_store, multicast;
 };
 
 #include "gemm_config_table.inc"   // static const TableEntry kTunedTable[]; kTunedCount
@@ -38,6 +38,8 @@ inline gemm_config_t model_config(int64_t M, int64_t N, int64_t K, gemm_dtype_t 
     c.split_mode = 0;
     c.cta_pair = 0;
     c.direct_store = 0;
+    c.multicast = 0;
+    c.l2_prefetch = 0;
     const int64_t mb = ceil_div(M, kBM);
     const int64_t num_kb = ceil_div(K, kBK);
     const int cands_f[3] = {256, 128, 64};
@@ -92,6 +94,8 @@ inline gemm_config_t select_config(int64_t M, int64_t N, int64_t K, gemm_dtype_t
             c.split_mode = e.split_mode;
             c.cta_pair = e.cta_pair;
             c.direct_store = e.direct_store;
+            c.multicast = e.multicast;
+            c.l2_prefetch = 0;
             c.max_ctas = 0;
             return c;
         }

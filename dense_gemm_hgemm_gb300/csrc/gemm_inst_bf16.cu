@@ -61,8 +61,8 @@ cudaError_t launch_pair(const LaunchShape& s, const CUtensorMap& a, const CUtens
     cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
-    attr[1].id = cudaLaunchAttributeClusterDimension;   // the SM pair
-    attr[1].val.clusterDim.x = 2;
+    attr[1].id = cudaLaunchAttributeClusterDimension;   // SM pairs (several with split-K)
+    attr[1].val.clusterDim.x = static_cast<unsigned>(s.cluster);
     attr[1].val.clusterDim.y = 1;
     attr[1].val.clusterDim.z = 1;
     cfg.attrs = attr;
@@ -102,6 +102,19 @@ cudaError_t gemm_launch_bf16(int bn, int stages, const LaunchShape& s, const CUt
     X(64, 8) X(128, 6) X(256, 4)
 #undef X
     return cudaErrorInvalidValue;
+}
+
+const void* gemm_kernel_ptr_bf16(int bn, int stages, int pair) {
+#define X(B, S) \
+    if (!pair && bn == B && stages == S) return reinterpret_cast<const void*>(gemm_tn_kernel<B, S, kOutBF16>);
+    X(64, 8) X(128, 6) X(256, 4)
+#undef X
+#define X(B, S) \
+    if (pair && bn == B && stages == S) \
+        return reinterpret_cast<const void*>(gemm_tn_pair_kernel<B, S, kOutBF16>);
+    X(256, 6) X(128, 8)
+#undef X
+    return nullptr;
 }
 
 }  // namespace gbg

@@ -120,16 +120,21 @@ __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
 }
 
+// Suspend-time hint of the barrier polls, in ns: measured 10-15% faster
+// k-block turnaround on mid-size shapes than the default time limit (the
+// hint bounds how long a polling thread may sleep before it looks again).
+constexpr uint32_t kWaitHintNs = 32;
+
 __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
     uint32_t done;
     asm volatile(
         "{\n\t"
         ".reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
         "selp.u32 %0, 1, 0, p;\n\t"
         "}"
         : "=r"(done)
-        : "r"(bar), "r"(parity)
+        : "r"(bar), "r"(parity), "n"(kWaitHintNs)
         : "memory");
     return done != 0;
 }
@@ -243,6 +248,26 @@ __device__ __forceinline__ void umma_f16(uint32_t d_tmem, uint64_t a_desc, uint6
         : "memory");
 }
 
+// TMA load delivered to the same shared-memory offset (and barrier offset) in
+// every CTA of `cta_mask` within the cluster.
+__device__ __forceinline__ void tma_load_2d_mcast(uint32_t dst, const CUtensorMap* map, uint32_t bar,
+                                                  int32_t x, int32_t y, uint16_t cta_mask) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.multicast::cluster"
+        " [%0], [%1, {%3, %4}], [%2], %5;" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(x), "r"(y), "h"(cta_mask)
+        : "memory");
+}
+
+// As umma_commit, arriving on the barrier at this offset in every CTA of `cta_mask`.
+__device__ __forceinline__ void umma_commit_mcast(uint32_t bar, uint16_t cta_mask) {
+    asm volatile(
+        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
+        " [%0], %1;" ::"r"(bar),
+        "h"(cta_mask)
+        : "memory");
+}
+
 // Arrive (once) on `bar` when every tcgen05.mma issued so far by this thread is done.
 __device__ __forceinline__ void umma_commit(uint32_t bar) {
     asm volatile(
@@ -344,29 +369,52 @@ __device__ __forceinline__ uint32_t pack2(float lo, float hi) {
 
 // Fused epilogue of a linear layer, in fp32 before the output conversion:
 // x = act(x + bias[col]).
-__device__ __forceinline__ float activation(float x, int32_t act) {
-    switch (act) {
-        case 1: return fmaxf(x, 0.0f);
-        case 2: return 0.5f * x * (1.0f + erff(x * 0.70710678118654752f));   // x * Phi(x)
-        case 3: return x / (1.0f + expf(-x));
-        default: return x;
+// The epilogue's activation, chosen at compile time: the kernel dispatches on
+// the plan's activation once per group of columns, not per element.
+template <int ACT>
+__device__ __forceinline__ float act_fn(float x) {
+    if constexpr (ACT == 1) {
+        return fmaxf(x, 0.0f);
+    } else if constexpr (ACT == 2) {
+        return 0.5f * x * (1.0f + erff(x * 0.70710678118654752f));   // x * Phi(x)
+    } else if constexpr (ACT == 3) {
+        // x * sigmoid(x); the fast exponential and divide are far inside the
+        // epilogue tolerance and keep the four epilogue warps ahead of the MMA
+        return __fdividef(x, 1.0f + __expf(-x));
+    } else {
+        return x;
     }
 }
 
 // v holds fp32 bits for columns [col, col + 4*G); N % 8 == 0, so a group of 4
-// columns is entirely inside or outside C.
+// columns is entirely inside or outside C.  The bias loads are issued together
+// before any use.
+template <int ACT, int G>
+__device__ __forceinline__ void bias_act(uint32_t* v, const float* bias, int32_t N, int32_t col) {
+    float4 b[G];
+#pragma unroll
+    for (int g = 0; g < G; ++g) {
+        b[g] = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (bias != nullptr && col + g * 4 < N)
+            b[g] = __ldg(reinterpret_cast<const float4*>(bias + col + g * 4));
+    }
+#pragma unroll
+    for (int g = 0; g < G; ++g) {
+        v[g * 4 + 0] = __float_as_uint(act_fn<ACT>(__uint_as_float(v[g * 4 + 0]) + b[g].x));
+        v[g * 4 + 1] = __float_as_uint(act_fn<ACT>(__uint_as_float(v[g * 4 + 1]) + b[g].y));
+        v[g * 4 + 2] = __float_as_uint(act_fn<ACT>(__uint_as_float(v[g * 4 + 2]) + b[g].z));
+        v[g * 4 + 3] = __float_as_uint(act_fn<ACT>(__uint_as_float(v[g * 4 + 3]) + b[g].w));
+    }
+}
+
 template <int G>
 __device__ __forceinline__ void apply_bias_act(uint32_t* v, const KParams& p, int32_t col) {
     if (p.bias == nullptr && p.act == 0) return;
-#pragma unroll
-    for (int g = 0; g < G; ++g) {
-        float4 b = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (p.bias != nullptr && col + g * 4 < p.N)
-            b = __ldg(reinterpret_cast<const float4*>(p.bias + col + g * 4));
-        v[g * 4 + 0] = __float_as_uint(activation(__uint_as_float(v[g * 4 + 0]) + b.x, p.act));
-        v[g * 4 + 1] = __float_as_uint(activation(__uint_as_float(v[g * 4 + 1]) + b.y, p.act));
-        v[g * 4 + 2] = __float_as_uint(activation(__uint_as_float(v[g * 4 + 2]) + b.z, p.act));
-        v[g * 4 + 3] = __float_as_uint(activation(__uint_as_float(v[g * 4 + 3]) + b.w, p.act));
+    switch (p.act) {
+        case 1: bias_act<1, G>(v, p.bias, p.N, col); break;
+        case 2: bias_act<2, G>(v, p.bias, p.N, col); break;
+        case 3: bias_act<3, G>(v, p.bias, p.N, col); break;
+        default: bias_act<0, G>(v, p.bias, p.N, col); break;
     }
 }
 
@@ -498,28 +546,73 @@ __device__ __forceinline__ void stage_row32(uint32_t staging, int row, int col, 
         st_shared_u4(base + g * 16, make_uint4(v[g * 4 + 0], v[g * 4 + 1], v[g * 4 + 2], v[g * 4 + 3]));
 }
 
-// CTA `rank` of the cluster owns rows [rank*128/S, (rank+1)*128/S) of the tile:
-// for each 4-column group it sums the S staged partials in slice order 0..S-1
-// (read from every CTA's shared memory) and stores the converted result.
-template <int BN, int OUT>
-__device__ __forceinline__ void cluster_reduce_store(const KParams& p, const UnitCoord& c,
-                                                     uint32_t staging, int tid, int nthreads) {
-    const int S = p.split_k;
-    const uint32_t rank = cluster_ctarank();
+// In-cluster split-K reduction (push, then local sums).  The S K-slices of a
+// 128-row block of C sit in S cluster CTAs; CTA "part" o (rank o * rank_stride +
+// rank_offset) owns rows [o*128/S, (o+1)*128/S) of the block.  After a cluster
+// barrier (every ring idle) each CTA stores each of its fp32 partial rows into
+// the owner's receive area, slot = its own slice index; after a second barrier
+// every owner sums its S slots in slice order 0..S-1 (fixed order: the same
+// result every run) from its own shared memory and writes C.
+// Receive area: S slots x 128/S rows x BN words, row stride BN+4 words.
+template <int BN>
+struct SplitRecv {
+    static constexpr int kRowWords = BN + 4;
+    static constexpr int kBytes = kBM * kRowWords * 4;
+};
+
+__device__ __forceinline__ void st_dsmem_u4(uint32_t cluster_addr, uint4 v) {
+    asm volatile("st.shared::cluster.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(cluster_addr), "r"(v.x),
+                 "r"(v.y), "r"(v.z), "r"(v.w)
+                 : "memory");
+}
+__device__ __forceinline__ uint4 ld_shared_u4(uint32_t saddr) {
+    uint4 v;
+    asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "r"(saddr)
+                 : "memory");
+    return v;
+}
+
+// Store 32 partial values of block row `row`, columns [col, col+32), of K-slice
+// `slice` into the receive area of the row's owner.
+template <int BN>
+__device__ __forceinline__ void push_row32(uint32_t recv, int S, int slice, int row, int col,
+                                           const uint32_t* v, uint32_t rank_stride,
+                                           uint32_t rank_offset) {
     const int rows = kBM / S;
-    const int r0 = static_cast<int>(rank) * rows;
+    const int owner = row / rows;
+    const int lr = row - owner * rows;
+    const uint32_t local =
+        recv + static_cast<uint32_t>(((slice * rows + lr) * SplitRecv<BN>::kRowWords + col) * 4);
+    const uint32_t dst = map_to_rank(local, static_cast<uint32_t>(owner) * rank_stride + rank_offset);
+#pragma unroll
+    for (int g = 0; g < 8; ++g)
+        st_dsmem_u4(dst + g * 16, make_uint4(v[g * 4 + 0], v[g * 4 + 1], v[g * 4 + 2], v[g * 4 + 3]));
+}
+
+// The owner's half: sum its S slots in slice order, apply the epilogue, store
+// rows [part*128/S, (part+1)*128/S) of the block whose first global row is
+// block_row (threads take consecutive 4-column groups: coalesced stores).
+template <int BN, int OUT>
+__device__ __forceinline__ void cluster_sum_store(const KParams& p, int32_t block_row,
+                                                  int32_t col_base, int part, uint32_t recv,
+                                                  int tid, int nthreads) {
+    const int S = p.split_k;
+    const int rows = kBM / S;
     constexpr int kVec = BN / 4;
     for (int t = tid; t < rows * kVec; t += nthreads) {
-        const int rr = r0 + t / kVec;
+        const int lr = t / kVec;
         const int c4 = (t % kVec) * 4;
-        const int32_t grow = c.m_blk * kBM + rr;
-        const int32_t gcol = c.n_blk * BN + c4;
+        const int32_t grow = block_row + part * rows + lr;
+        const int32_t gcol = col_base + c4;
         if (grow >= p.M || gcol >= p.N) continue;
-        const uint32_t off = staging + static_cast<uint32_t>((rr * (BN + 4) + c4) * 4);
+        const uint32_t off = recv + static_cast<uint32_t>((lr * SplitRecv<BN>::kRowWords + c4) * 4);
+        const uint32_t slot = static_cast<uint32_t>(rows * SplitRecv<BN>::kRowWords * 4);
         uint4 q[8];
 #pragma unroll
         for (int s = 0; s < 8; ++s)
-            if (s < S) q[s] = ld_dsmem_u4(map_to_rank(off, static_cast<uint32_t>(s)));
+            if (s < S) q[s] = ld_shared_u4(off + static_cast<uint32_t>(s) * slot);
         uint32_t v[4] = {0u, 0u, 0u, 0u};
 #pragma unroll
         for (int s = 0; s < 8; ++s)
@@ -560,6 +653,26 @@ __device__ __forceinline__ void stage_store_row(uint32_t buf, int row, int c0, c
     }
 }
 
+// Persistent iteration space of this CTA: units blockIdx.x, +gridDim.x, ... or,
+// with A multicast, tile groups cluster_id, +num_clusters, ... shared by the
+// CTAs of a cluster.
+struct UnitIter {
+    int32_t first, stride;
+};
+__device__ __forceinline__ UnitIter unit_iter(const KParams& p) {
+    return UnitIter{static_cast<int32_t>(blockIdx.x >> p.mcast_shift),
+                    static_cast<int32_t>(gridDim.x >> p.mcast_shift)};
+}
+// Coordinates of unit u for this CTA.  With multicast, unit u is a group of
+// mcast adjacent n-blocks of one m-block, this CTA taking the one of its
+// cluster rank; a tile past N loads zeros and stores nothing.
+__device__ __forceinline__ UnitCoord unit_at(const KParams& p, int32_t u) {
+    UnitCoord c = unit_coord_fast(u, p);   // with multicast: tile group u (split_k is 1)
+    if (p.mcast > 1)
+        c.n_blk = c.n_blk * p.mcast + static_cast<int32_t>(blockIdx.x & (p.mcast - 1));
+    return c;
+}
+
 // ----------------------------------------------------------------------------
 // the kernel
 // ----------------------------------------------------------------------------
@@ -569,6 +682,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                    const __grid_constant__ CUtensorMap tmap_b,
                    const __grid_constant__ CUtensorMap tmap_c, const KParams p) {
     using L = SmemLayout<BN, STAGES>;
+    static_assert((OUT == kOutI32 ? 2 : 1) * SplitRecv<BN>::kBytes <= L::kRingBytes,
+                  "split-K receive area (and parked integer sums) must fit in the ring");
     static_assert(BN == 64 || BN == 128 || BN == 256, "tile width");
     static_assert(OUT != kOutI32 || BN <= 128, "integer mode keeps BN int32 sums in registers");
     constexpr uint32_t kTmemCols = 2 * BN;   // two accumulator buffers; 128/256/512 columns
@@ -592,7 +707,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         prefetch_tmap(&tmap_c);
         for (int s = 0; s < STAGES; ++s) {
             mbar_init(smem_addr(&ctl->full[s]), 1);
-            mbar_init(smem_addr(&ctl->empty[s]), 1);
+            // with A multicast a slot is free only once every CTA of the cluster
+            // has consumed it (each one's MMA commit arrives here)
+            mbar_init(smem_addr(&ctl->empty[s]), p.mcast > 1 ? p.mcast : 1);
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(smem_addr(&ctl->tmem_full[b]), 1);
@@ -608,28 +725,39 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_relinquish();
     }
     tc_fence_before();
-    __syncthreads();
+    if (p.mcast > 1)
+        cluster_sync_all();   // peers' copies and commits target this CTA's barriers
+    else
+        __syncthreads();
     tc_fence_after();
     const uint32_t tmem_base = ctl->tmem_base;
     // Programmatic dependent launch: the set-up above may overlap the previous
     // kernel of the stream; no global memory is touched before that kernel has
     // completed and its writes are visible.  The next kernel may be scheduled
     // from here on (it waits the same way before reading anything we write).
-    if (warp == 0 && lane == 0 && static_cast<int32_t>(blockIdx.x) < p.num_units) {
+    const UnitIter it = unit_iter(p);
+    // This CTA's first unit, worked out while the previous kernel may still run.
+    const UnitCoord c_first = unit_at(p, it.first);
+    if (warp == 0 && lane == 0 && it.first < p.num_units) {
         // Warm L2 with this CTA's first k-blocks while the previous kernel drains.
         // Only L2 is touched (the coherence point); the data is read after the
         // wait below, so this cannot observe stale values.
-        const UnitCoord c = unit_coord(blockIdx.x, p.split_k, p.kb_per_split, p.num_kb,
-                                       p.m_blocks, p.n_blocks, p.raster_group);
-        const int32_t kb_end = c.kb_begin + STAGES < c.kb_end ? c.kb_begin + STAGES : c.kb_end;
+        const UnitCoord c = c_first;
+        const int32_t ahead = STAGES > p.l2_prefetch ? STAGES : p.l2_prefetch;
+        const int32_t kb_end = c.kb_begin + ahead < c.kb_end ? c.kb_begin + ahead : c.kb_end;
+        // with multicast, this CTA's slice of the A tile (its A box is that slice)
+        const int32_t a_rows = kBM >> p.mcast_shift;
+        const int32_t a_row0 =
+            c.m_blk * kBM + static_cast<int32_t>(blockIdx.x & ((1u << p.mcast_shift) - 1u)) * a_rows;
         for (int32_t kb = c.kb_begin; kb < kb_end; ++kb) {
-            prefetch_operand(&tmap_a, kb, c.m_blk * kBM, kBM, p.a_mn_major);
+            prefetch_operand(&tmap_a, kb, a_row0, a_rows, p.a_mn_major);
             prefetch_operand(&tmap_b, kb, c.n_blk * BN, BN, p.b_mn_major);
         }
     }
     grid_dependency_wait();
     grid_launch_dependents();
     const Watch watch{&ctl->abort, p.error_word, p.timeout_ns};
+    bool epi_ok = false;   // epilogue: this CTA's accumulator is complete (split-K in the cluster)
 
     if (warp == 0) {
         // ------------------------------------------------------------ producer
@@ -638,9 +766,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint32_t phase = 0;
             int issued = 0;
             bool ok = true;
-            for (int32_t u = blockIdx.x; ok && u < p.num_units; u += gridDim.x) {
-                const UnitCoord c = unit_coord(u, p.split_k, p.kb_per_split, p.num_kb, p.m_blocks,
-                                               p.n_blocks, p.raster_group);
+            for (int32_t u = it.first; ok && u < p.num_units; u += it.stride) {
+                const UnitCoord c = u == it.first ? c_first : unit_at(p, u);
                 for (int32_t kb = c.kb_begin; kb < c.kb_end; ++kb) {
                     const uint32_t full = smem_addr(&ctl->full[stage]);
                     if (!wait_phase(smem_addr(&ctl->empty[stage]), phase ^ 1u, watch,
@@ -649,10 +776,36 @@ __global__ void __launch_bounds__(kThreads, 1)
                         break;
                     }
                     mbar_arrive_expect_tx(full, kStageTx + p.tx_extra);
-                    load_operand(ring + stage * kATileBytes, &tmap_a, full, kb, c.m_blk * kBM, kBM,
-                                 p.a_mn_major);
+                    if (p.mcast > 1) {
+                        // this CTA's 1/mcast of the A tile, delivered to every CTA of
+                        // the cluster (the slot's bytes arrive from all of them)
+                        const int32_t rank = static_cast<int32_t>(blockIdx.x & (p.mcast - 1));
+                        const uint16_t all = static_cast<uint16_t>((1u << p.mcast) - 1u);
+                        const uint32_t a_slot = ring + stage * kATileBytes;
+                        if (p.a_mn_major) {   // mcast == 2: one 64-row M block each
+                            tma_load_2d_mcast(a_slot + static_cast<uint32_t>(rank) * 8192u, &tmap_a,
+                                              full, c.m_blk * kBM + rank * 64, kb * kBK, all);
+                        } else {
+                            const int32_t rows = kBM >> p.mcast_shift;
+                            tma_load_2d_mcast(a_slot + static_cast<uint32_t>(rank * rows * 128),
+                                              &tmap_a, full, kb * kBK, c.m_blk * kBM + rank * rows,
+                                              all);
+                        }
+                    } else {
+                        load_operand(ring + stage * kATileBytes, &tmap_a, full, kb, c.m_blk * kBM,
+                                     kBM, p.a_mn_major);
+                    }
                     load_operand(ring_b + stage * L::kBTileBytes, &tmap_b, full, kb, c.n_blk * BN,
                                  BN, p.b_mn_major);
+                    if (p.l2_prefetch > 0 && kb + p.l2_prefetch < c.kb_end) {
+                        // warm L2 with a later k-block of this tile (this CTA's A share)
+                        const int32_t a_rows = kBM >> p.mcast_shift;
+                        const int32_t a_rank =
+                            static_cast<int32_t>(blockIdx.x & ((1u << p.mcast_shift) - 1u));
+                        prefetch_operand(&tmap_a, kb + p.l2_prefetch, c.m_blk * kBM + a_rank * a_rows,
+                                         a_rows, p.a_mn_major);
+                        prefetch_operand(&tmap_b, kb + p.l2_prefetch, c.n_blk * BN, BN, p.b_mn_major);
+                    }
                     ++issued;
                     if (++stage == STAGES) {
                         stage = 0;
@@ -673,6 +826,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                         ph ^= 1u;
                     }
                     wait_phase_unwind(smem_addr(&ctl->full[s]), ph, 100000000ull);
+                    // With multicast, also wait until every CTA of the cluster has
+                    // released the slot, so no peer's commit arrives after exit.
+                    if (p.mcast > 1) wait_phase_unwind(smem_addr(&ctl->empty[s]), ph, 100000000ull);
                 }
             }
             (void)ok;
@@ -685,9 +841,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint32_t phase = 0;
             uint32_t acc_iter = 0;
             bool ok = true;
-            for (int32_t u = blockIdx.x; ok && u < p.num_units; u += gridDim.x) {
-                const UnitCoord c = unit_coord(u, p.split_k, p.kb_per_split, p.num_kb, p.m_blocks,
-                                               p.n_blocks, p.raster_group);
+            for (int32_t u = it.first; ok && u < p.num_units; u += it.stride) {
+                const UnitCoord c = u == it.first ? c_first : unit_at(p, u);
                 for (int32_t k0 = c.kb_begin; ok && k0 < c.kb_end; k0 += p.chunk_kb) {
                     const int32_t k1 = (k0 + p.chunk_kb < c.kb_end) ? k0 + p.chunk_kb : c.kb_end;
                     const uint32_t buf = acc_iter & 1u;
@@ -715,7 +870,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                             umma_f16(d_tmem, a_desc + a_step * k, b_desc + b_step * k, p.idesc,
                                      (kb > k0 || k > 0) ? 1u : 0u);
                         }
-                        umma_commit(smem_addr(&ctl->empty[stage]));
+                        if (p.mcast > 1)   // every CTA's copy of A in this slot is consumed
+                            umma_commit_mcast(smem_addr(&ctl->empty[stage]),
+                                              static_cast<uint16_t>((1u << p.mcast) - 1u));
+                        else
+                            umma_commit(smem_addr(&ctl->empty[stage]));
                         if (++stage == STAGES) {
                             stage = 0;
                             phase ^= 1u;
@@ -742,14 +901,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t store_sel = 0;
         uint32_t acc_iter = 0;
         bool ok = true;
-        for (int32_t u = blockIdx.x; ok && u < p.num_units; u += gridDim.x) {
-            const UnitCoord c = unit_coord(u, p.split_k, p.kb_per_split, p.num_kb, p.m_blocks,
-                                           p.n_blocks, p.raster_group);
+        for (int32_t u = it.first; ok && u < p.num_units; u += it.stride) {
+            const UnitCoord c = u == it.first ? c_first : unit_at(p, u);
             const int32_t row = c.m_blk * kBM + row_in_tile;
             const int32_t col0 = c.n_blk * BN;
             const bool split = p.split_k > 1 && !p.cluster_split;
             const bool cluster = p.cluster_split != 0;
-            if (cluster) fence_proxy_async_smem();   // the ring becomes the staging buffer
             uint32_t* ws_row = nullptr;
             if (split)
                 ws_row = reinterpret_cast<uint32_t*>(p.workspace) +
@@ -784,10 +941,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                     ++acc_iter;
                 }
                 if (!ok) break;
+                // cluster split: park the sums behind the receive area of the ring
+                // (idle now) until they are pushed after the cluster barrier
+                if (cluster) fence_proxy_async_smem();
 #pragma unroll
                 for (int j = 0; j < BN / 32; ++j) {
                     if (cluster) {
-                        stage_row32<BN>(ring, row_in_tile, j * 32, &sum[j * 32]);
+                        stage_row32<BN>(ring + SplitRecv<BN>::kBytes, row_in_tile, j * 32,
+                                        &sum[j * 32]);
                     } else if (split) {
                         if (row < p.M) store_ws32(ws_row + j * 32, &sum[j * 32]);
                     } else if (p.direct_store) {
@@ -822,15 +983,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                     break;
                 }
                 tc_fence_after();
-                if (cluster || split || p.direct_store) {
+                if (cluster) {
+                    // the accumulator stays in TMEM until it is pushed after the
+                    // cluster barrier
+                } else if (split || p.direct_store) {
 #pragma unroll 1
                     for (int j = 0; j < BN / 32; ++j) {
                         uint32_t v[32];
                         tmem_ld_32x32b_x32(tmem_base + lane_addr + buf * BN + j * 32, v);
                         tmem_ld_wait();
-                        if (cluster) {
-                            stage_row32<BN>(ring, row_in_tile, j * 32, v);
-                        } else if (row < p.M) {
+                        if (row < p.M) {
                             if (split) {
                                 store_ws32(ws_row + j * 32, v);
                             } else {
@@ -915,6 +1077,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             }
         }
+        epi_ok = ok && it.first < p.num_units;
     }
 
     if (warp >= 2) {
@@ -926,19 +1089,47 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     // ------------------------------------------- split-K reduction in the cluster
     if (p.cluster_split) {
-        cluster_sync_all();   // every CTA of the cluster has staged its slice
-        if (warp >= 2) {
-            const UnitCoord c = unit_coord(blockIdx.x, p.split_k, p.kb_per_split, p.num_kb,
-                                           p.m_blocks, p.n_blocks, p.raster_group);
-            cluster_reduce_store<BN, OUT>(p, c, ring, static_cast<int>(threadIdx.x) - 64,
-                                          kEpiWarps * 32);
+        fence_proxy_async_smem();   // the TMA-written ring now receives peers' stores
+        cluster_sync_all();         // every CTA's main loop is over: all rings are idle
+        tc_fence_after();
+        const UnitCoord c = unit_coord_fast(blockIdx.x, p);
+        if (warp >= 2 && epi_ok) {
+            const int quad = warp & 3;
+            const int row = quad * 32 + lane;
+#pragma unroll 1
+            for (int j = 0; j < BN / 32; ++j) {
+                uint32_t v[32];
+                if constexpr (OUT == kOutI32) {
+                    const uint32_t src = ring + SplitRecv<BN>::kBytes +
+                                         static_cast<uint32_t>((row * (BN + 4) + j * 32) * 4);
+#pragma unroll
+                    for (int g = 0; g < 8; ++g) {
+                        const uint4 q = ld_shared_u4(src + g * 16);
+                        v[g * 4 + 0] = q.x;
+                        v[g * 4 + 1] = q.y;
+                        v[g * 4 + 2] = q.z;
+                        v[g * 4 + 3] = q.w;
+                    }
+                } else {
+                    tmem_ld_32x32b_x32(tmem_base + (static_cast<uint32_t>(quad * 32) << 16) + j * 32, v);
+                    tmem_ld_wait();
+                }
+                push_row32<BN>(ring, p.split_k, c.split, row, j * 32, v, 1u, 0u);
+            }
         }
-        cluster_sync_all();   // no CTA leaves while its shared memory may still be read
+        cluster_sync_all();         // every slice has arrived at its owner
+        if (warp >= 2)
+            cluster_sum_store<BN, OUT>(p, c.m_blk * kBM, c.n_blk * BN,
+                                       static_cast<int>(cluster_ctarank()), ring,
+                                       static_cast<int>(threadIdx.x) - 64, kEpiWarps * 32);
     }
 
     // ---------------------------------------------------------------- teardown
     tc_fence_before();
-    __syncthreads();
+    if (p.mcast > 1)
+        cluster_sync_all();   // no peer still sends copies or commits to this CTA
+    else
+        __syncthreads();
     if (warp == 1) {
         tc_fence_after();
         tmem_dealloc(tmem_base, kTmemCols);

@@ -18,6 +18,12 @@
 // Same conventions as gemm_kernel.cuh: persistent over tiles (one cluster per SM
 // pair), double-buffered TMEM accumulator, bounded waits with an error word,
 // programmatic dependent launch, L2 prefetch before the dependency wait.
+//
+// Split-K in the cluster (cluster_split, S = 2 or 4): a cluster of 2S CTAs holds
+// S pairs (ranks 2s, 2s+1 form pair s) that compute K-slices s of one 256 x BN
+// tile; each CTA stages its fp32 partial rows in its (then idle) ring, and CTA
+// (s, half h) sums rows [s*128/S, (s+1)*128/S) of half h over the S pairs in
+// slice order through distributed shared memory.
 #pragma once
 
 #include "gemm_kernel.cuh"
@@ -110,11 +116,11 @@ __device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t par
     asm volatile(
         "{\n\t"
         ".reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2, %3;\n\t"
         "selp.u32 %0, 1, 0, p;\n\t"
         "}"
         : "=r"(done)
-        : "r"(bar), "r"(parity)
+        : "r"(bar), "r"(parity), "n"(kWaitHintNs)
         : "memory");
     return done != 0;
 }
@@ -149,6 +155,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                         const __grid_constant__ CUtensorMap tmap_b,
                         const __grid_constant__ CUtensorMap tmap_c, const KParams p) {
     using L = SmemLayout2<BN, STAGES>;
+    static_assert((OUT == kOutI32 ? 2 : 1) * SplitRecv<BN>::kBytes <= L::kRingBytes,
+                  "split-K receive area (and parked integer sums) must fit in the ring");
     static_assert(BN == 128 || BN == 256, "pair tile width");
     static_assert(OUT != kOutI32 || BN == 128, "integer mode keeps BN int32 sums in registers");
     constexpr uint32_t kTmemCols = 2 * BN;
@@ -165,7 +173,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     const int warp = __shfl_sync(0xffffffffu, static_cast<int>(threadIdx.x) / 32, 0);
     const int lane = static_cast<int>(threadIdx.x) & 31;
-    const uint32_t rank = cluster_ctarank();          // 0: leader, 1: peer
+    const uint32_t crank = cluster_ctarank();
+    const uint32_t rank = crank & 1u;                  // 0: leader, 1: peer (within the pair)
+    const uint32_t lead = crank & ~1u;                 // cluster rank of this pair's leader
+    const uint16_t pair_mask = static_cast<uint16_t>(3u << lead);
     const bool leader = rank == 0;
     const int32_t pair = static_cast<int32_t>(blockIdx.x >> 1);
     const int32_t npairs = static_cast<int32_t>(gridDim.x >> 1);
@@ -198,18 +209,21 @@ __global__ void __launch_bounds__(kThreads, 1)
     const Watch watch{&ctl->abort, p.error_word, p.timeout_ns};
     if (!leader && threadIdx.x == 0) {
         // The leader's MMAs address the peer's TMEM with the leader's address.
-        const uint32_t lead_base = ld_dsmem_u32(map_to_rank(smem_addr(&ctl->tmem_base), 0));
+        const uint32_t lead_base = ld_dsmem_u32(map_to_rank(smem_addr(&ctl->tmem_base), lead));
         if (lead_base != tmem_base) {
             atomicCAS(p.error_word, 0, kSitePairTmem);
             ctl->abort = 1;
         }
     }
 
+    bool epi_ok = false;   // epilogue: this CTA's accumulator is complete (split-K in the cluster)
+    // This pair's first unit, worked out while the previous kernel may still run.
+    const UnitCoord c_first = unit_coord_fast(pair, p);
     if (warp == 0 && lane == 0 && pair < p.num_units) {
-        const UnitCoord c = unit_coord(pair, 1, p.kb_per_split, p.num_kb, p.m_blocks, p.n_blocks,
-                                       p.raster_group);
-        const int32_t kb_end = STAGES < c.kb_end ? STAGES : c.kb_end;
-        for (int32_t kb = 0; kb < kb_end; ++kb) {
+        const UnitCoord c = c_first;
+        const int32_t ahead = STAGES > p.l2_prefetch ? STAGES : p.l2_prefetch;
+        const int32_t kb_end = c.kb_begin + ahead < c.kb_end ? c.kb_begin + ahead : c.kb_end;
+        for (int32_t kb = c.kb_begin; kb < kb_end; ++kb) {
             prefetch_operand(&tmap_a, kb, c.m_blk * 2 * kBM + static_cast<int32_t>(rank) * kBM, kBM,
                              p.a_mn_major);
             prefetch_operand(&tmap_b, kb, c.n_blk * BN + static_cast<int32_t>(rank) * (BN / 2),
@@ -227,8 +241,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             int issued = 0;
             bool ok = true;
             for (int32_t u = pair; ok && u < p.num_units; u += npairs) {
-                const UnitCoord c = unit_coord(u, 1, p.kb_per_split, p.num_kb, p.m_blocks,
-                                               p.n_blocks, p.raster_group);
+                const UnitCoord c = u == pair ? c_first : unit_coord_fast(u, p);
                 const int32_t a_row = c.m_blk * 2 * kBM + static_cast<int32_t>(rank) * kBM;
                 const int32_t b_row = c.n_blk * BN + static_cast<int32_t>(rank) * (BN / 2);
                 for (int32_t kb = c.kb_begin; kb < c.kb_end; ++kb) {
@@ -239,11 +252,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                     const uint32_t full_local = smem_addr(&ctl->full[stage]);
                     if (leader) mbar_arrive_expect_tx(full_local, kPairTx + p.tx_extra);
-                    const uint32_t full_lead = map_to_rank(full_local, 0);
+                    const uint32_t full_lead = map_to_rank(full_local, lead);
                     load_operand_pair(ring + stage * kATileBytes, &tmap_a, full_lead, kb, a_row, kBM,
                                       p.a_mn_major);
                     load_operand_pair(ring_b + stage * L::kBTileBytes, &tmap_b, full_lead, kb, b_row,
                                       BN / 2, p.b_mn_major);
+                    if (p.l2_prefetch > 0 && kb + p.l2_prefetch < c.kb_end) {
+                        prefetch_operand(&tmap_a, kb + p.l2_prefetch, a_row, kBM, p.a_mn_major);
+                        prefetch_operand(&tmap_b, kb + p.l2_prefetch, b_row, BN / 2, p.b_mn_major);
+                    }
                     ++issued;
                     if (++stage == STAGES) {
                         stage = 0;
@@ -276,8 +293,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint32_t acc_iter = 0;
             bool ok = true;
             for (int32_t u = pair; ok && u < p.num_units; u += npairs) {
-                const UnitCoord c = unit_coord(u, 1, p.kb_per_split, p.num_kb, p.m_blocks,
-                                               p.n_blocks, p.raster_group);
+                const UnitCoord c = u == pair ? c_first : unit_coord_fast(u, p);
                 // One accumulation per chunk of k-blocks (the whole K range except in
                 // integer mode, where a chunk keeps every fp32 partial sum exact).
                 for (int32_t k0 = c.kb_begin; ok && k0 < c.kb_end; k0 += p.chunk_kb) {
@@ -306,18 +322,18 @@ __global__ void __launch_bounds__(kThreads, 1)
                         for (int k = 0; k < kBK / 16; ++k)
                             umma_f16_pair(d_tmem, a_desc + a_step * k, b_desc + b_step * k, p.idesc,
                                           (kb > k0 || k > 0) ? 1u : 0u);
-                        umma_commit_pair(smem_addr(&ctl->empty[stage]), 0x3);
+                        umma_commit_pair(smem_addr(&ctl->empty[stage]), pair_mask);
                         if (++stage == STAGES) {
                             stage = 0;
                             phase ^= 1u;
                         }
                     }
                     if (!ok) break;
-                    umma_commit_pair(smem_addr(&ctl->tmem_full[buf]), 0x3);
+                    umma_commit_pair(smem_addr(&ctl->tmem_full[buf]), pair_mask);
                     ++acc_iter;
                 }
             }
-            umma_commit_pair(smem_addr(&ctl->drain), 0x1);
+            umma_commit_pair(smem_addr(&ctl->drain), static_cast<uint16_t>(1u << lead));
             wait_phase_unwind(smem_addr(&ctl->drain), 0, 100000000ull);
         }
         __syncwarp();
@@ -330,10 +346,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t acc_iter = 0;
         bool ok = true;
         for (int32_t u = pair; ok && u < p.num_units; u += npairs) {
-            const UnitCoord c = unit_coord(u, 1, p.kb_per_split, p.num_kb, p.m_blocks, p.n_blocks,
-                                           p.raster_group);
+            const UnitCoord c = u == pair ? c_first : unit_coord_fast(u, p);
             const int32_t y = c.m_blk * 2 * kBM + static_cast<int32_t>(rank) * kBM + quad * 32;
             const int32_t col0 = c.n_blk * BN;
+            const int row_in_tile = quad * 32 + lane;
             if constexpr (OUT == kOutI32) {
                 // Integer mode: round each exact fp32 chunk to int32 and add (mod 2^32).
                 uint32_t sum[BN];
@@ -360,10 +376,21 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                     tc_fence_before();
                     __syncwarp();
-                    if (lane == 0) mbar_arrive_remote(map_to_rank(smem_addr(&ctl->tmem_empty[buf]), 0));
+                    if (lane == 0)
+                        mbar_arrive_remote(map_to_rank(smem_addr(&ctl->tmem_empty[buf]), lead));
                     ++acc_iter;
                 }
                 if (!ok) break;
+                if (p.cluster_split) {
+                    // park the sums behind the receive area of the (idle) ring until
+                    // they are pushed after the cluster barrier
+                    fence_proxy_async_smem();
+#pragma unroll
+                    for (int j = 0; j < BN / 32; ++j)
+                        stage_row32<BN>(ring + SplitRecv<BN>::kBytes, row_in_tile, j * 32,
+                                        &sum[j * 32]);
+                    continue;
+                }
 #pragma unroll
                 for (int j = 0; j < BN / 32; ++j) {
                     const int32_t x = col0 + j * 32;   // 32 int32 = one 128-byte buffer row
@@ -384,13 +411,17 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             const uint32_t buf = acc_iter & 1u;
             const uint32_t acc_phase = (acc_iter >> 1) & 1u;
-            if (!wait_phase(smem_addr(&ctl->tmem_full[buf]), acc_phase, watch, kSiteEpiTmemFull))
+            if (!wait_phase(smem_addr(&ctl->tmem_full[buf]), acc_phase, watch, kSiteEpiTmemFull)) {
+                ok = false;
                 break;
+            }
             tc_fence_after();
+            // (cluster split: the accumulator stays in TMEM until it is pushed after
+            // the cluster barrier)
 #pragma unroll 1
             for (int sc = 0; sc < BN / 64; ++sc) {
                 const int32_t x = col0 + sc * 64;
-                if (y >= p.M || x >= p.N) continue;   // warp-uniform
+                if (p.cluster_split || y >= p.M || x >= p.N) continue;   // warp-uniform
                 const uint32_t sbuf = store_buf0 + store_sel * L::kStoreBufBytes;
                 if (lane == 0) bulk_wait_group_read<1>();
                 __syncwarp();
@@ -418,12 +449,51 @@ __global__ void __launch_bounds__(kThreads, 1)
             __syncwarp();
             if (lane == 0) {
                 const uint32_t bar = smem_addr(&ctl->tmem_empty[buf]);
-                mbar_arrive_remote(map_to_rank(bar, 0));
+                mbar_arrive_remote(map_to_rank(bar, lead));
             }
             ++acc_iter;
         }
         if (lane == 0) bulk_wait_group_read<0>();   // sources read; writes complete with the grid
         __syncwarp();
+        epi_ok = ok && pair < p.num_units;
+    }
+
+    // ------------------------------------- split-K reduction across the cluster's pairs
+    if (p.cluster_split) {
+        fence_proxy_async_smem();   // the TMA-written ring now receives peers' stores
+        cluster_sync_all();         // every pair's main loop is over: all rings are idle
+        tc_fence_after();
+        const UnitCoord c = c_first;
+        if (warp >= 2 && epi_ok) {
+            // rows of this CTA's half go to the CTAs (s', same half) of the cluster
+            const int quad = warp & 3;
+            const int row = quad * 32 + lane;
+#pragma unroll 1
+            for (int j = 0; j < BN / 32; ++j) {
+                uint32_t v[32];
+                if constexpr (OUT == kOutI32) {
+                    const uint32_t src = ring + SplitRecv<BN>::kBytes +
+                                         static_cast<uint32_t>((row * (BN + 4) + j * 32) * 4);
+#pragma unroll
+                    for (int g = 0; g < 8; ++g) {
+                        const uint4 q = ld_shared_u4(src + g * 16);
+                        v[g * 4 + 0] = q.x;
+                        v[g * 4 + 1] = q.y;
+                        v[g * 4 + 2] = q.z;
+                        v[g * 4 + 3] = q.w;
+                    }
+                } else {
+                    tmem_ld_32x32b_x32(tmem_base + (static_cast<uint32_t>(quad * 32) << 16) + j * 32, v);
+                    tmem_ld_wait();
+                }
+                push_row32<BN>(ring, p.split_k, c.split, row, j * 32, v, 2u, rank);
+            }
+        }
+        cluster_sync_all();         // every slice has arrived at its owner
+        if (warp >= 2)
+            cluster_sum_store<BN, OUT>(p, c.m_blk * 2 * kBM + static_cast<int32_t>(rank) * kBM,
+                                       c.n_blk * BN, static_cast<int>(crank >> 1), ring,
+                                       static_cast<int>(threadIdx.x) - 64, kEpiWarps * 32);
     }
 
     // ---------------------------------------------------------------- teardown

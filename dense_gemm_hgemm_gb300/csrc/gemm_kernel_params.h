@@ -35,6 +35,10 @@ struct KParams {
     int32_t direct_store;   // 1: epilogue stores C with 16-byte st.global per thread; 0: TMA stores
     int32_t a_mn_major;     // 1: A stored K x M (M contiguous); 0: M x K (K contiguous)
     int32_t b_mn_major;     // 1: B stored K x N (N contiguous); 0: N x K (K contiguous)
+    int32_t mcast;          // > 1: clusters of mcast CTAs own mcast adjacent N-tiles of the same
+                            // rows; each loads 1/mcast of the A tile and multicasts it to all
+                            // (num_units then counts tile groups)
+    int32_t l2_prefetch;    // > 0: the producer also prefetches k-block kb + l2_prefetch into L2
     int32_t num_units;      // m_blocks * n_blocks * split_k
     uint32_t idesc;         // tcgen05 instruction descriptor
     uint32_t tx_extra;      // extra bytes each ring slot expects (0 in normal operation)
@@ -45,6 +49,39 @@ struct KParams {
     uint32_t* counters;     // split-K arrival counter per tile (self-resetting)
     int32_t* error_word;
     uint64_t timeout_ns;
+    // Multiply-shift divisors of the work decomposition (see FastDiv): by
+    // split_k, and of the raster over (m_blocks, raster_n) in bands of
+    // raster_group, where raster_n is n_blocks, or the number of n-block groups
+    // with multicast (mcast = 1 << mcast_shift).
+    FastDiv fd_split;
+    RasterDiv rd;
+    int32_t raster_n;
+    int32_t mcast_shift;
 };
+
+// Coordinates of unit u (as unit_coord) from the plan's precomputed divisors.
+GBG_HD UnitCoord unit_coord_fast(int32_t u, const KParams& p) {
+    UnitCoord c;
+    c.tile = fdiv(u, p.fd_split);
+    c.split = u - c.tile * p.split_k;
+    raster_tile_fast(p.m_blocks, p.rd, c.tile, &c.m_blk, &c.n_blk);
+    c.kb_begin = c.split * p.kb_per_split;
+    const int32_t e = c.kb_begin + p.kb_per_split;
+    c.kb_end = e < p.num_kb ? e : p.num_kb;
+    return c;
+}
+
+// Fill the divisor fields from the plain ones (m_blocks, n_blocks, split_k,
+// raster_group, mcast).
+inline void set_divisors(KParams* p) {
+    p->fd_split = make_fastdiv(p->split_k);
+    const int32_t mc = p->mcast > 1 ? p->mcast : 1;
+    p->raster_n = (p->n_blocks + mc - 1) / mc;
+    int32_t sh = 0;
+    while ((1 << sh) < mc) ++sh;
+    p->mcast_shift = sh;
+    const int32_t g = p->raster_group < 1 ? 1 : p->raster_group;
+    p->rd = make_raster_div(p->m_blocks, p->raster_n, g);
+}
 
 }  // namespace gbg

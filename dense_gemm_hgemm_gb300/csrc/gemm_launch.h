@@ -38,6 +38,14 @@ cudaError_t gemm_launch_bf16(int bn, int stages, const LaunchShape&, const CUten
 cudaError_t gemm_launch_i32(int bn, int stages, const LaunchShape&, const CUtensorMap&, const CUtensorMap&,
                             const CUtensorMap&, const KParams&, cudaStream_t);
 
+// Co-resident clusters of shape.cluster CTAs of a kernel variant (pair = 1: the
+// SM-pair kernel).
+cudaError_t gemm_max_clusters(int bn, int stages, int out, int pair, const LaunchShape& shape,
+                              int* n);
+const void* gemm_kernel_ptr_f16(int bn, int stages, int pair);
+const void* gemm_kernel_ptr_bf16(int bn, int stages, int pair);
+const void* gemm_kernel_ptr_i32(int bn, int stages, int pair);
+
 // SM-pair (cta_group::2) kernels, 16-bit outputs.
 cudaError_t gemm_prepare_pair_f16(int bn, int stages, size_t* smem_bytes);
 cudaError_t gemm_prepare_pair_bf16(int bn, int stages, size_t* smem_bytes);

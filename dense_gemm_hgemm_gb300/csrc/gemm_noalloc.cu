@@ -204,6 +204,7 @@ extern "C" gemm_status_t gemm_run_splitk_noalloc(int64_t M, int64_t N, int64_t K
     kp.chunk_kb = static_cast<int32_t>(per);
     kp.raster_group = static_cast<int32_t>(m_blocks < 16 ? m_blocks : 16);
     kp.num_units = static_cast<int32_t>(tiles * s);
+    gbg::set_divisors(&kp);
     const uint32_t fmt = dtype == GEMM_BF16 ? 1u : 0u;
     kp.idesc = (1u << 4) | (fmt << 7) | (fmt << 10) |
                (static_cast<uint32_t>(kBlockN >> 3) << 17) |

@@ -102,6 +102,13 @@ typedef enum {
  *   direct_store : epilogue store path: 0 = TMA tensor stores from a swizzled
  *                  shared-memory buffer; 1 = 16-byte global stores from each
  *                  thread's row (one-SM kernel only)
+ *   multicast    : 0/1 = off; 2 or 4 = clusters of that many CTAs compute
+ *                  adjacent N-tiles of the same rows, each loading 1/multicast
+ *                  of the shared A tile and multicasting it to the others
+ *                  (one-SM kernel, split_k 1; 4 needs A stored M x K)
+ *   l2_prefetch  : 0 = off; d in 1..64 = while loading k-block kb, also ask L2
+ *                  to fetch k-block kb + d of the same tile (hides DRAM latency
+ *                  on long K)
  */
 typedef struct {
     int32_t block_n;
@@ -112,6 +119,8 @@ typedef struct {
     int32_t split_mode;
     int32_t cta_pair;
     int32_t direct_store;
+    int32_t multicast;
+    int32_t l2_prefetch;
 } gemm_config_t;
 
 typedef struct gemm_plan *gemm_plan_t;
@@ -179,6 +188,17 @@ gemm_status_t gemm_plan_destroy(gemm_plan_t plan);
 
 /* The configuration a plan runs with. */
 gemm_status_t gemm_plan_get_config(gemm_plan_t plan, gemm_config_t *config);
+
+/*
+ * How the plan launches its GEMM kernel: `grid` CTAs in thread-block clusters
+ * of `cluster` CTAs, of which at most `max_active_clusters` fit on the device
+ * at once (as the CUDA occupancy calculator reports for the kernel, its block
+ * size and shared memory; 0 if that query failed).  A grid above
+ * cluster * max_active_clusters runs in more than one wave.  Any output pointer
+ * may be NULL.  GEMM_ERR_INVALID_ARG for a NULL plan.
+ */
+gemm_status_t gemm_plan_get_launch(gemm_plan_t plan, int32_t *grid, int32_t *cluster,
+                                   int32_t *max_active_clusters);
 
 /*
  * Set the limit, in nanoseconds, after which a kernel wait of this plan gives

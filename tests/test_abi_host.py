@@ -89,6 +89,7 @@ def test_null_handles(gemm_lib):
     assert lib.gemm_run(None, None, None, None, None) == 1
     assert lib.gemm_plan_check(None, None) == 1
     assert lib.gemm_plan_get_config(None, None) == 1
+    assert lib.gemm_plan_get_launch(None, None, None, None) == 1
     assert lib.gemm_plan_set_timeout(None, 5) == 1
     assert lib.gemm_plan_create(64, 64, 64, 0, 0, None) == 1
 
@@ -201,10 +202,63 @@ def test_table_covers_the_sweep_and_named_shapes(gemm_lib):
 def test_pair_config_validation(gemm_lib):
     ok = gemm_lib.gemm_workspace_bytes(4096, 4096, 4096, "f16", {"block_n": 256, "cta_pair": 1})
     assert ok > 0
+    base = gemm_lib.gemm_workspace_bytes(1024, 1024, 4096, "f16", {"block_n": 256, "cta_pair": 1})
+    for s in (2, 4):   # K slices across the pairs of one cluster of 2 * s CTAs: no scratch
+        cfg = {"block_n": 256, "cta_pair": 1, "split_k": s, "split_mode": 1}
+        assert gemm_lib.gemm_workspace_bytes(1024, 1024, 4096, "f16", cfg) == base
     for dtype, bad in (("i8", {"block_n": 256, "cta_pair": 1}),
                        ("f16", {"block_n": 64, "cta_pair": 1}),
                        ("f16", {"block_n": 256, "cta_pair": 1, "split_k": 2}),
+                       ("f16", {"block_n": 256, "cta_pair": 1, "split_k": 8, "split_mode": 1}),
                        ("f16", {"block_n": 256, "cta_pair": 1, "stages": 4}),
                        ("f16", {"block_n": 256, "cta_pair": 3})):
         with pytest.raises(gemm_lib.GemmError):
             gemm_lib.gemm_workspace_bytes(4096, 4096, 4096, dtype, bad)
+
+
+def test_multicast_config_validation(gemm_lib):
+    ok = gemm_lib.gemm_workspace_bytes(1024, 1024, 4096, "f16", {"block_n": 64, "multicast": 4})
+    assert ok == gemm_lib.gemm_workspace_bytes(1024, 1024, 4096, "f16", {"block_n": 64})
+    for bad in ({"block_n": 64, "multicast": 3},
+                {"block_n": 64, "multicast": 8},
+                {"block_n": 64, "multicast": 2, "split_k": 2},
+                {"block_n": 256, "multicast": 2, "cta_pair": 1}):
+        with pytest.raises(gemm_lib.GemmError):
+            gemm_lib.gemm_workspace_bytes(1024, 1024, 4096, "f16", bad)
+
+
+def test_multicast_four_needs_k_major_a(gemm_lib):
+    import ctypes
+    cfg = gemm_lib._config({"block_n": 64, "multicast": 4})
+    h = ctypes.c_void_p()
+    lib = gemm_lib.library()
+    for layout in (2, 3):                 # TT, NT: A stored K x M
+        assert lib.gemm_plan_create_with_config(512, 512, 512, 0, layout, ctypes.byref(cfg),
+                                                ctypes.byref(h)) == 1   # INVALID_ARG
+
+
+def _raster_reference(mb, nb, g, t):
+    """The raster order by definition: bands of g m-blocks (the last band may be
+    shorter); inside a band the m index runs fastest."""
+    band = g * nb
+    first_m = (t // band) * g
+    r = t % band
+    gsize = min(g, mb - first_m)
+    return first_m + r % gsize, r // gsize
+
+
+@pytest.mark.parametrize("mb,nb,g", [(1, 1, 1), (3, 5, 2), (7, 3, 16), (64, 32, 16), (33, 57, 8),
+                                     (1000, 3, 7), (4096, 2048, 24), (129, 1, 128), (5, 9, 5),
+                                     (46341, 46340, 3)])
+def test_raster_matches_its_definition(gemm_lib, mb, nb, g):
+    """The kernels evaluate the raster with multiply-shift divisions; compare
+    with integer division on tiles spread over the whole grid (both band kinds,
+    the last band, large tile ids)."""
+    import random
+    total = mb * nb
+    rng = random.Random(mb * 1000003 + nb * 7 + g)
+    ts = set(range(min(total, 2000)))
+    ts |= {total - 1 - i for i in range(min(total, 2000))}
+    ts |= {rng.randrange(total) for _ in range(3000)}
+    for t in sorted(ts):
+        assert gemm_lib.gemm_tile_coords(mb, nb, g, t) == _raster_reference(mb, nb, g, t), (t,)

@@ -23,6 +23,10 @@ MODES = [
     ("workspace_split", (200, 136, 1024), {"block_n": 64, "split_k": 3}),
     ("cluster_split", (128, 256, 2048), {"block_n": 64, "split_k": 4, "split_mode": 1}),
     ("sm_pair", (1000, 520, 512), {"block_n": 256, "cta_pair": 1}),
+    ("multicast2", (300, 264, 1000), {"block_n": 64, "multicast": 2}),
+    ("multicast4", (200, 520, 640), {"block_n": 128, "multicast": 4}),
+    ("pair_split", (300, 264, 1024), {"block_n": 256, "cta_pair": 1, "split_k": 4,
+                                      "split_mode": 1}),
 ]
 
 

@@ -21,6 +21,9 @@ CONFIGS = [
     ("workspace_split", (128, 128, 1024), {"block_n": 64, "split_k": 4}),
     ("cluster_split", (128, 128, 1024), {"block_n": 64, "split_k": 4, "split_mode": 1}),
     ("sm_pair", (512, 512, 512), {"block_n": 256, "cta_pair": 1}),
+    ("sm_pair_split", (512, 512, 1024), {"block_n": 256, "cta_pair": 1, "split_k": 4,
+                                         "split_mode": 1}),
+    ("multicast", (256, 512, 512), {"block_n": 64, "multicast": 4}),
 ]
 
 

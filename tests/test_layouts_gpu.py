@@ -19,6 +19,8 @@ CONFIGS = [
     ("pair256", {"block_n": 256, "cta_pair": 1}),
     ("split_ws", {"block_n": 64, "split_k": 3}),
     ("split_cluster", {"block_n": 128, "split_k": 4, "split_mode": 1}),
+    ("pair_split", {"block_n": 256, "cta_pair": 1, "split_k": 2, "split_mode": 1}),
+    ("multicast2", {"block_n": 64, "multicast": 2}),
 ]
 SHAPES = [(136, 72, 200), (384, 264, 512), (1000, 520, 1024)]
 

@@ -107,6 +107,28 @@ def test_pair_kernel_parity(shape, bn, dtype):
 
 
 @pytest.mark.parametrize("dtype", ["f16", "bf16", "i8"])
+@pytest.mark.parametrize("split", [2, 4])
+@pytest.mark.parametrize("shape", [(256, 128, 1024), (300, 264, 1000), (1000, 520, 4096),
+                                   (64, 136, 640)],
+                         ids=lambda s: "x".join(map(str, s)))
+def test_pair_cluster_split_k_parity_and_determinism(shape, split, dtype):
+    """SM pairs with K sliced across the pairs of one cluster (2 * split CTAs),
+    reduced in distributed shared memory in slice order: ragged M (the peer's
+    half beyond M), ragged N and K, uneven last slice."""
+    M, N, K = shape
+    if dtype == "i8":
+        K = -(-K // 16) * 16                  # int8 rows must be whole 16-byte groups
+    A, B = inputs.make_operands(M, N, K, dtype)
+    for bn in ((128,) if dtype == "i8" else (128, 256)):
+        cfg = {"block_n": bn, "cta_pair": 1, "split_k": split, "split_mode": 1}
+        C1 = pu.run_gpu(A, B, dtype, cfg, repeats=2)
+        pu.check_full(A, B, dtype, C1, "pair split %d bn=%d %s %s" % (split, bn, shape, dtype))
+        C2 = pu.run_gpu(A, B, dtype, cfg)
+        assert torch.equal(C1.view(torch.int16) if dtype != "i8" else C1,
+                           C2.view(torch.int16) if dtype != "i8" else C2)
+
+
+@pytest.mark.parametrize("dtype", ["f16", "bf16", "i8"])
 @pytest.mark.parametrize("shape", [(64, 4096, 64), (130, 72, 208), (257, 520, 1040)],
                          ids=lambda s: "x".join(map(str, s)))
 def test_direct_store_epilogue_parity(shape, dtype):

@@ -56,8 +56,11 @@ def test_noalloc_matches_plan_entry_point_two_calls_in_a_row(gemm_lib):
         torch.cuda.synchronize()
         g.gemm_run_splitk_noalloc(M, N, K, dtype, split, dA, dB, got)
         torch.cuda.synchronize()
+    free_after = torch.cuda.mem_get_info()[0]
+    # (checked afterwards: the comparison itself may make torch's allocator grow)
+    for M, N, K, dtype, split, dA, dB, want, got in prepared:
         _tolerance_check(got, want, K)
-    assert torch.cuda.mem_get_info()[0] == free_before   # the calls allocated nothing
+    assert free_after == free_before   # the calls allocated nothing
 
 
 def test_noalloc_rejects_problems_beyond_its_scratch(gemm_lib):
