@@ -238,6 +238,40 @@ def time_sweep(items, dist, steps, warmup, stream, sampler=None):
     return ms, wall, clocks
 
 
+def capture_step(items, stream):
+    """One sweep step (all 343 gemm_run launches) captured as a CUDA graph: the
+    same kernels, parameters and buffers, replayed without per-launch host work."""
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        run_step(items, stream)
+    torch.cuda.synchronize()
+    return graph
+
+
+def time_graph(graph, dist, steps, warmup, stream, sampler=None):
+    with torch.cuda.stream(stream):
+        for _ in range(warmup):
+            graph.replay()
+    torch.cuda.synchronize()
+    dist.barrier()
+    torch.cuda.synchronize()
+    if sampler:
+        sampler.start()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    t0 = time.perf_counter()
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for _ in range(steps):
+            graph.replay()
+        e1.record(stream)
+    torch.cuda.synchronize()
+    wall = time.perf_counter() - t0
+    clocks = sampler.stop() if sampler else None
+    dist.barrier()
+    return e0.elapsed_time(e1), wall, clocks
+
+
 def per_shape_times(items, stream, reps=3):
     """Device time of every launch of one step (events around each launch), median of reps."""
     res = {}
@@ -295,13 +329,30 @@ def e2e_sweep(items, stream, steps):
     return ms, h2d, d2h
 
 
-def launch_floor_us(stream, sms, n=2000):
+def launch_floor_us(stream, sms, n=2000, graph=False):
+    """Back-to-back period of an empty kernel launched like the GEMM (PDL, one CTA
+    per SM): eagerly one call at a time, or replayed from a captured graph."""
     import dense_gemm_hgemm_gb300 as g
     for _ in range(100):
         g.gemm_launch_empty(sms, stream.cuda_stream)
     torch.cuda.synchronize()
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
+    if graph:
+        per = 500
+        cg = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(cg, stream=stream):
+            for _ in range(per):
+                g.gemm_launch_empty(sms, stream.cuda_stream)
+        with torch.cuda.stream(stream):
+            cg.replay()
+            torch.cuda.synchronize()
+            e0.record(stream)
+            for _ in range(n // per):
+                cg.replay()
+            e1.record(stream)
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) * 1e3 / (per * (n // per))
     e0.record(stream)
     for _ in range(n):
         g.gemm_launch_empty(sms, stream.cuda_stream)
@@ -522,10 +573,18 @@ def ours(args):
             plan.check(stream)
         return
 
-    sampler = ClockSampler(dist.local_rank)
-    ms, wall, clocks = time_sweep(items, dist, args.steps, args.warmup, stream, sampler)
+    # Eager: one gemm_run (ctypes -> C ABI -> cudaLaunchKernelEx) per shape.
+    ms_e, wall_e, _ = time_sweep(items, dist, args.steps, args.warmup, stream)
     for _, plan, *_ in items:
         plan.check(stream)     # raises if any kernel gave up on a wait
+    ms_step_eager = dist.max(ms_e) / args.steps
+    # Headline: the same step launched from a captured CUDA graph (the launch
+    # overhead of 343 mostly tiny GEMMs is host work, not GEMM work).
+    graph = capture_step(items, stream)
+    sampler = ClockSampler(dist.local_rank)
+    ms, wall, clocks = time_graph(graph, dist, args.steps, args.warmup, stream, sampler)
+    for _, plan, *_ in items:
+        plan.check(stream)
     ms_max = dist.max(ms)
     ms_step = ms_max / args.steps
     value = dist.world * flops_step / (ms_step * 1e-3) / 1e12
@@ -540,7 +599,11 @@ def ours(args):
                    "compulsory_bytes_per_step": bytes_step,
                    "l2": "inputs larger than L2: each shape has its own A, B, C "
                          "(%.2f GB per step vs 129 MB L2); no explicit flush" % (bytes_step / 1e9),
-                   "replicas": dist.world, "layout": "TN", "accumulate": "fp32"},
+                   "replicas": dist.world, "layout": "TN", "accumulate": "fp32",
+                   "launch": "one step = the 343 gemm_run launches captured once as a CUDA "
+                             "graph and replayed; eager = one gemm_run call per shape"},
+        "eager": {"value": round(dist.world * flops_step / (ms_step_eager * 1e-3) / 1e12, 3),
+                  "unit": UNIT, "ms_per_step": round(ms_step_eager, 4)},
         "gpu_launches": len(items) * args.steps,
         "clocks": clocks,
         "wall_s_timed_region": round(wall, 3),
@@ -559,14 +622,16 @@ def ours(args):
 
     if not args.skip_extras and dist.rank == 0:
         floor = launch_floor_us(stream, sms)
+        floor_graph = launch_floor_us(stream, sms, graph=True)
         times = per_shape_times(items, stream)
-        t_meas = t_roof = 0.0
+        t_meas = t_roof = t_roof_graph = 0.0
         classes = {}
         for w, *_ in items:
             us = times[w.name] * 1e3
             tt = w.flops / (peaks["bf16_tflops"] * 1e12) * 1e6
             th = w.compulsory_bytes / (peaks["hbm_gbs"] * 1e9) * 1e6
             tr = max(tt, th, floor)
+            t_roof_graph += max(tt, th, floor_graph)
             kind = "tensor" if tr == tt else ("hbm" if tr == th else "launch")
             c = classes.setdefault(kind, {"shapes": 0, "t_meas_us": 0.0, "t_roof_us": 0.0})
             c["shapes"] += 1
@@ -581,20 +646,26 @@ def ours(args):
         head = workloads.HEADLINE_SWEEP.name.replace("hgemm_tn_", "sweep_").replace("_f16", "_f16")
         line["sweep_roofline"] = {
             "launch_floor_us": round(floor, 3),
-            "t_roof_us_sum": round(t_roof, 1),
-            "frac_of_timed_step": round(t_roof / (ms_step * 1e3), 4),
+            "launch_floor_graph_us": round(floor_graph, 3),
+            "t_roof_us_sum": round(t_roof_graph, 1),
+            "frac_of_timed_step": round(t_roof_graph / (ms_step * 1e3), 4),
+            "t_roof_us_sum_eager_floor": round(t_roof, 1),
+            "frac_of_eager_step": round(t_roof / (ms_step_eager * 1e3), 4),
             "t_meas_us_sum_isolated": round(t_meas, 1),
             "frac_isolated": round(t_roof / t_meas, 4), "by_bound_isolated": classes,
             "rule": "per shape t_roof = max(2MNK/bf16 burst peak, compulsory bytes/HBM, "
-                    "launch floor of an empty kernel launched like the GEMM); "
-                    "frac_of_timed_step = sum t_roof / timed ms_per_step; *_isolated = each "
-                    "launch timed alone between events (no launch overlap)",
+                    "launch floor of an empty kernel launched like the GEMM: from a graph "
+                    "for the timed (graph) step, one call at a time for the eager step and "
+                    "the isolated times); frac_of_timed_step = sum t_roof / timed "
+                    "ms_per_step; *_isolated = each launch timed alone between events (no "
+                    "launch overlap)",
             "headline_128x2048x128_us_in_sweep": round(times.get("sweep_128x2048x128_f16", 0) * 1e3, 3),
         }
         e2e_ms, h2d, d2h = e2e_sweep(items, stream, steps=max(3, min(20, args.steps)))
         line["e2e"] = {"value": round(flops_step / (e2e_ms * 1e-3) / 1e12, 3), "unit": UNIT,
                        "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                        "ms_per_step": round(e2e_ms, 3)}
+        del graph
         for _, plan, *_ in items:
             plan.close()
         del items

@@ -46,6 +46,12 @@ def candidates(M, N, K, dtype, sms):
             if s == 1 and K <= 1024:
                 out.append({"block_n": bn, "split_k": 1, "raster_group": 16, "split_mode": 0,
                             "direct_store": 1})
+            if s == 1 and K >= 512 and tiles >= 2:
+                # clusters sharing each A tile by multicast (2 or 4 adjacent N-tiles)
+                for mc in (2, 4):
+                    if -(-N // bn) >= mc:
+                        out.append({"block_n": bn, "split_k": 1, "raster_group": 16,
+                                    "split_mode": 0, "multicast": mc})
             per = -(-num_kb // s) if s > 1 else 0
             if s in (2, 4, 8) and -(-num_kb // per) == s:
                 out.append({"block_n": bn, "split_k": s, "raster_group": 16, "split_mode": 1})
@@ -56,30 +62,51 @@ def candidates(M, N, K, dtype, sms):
             for g in groups:
                 out.append({"block_n": bn, "split_k": 1, "raster_group": g, "split_mode": 0,
                             "cta_pair": 1})
+            for ps in (2, 4):
+                # K sliced over the pairs of one cluster (2 * ps CTAs), one wave at most
+                per = -(-num_kb // ps)
+                if (num_kb >= 2 * ps and -(-num_kb // per) == ps
+                        and pair_tiles * ps * 2 <= sms and pair_tiles < sms // 2):
+                    out.append({"block_n": bn, "split_k": ps, "raster_group": 8,
+                                "split_mode": 1, "cta_pair": 1})
     return out
 
 
 def _time(plan, copies, stream, flush, batches=5, reps_warm=20):
+    """(seq, warm) microseconds per call.  seq: after an L2 flush, the R cold
+    copies back to back; warm: the same buffers back to back.  Both replay a
+    captured CUDA graph, so the device time is measured, not the host's launch
+    rate (small shapes are far faster on the device than one Python call)."""
     import torch
     A0, B0, C0 = copies[0]
     for _ in range(3):
         plan.run(A0, B0, C0, stream)
+    torch.cuda.synchronize()
+    g_seq = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g_seq, stream=stream):
+        for A, B, C in copies:
+            plan.run(A, B, C, stream)
+    g_warm = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g_warm, stream=stream):
+        for _ in range(reps_warm):
+            plan.run(A0, B0, C0, stream)
+    torch.cuda.synchronize()
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
     seq = []
-    for _ in range(batches):
-        with torch.cuda.stream(stream):
+    with torch.cuda.stream(stream):
+        g_seq.replay()
+        for _ in range(batches):
             flush.add_(1)
+            e0.record(stream)
+            g_seq.replay()
+            e1.record(stream)
+            torch.cuda.synchronize()
+            seq.append(e0.elapsed_time(e1) * 1e3 / len(copies))
+        g_warm.replay()
         e0.record(stream)
-        for A, B, C in copies:
-            plan.run(A, B, C, stream)
+        g_warm.replay()
         e1.record(stream)
-        torch.cuda.synchronize()
-        seq.append(e0.elapsed_time(e1) * 1e3 / len(copies))
-    e0.record(stream)
-    for _ in range(reps_warm):
-        plan.run(A0, B0, C0, stream)
-    e1.record(stream)
     torch.cuda.synchronize()
     plan.check(stream)
     return statistics.median(seq), e0.elapsed_time(e1) * 1e3 / reps_warm
@@ -126,14 +153,15 @@ def sweep(out_path, only=None, dtype=None):
             rec["candidates"].append({**cfg, "seq_us": round(seq, 3), "warm_us": round(warm, 3)})
         best = min(rec["candidates"], key=lambda c: (c["seq_us"], c["warm_us"]))
         rec["best"] = {k: best.get(k, 0) for k in ("block_n", "split_k", "raster_group",
-                                                   "split_mode", "cta_pair", "direct_store")}
+                                                   "split_mode", "cta_pair", "direct_store",
+                                                   "multicast")}
         rec["model"] = g.gemm_select_config(M, N, K, dtype, sms)
         results.append(rec)
         del copies
     doc = {"gpu": props.name, "sms": sms, "when": time.strftime("%Y-%m-%dT%H:%M:%SZ", time.gmtime()),
            "seconds": round(time.time() - t_start, 1),
-           "regime": "seq: L2 flushed, R cold copies back to back, median of 5 batches; "
-                     "warm = same buffers back to back, mean of 20",
+           "regime": "CUDA-graph replay; seq: L2 flushed, R cold copies back to back, median "
+                     "of 5 batches; warm = same buffers back to back, mean of 20",
            "shapes": results}
     with open(out_path, "w") as f:
         json.dump(doc, f, indent=1)
@@ -151,7 +179,7 @@ def compact(full_json, out_json=TUNED_JSON):
         key = lambda c: (c["seq_us"], c["warm_us"])
         b = min(r["candidates"], key=key)
         plain = [c for c in r["candidates"] if c["split_k"] == 1 and not c.get("cta_pair")
-                 and not c.get("direct_store")]
+                 and not c.get("direct_store") and not c.get("multicast")]
         rows.append({"M": r["M"], "N": r["N"], "K": r["K"], "dtype": r["dtype"],
                      "best": r["best"], "seq_us": b["seq_us"], "warm_us": b["warm_us"],
                      "plain_seq_us": min(plain, key=key)["seq_us"] if plain else None,
@@ -173,16 +201,17 @@ def emit(json_path, table_path=TABLE):
         "// (%s, %d SMs, %s; %s)." % (doc["gpu"], doc["sms"], doc["when"], doc["regime"]),
         "// Fields: M, N, K, dtype (0 f16, 1 bf16, 2 i8), block_n, split_k, raster_group,",
         "// split_mode (0 workspace, 1 cluster), cta_pair (0 one SM, 1 SM pair),",
-        "// direct_store (0 TMA store, 1 per-thread stores).",
+        "// direct_store (0 TMA store, 1 per-thread stores), multicast (0 off, 2/4 CTAs",
+        "// sharing each A tile).",
         "static const TableEntry kTunedTable[] = {",
     ]
     n = 0
     for r in doc["shapes"]:
         b = r["best"]
-        lines.append("    {%d, %d, %d, %d, %d, %d, %d, %d, %d, %d}," % (
+        lines.append("    {%d, %d, %d, %d, %d, %d, %d, %d, %d, %d, %d}," % (
             r["M"], r["N"], r["K"], code[r["dtype"]], b["block_n"], b["split_k"],
             b["raster_group"], b.get("split_mode", 0), b.get("cta_pair", 0),
-            b.get("direct_store", 0)))
+            b.get("direct_store", 0), b.get("multicast", 0)))
         n += 1
     lines.append("};")
     lines.append("static const int kTunedCount = %d;" % n)
