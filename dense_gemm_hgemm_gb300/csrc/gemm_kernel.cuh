@@ -770,7 +770,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const UnitCoord c = u == it.first ? c_first : unit_at(p, u);
                 for (int32_t kb = c.kb_begin; kb < c.kb_end; ++kb) {
                     const uint32_t full = smem_addr(&ctl->full[stage]);
-                    if (!wait_phase(smem_addr(&ctl->empty[stage]), phase ^ 1u, watch,
+                    // (the first pass over the ring finds every slot free)
+                    if (issued >= STAGES &&
+                        !wait_phase(smem_addr(&ctl->empty[stage]), phase ^ 1u, watch,
                                     kSiteProducerEmpty)) {
                         ok = false;
                         break;
@@ -847,7 +849,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const int32_t k1 = (k0 + p.chunk_kb < c.kb_end) ? k0 + p.chunk_kb : c.kb_end;
                     const uint32_t buf = acc_iter & 1u;
                     const uint32_t acc_phase = (acc_iter >> 1) & 1u;
-                    if (!wait_phase(smem_addr(&ctl->tmem_empty[buf]), acc_phase ^ 1u, watch,
+                    // (both accumulator buffers start free)
+                    if (acc_iter >= 2 &&
+                        !wait_phase(smem_addr(&ctl->tmem_empty[buf]), acc_phase ^ 1u, watch,
                                     kSiteMmaTmemEmpty)) {
                         ok = false;
                         break;
@@ -1080,13 +1084,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         epi_ok = ok && it.first < p.num_units;
     }
 
-    if (warp >= 2) {
-        // This warp's bulk stores must have read their shared-memory source before
-        // the CTA ends; their global writes complete with the grid.
-        if ((threadIdx.x & 31) == 0) bulk_wait_group_read<0>();
-        __syncwarp();
-    }
-
     // ------------------------------------------- split-K reduction in the cluster
     if (p.cluster_split) {
         fence_proxy_async_smem();   // the TMA-written ring now receives peers' stores
@@ -1133,6 +1130,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp == 1) {
         tc_fence_after();
         tmem_dealloc(tmem_base, kTmemCols);
+    } else if (warp >= 2) {
+        // This warp's bulk stores must have read their shared-memory source before
+        // the CTA ends (while warp 1 frees TMEM); their global writes complete
+        // with the grid.
+        if (lane == 0) bulk_wait_group_read<0>();
+        __syncwarp();
     }
 }
 

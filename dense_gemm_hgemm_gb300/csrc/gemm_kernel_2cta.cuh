@@ -245,7 +245,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int32_t a_row = c.m_blk * 2 * kBM + static_cast<int32_t>(rank) * kBM;
                 const int32_t b_row = c.n_blk * BN + static_cast<int32_t>(rank) * (BN / 2);
                 for (int32_t kb = c.kb_begin; kb < c.kb_end; ++kb) {
-                    if (!wait_phase(smem_addr(&ctl->empty[stage]), phase ^ 1u, watch,
+                    // (the first pass over the ring finds every slot free)
+                    if (issued >= STAGES &&
+                        !wait_phase(smem_addr(&ctl->empty[stage]), phase ^ 1u, watch,
                                     kSiteProducerEmpty)) {
                         ok = false;
                         break;
@@ -300,7 +302,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const int32_t k1 = (k0 + p.chunk_kb < c.kb_end) ? k0 + p.chunk_kb : c.kb_end;
                     const uint32_t buf = acc_iter & 1u;
                     const uint32_t acc_phase = (acc_iter >> 1) & 1u;
-                    if (!wait_phase_cluster(smem_addr(&ctl->tmem_empty[buf]), acc_phase ^ 1u,
+                    // (both accumulator buffers start free)
+                    if (acc_iter >= 2 &&
+                        !wait_phase_cluster(smem_addr(&ctl->tmem_empty[buf]), acc_phase ^ 1u,
                                             watch, kSiteMmaTmemEmpty)) {
                         ok = false;
                         break;
@@ -453,8 +457,6 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             ++acc_iter;
         }
-        if (lane == 0) bulk_wait_group_read<0>();   // sources read; writes complete with the grid
-        __syncwarp();
         epi_ok = ok && pair < p.num_units;
     }
 
@@ -502,6 +504,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp == 1) {
         tc_fence_after();
         tmem_dealloc_pair(tmem_base, kTmemCols);
+    } else if (warp >= 2) {
+        // bulk stores have read their shared-memory source before the CTA ends;
+        // their global writes complete with the grid
+        if (lane == 0) bulk_wait_group_read<0>();
+        __syncwarp();
     }
 }
 
