@@ -51,7 +51,8 @@ class gemm_config_t(ctypes.Structure):
                 ("split_k", ctypes.c_int32), ("raster_group", ctypes.c_int32),
                 ("max_ctas", ctypes.c_int32), ("split_mode", ctypes.c_int32),
                 ("cta_pair", ctypes.c_int32), ("direct_store", ctypes.c_int32),
-                ("multicast", ctypes.c_int32), ("l2_prefetch", ctypes.c_int32)]
+                ("multicast", ctypes.c_int32), ("l2_prefetch", ctypes.c_int32),
+                ("kblocks_per_stage", ctypes.c_int32)]
 
     def as_dict(self):
         return {f: int(getattr(self, f)) for f, _ in self._fields_}
@@ -145,6 +146,7 @@ def _config(cfg) -> gemm_config_t:
     c.direct_store = int(cfg.get("direct_store", 0))
     c.multicast = int(cfg.get("multicast", 0))
     c.l2_prefetch = int(cfg.get("l2_prefetch", 0))
+    c.kblocks_per_stage = int(cfg.get("kblocks_per_stage", 0))
     return c
 
 

@@ -98,14 +98,22 @@ gemm_status_t normalise_config(int64_t M, int64_t N, int64_t K, gemm_dtype_t dty
     if (c.multicast == 1) c.multicast = 0;   // 0 and 1 both mean off
     if (c.multicast != 0 && c.multicast != 2 && c.multicast != 4) return GEMM_ERR_INVALID_ARG;
     if (c.l2_prefetch < 0 || c.l2_prefetch > 64) return GEMM_ERR_INVALID_ARG;
+    if (c.kblocks_per_stage == 0) c.kblocks_per_stage = 1;
+    if (c.kblocks_per_stage != 1 && c.kblocks_per_stage != 2) return GEMM_ERR_INVALID_ARG;
+    if (c.kblocks_per_stage == 2 &&
+        ((!c.cta_pair && c.block_n > 128) || c.multicast > 1 || K % gbg::kBK != 0))
+        return GEMM_ERR_INVALID_ARG;
     if (c.cta_pair) {
         // SM pair: 256-row tiles; K is sliced only across the pairs of a cluster.
         if (c.block_n < 128) return GEMM_ERR_INVALID_ARG;
         if (dtype == GEMM_I8_I32 && c.block_n != 128) return GEMM_ERR_INVALID_ARG;
         if (c.split_k != 1 && c.split_mode != 1) return GEMM_ERR_INVALID_ARG;
     }
-    const int want_stages =
-        c.cta_pair ? gbg::default_pair_stages(c.block_n) : gbg::default_stages(c.block_n);
+    const bool ks2 = c.kblocks_per_stage == 2;
+    const int want_stages = c.cta_pair ? (ks2 ? gbg::default_pair_stages_ks2(c.block_n)
+                                              : gbg::default_pair_stages(c.block_n))
+                                       : (ks2 ? gbg::default_stages_ks2(c.block_n)
+                                              : gbg::default_stages(c.block_n));
     if (c.stages == 0) c.stages = want_stages;
     if (c.stages != want_stages) return GEMM_ERR_INVALID_ARG;
     if (c.split_k < 1 || c.raster_group < 1 || c.max_ctas < 0) return GEMM_ERR_INVALID_ARG;
@@ -223,9 +231,32 @@ gemm_status_t encode_mnmajor(CUtensorMap* map, const void* base, int64_t rows, i
     return r == CUDA_SUCCESS ? GEMM_OK : GEMM_ERR_TENSORMAP;
 }
 
-// Map for operand A (rows = M) or B (rows = N) in the plan's storage.
+// 3-D view of a K-contiguous rows x K operand (K % 64 == 0) as (64 elements,
+// rows, K/64 k-blocks) with strides (K*2 bytes, 128 bytes): one box of
+// 64 x box_rows x kblocks brings kblocks consecutive k-blocks of box_rows rows,
+// k-block-major in shared memory, 128-byte swizzled like the 2-D boxes.
+gemm_status_t encode_kmajor3d(CUtensorMap* map, const void* base, int64_t rows, int64_t K,
+                              int box_rows, int kblocks, CUtensorMapDataType dt) {
+    PFN_cuTensorMapEncodeTiled_v12000 fn = encode_fn();
+    if (!fn) return GEMM_ERR_TENSORMAP;
+    const cuuint64_t dims[3] = {static_cast<cuuint64_t>(gbg::kBK), static_cast<cuuint64_t>(rows),
+                                static_cast<cuuint64_t>(K / gbg::kBK)};
+    const cuuint64_t strides[2] = {static_cast<cuuint64_t>(K) * 2, static_cast<cuuint64_t>(gbg::kBK) * 2};
+    const cuuint32_t box[3] = {static_cast<cuuint32_t>(gbg::kBK), static_cast<cuuint32_t>(box_rows),
+                               static_cast<cuuint32_t>(kblocks)};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    const CUresult r = fn(map, dt, 3, const_cast<void*>(base), dims, strides, box, estr,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? GEMM_OK : GEMM_ERR_TENSORMAP;
+}
+
+// Map for operand A (rows = M) or B (rows = N) in the plan's storage; kblocks = 2
+// selects the 3-D two-k-block view (K-contiguous operands only).
 gemm_status_t encode_operand_map(CUtensorMap* map, const void* base, int64_t rows, int64_t K,
-                                 int box_rows, bool mn_major, CUtensorMapDataType dt) {
+                                 int box_rows, bool mn_major, CUtensorMapDataType dt,
+                                 int kblocks = 1) {
+    if (kblocks > 1) return encode_kmajor3d(map, base, rows, K, box_rows, kblocks, dt);
     return mn_major ? encode_mnmajor(map, base, rows, K, dt)
                     : encode_kmajor(map, base, rows, K, box_rows, dt);
 }
@@ -261,6 +292,9 @@ gemm_status_t create_plan(int64_t M, int64_t N, int64_t K, gemm_dtype_t dtype,
     if (st != GEMM_OK) return st;
     // A stored K x M is copied in 64-column blocks: at most two multicast slices
     if (user_cfg && user_cfg->multicast > 2 && a_mn_major(layout)) return GEMM_ERR_INVALID_ARG;
+    // two k-blocks per slot come as 3-D copies of K-contiguous operands only
+    if (user_cfg && user_cfg->kblocks_per_stage == 2 && layout != GEMM_LAYOUT_TN)
+        return GEMM_ERR_INVALID_ARG;
     if (user_cfg) {
         gemm_config_t tmp;
         int32_t per;
@@ -273,6 +307,10 @@ gemm_status_t create_plan(int64_t M, int64_t N, int64_t K, gemm_dtype_t dtype,
 
     gemm_config_t want = user_cfg ? *user_cfg : gbg::select_config(M, N, K, dtype, sms);
     if (want.multicast > 2 && a_mn_major(layout)) want.multicast = 2;
+    if (want.kblocks_per_stage == 2 && (layout != GEMM_LAYOUT_TN || K % gbg::kBK != 0)) {
+        want.kblocks_per_stage = 1;
+        want.stages = 0;
+    }
     gemm_config_t cfg;
     int32_t kb_per_split = 0;
     st = normalise_config(M, N, K, dtype, want, &cfg, &kb_per_split);
@@ -396,11 +434,12 @@ gemm_status_t create_plan(int64_t M, int64_t N, int64_t K, gemm_dtype_t dtype,
 
     if (dtype == GEMM_I8_I32 && M > 0 && N > 0 && K > 0) {
         st = encode_operand_map(&p->map_a, p->d_a16, M, K, gbg::kBM / kp.mcast, a_mn_major(layout),
-                                CU_TENSOR_MAP_DATA_TYPE_FLOAT16);
+                                CU_TENSOR_MAP_DATA_TYPE_FLOAT16, cfg.kblocks_per_stage);
         if (st == GEMM_OK)
             st = encode_operand_map(&p->map_b, p->d_b16, N, K,
                                     cfg.cta_pair ? cfg.block_n / 2 : cfg.block_n,
-                                    b_mn_major(layout), CU_TENSOR_MAP_DATA_TYPE_FLOAT16);
+                                    b_mn_major(layout), CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
+                                    cfg.kblocks_per_stage);
         if (st != GEMM_OK) {
             cudaFree(p->dmem);
             delete p;
@@ -523,7 +562,7 @@ gemm_status_t gemm_run_bias_act(gemm_plan_t p, const void* A, const void* B, voi
             p->map_a_valid = false;
             const gemm_status_t st =
                 encode_operand_map(&p->map_a, A, p->M, p->K, gbg::kBM / p->kp.mcast,
-                                   a_mn_major(p->layout), dt);
+                                   a_mn_major(p->layout), dt, p->cfg.kblocks_per_stage);
             if (st != GEMM_OK) return st;
             p->map_a_src = A;
             p->map_a_valid = true;
@@ -533,7 +572,8 @@ gemm_status_t gemm_run_bias_act(gemm_plan_t p, const void* A, const void* B, voi
             // an SM pair loads half of the tile's B rows per CTA
             const int b_rows = p->cfg.cta_pair ? p->cfg.block_n / 2 : p->cfg.block_n;
             const gemm_status_t st =
-                encode_operand_map(&p->map_b, B, p->N, p->K, b_rows, b_mn_major(p->layout), dt);
+                encode_operand_map(&p->map_b, B, p->N, p->K, b_rows, b_mn_major(p->layout), dt,
+                                   p->cfg.kblocks_per_stage);
             if (st != GEMM_OK) return st;
             p->map_b_src = B;
             p->map_b_valid = true;

@@ -16,7 +16,8 @@ namespace gbg {
 
 struct TableEntry {
     int32_t M, N, K, dtype;
-    int32_t block_n, split_k, raster_group, split_mode, cta_pair, direct_store, multicast;
+    int32_t block_n, split_k, raster_group, split_mode, cta_pair, direct_store, multicast,
+        kblocks_per_stage;
 };
 
 #include "gemm_config_table.inc"   // static const TableEntry kTunedTable[]; kTunedCount
@@ -40,6 +41,7 @@ inline gemm_config_t model_config(int64_t M, int64_t N, int64_t K, gemm_dtype_t 
     c.direct_store = 0;
     c.multicast = 0;
     c.l2_prefetch = 0;
+    c.kblocks_per_stage = 0;
     const int64_t mb = ceil_div(M, kBM);
     const int64_t num_kb = ceil_div(K, kBK);
     const int cands_f[3] = {256, 128, 64};
@@ -96,6 +98,7 @@ inline gemm_config_t select_config(int64_t M, int64_t N, int64_t K, gemm_dtype_t
             c.direct_store = e.direct_store;
             c.multicast = e.multicast;
             c.l2_prefetch = 0;
+            c.kblocks_per_stage = e.kblocks_per_stage;
             c.max_ctas = 0;
             return c;
         }

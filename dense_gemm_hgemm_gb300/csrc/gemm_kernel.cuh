@@ -45,10 +45,17 @@
 
 namespace gbg {
 
-template <int BN, int STAGES>
+// KS = 64-wide k-blocks per ring slot.  A slot's copies complete on one barrier
+// phase, and the copy engine turns a phase of one A and one B box around in
+// ~0.24 us per SM for boxes up to 32 KiB (measured on GB300), so with KS = 2 the
+// narrow tiles load each operand's two k-blocks as one 3-D box (operand maps
+// viewed as 64 elements x rows x k-blocks) and stream about twice as fast.
+template <int BN, int STAGES, int KS = 1>
 struct SmemLayout {
-    static constexpr int kBTileBytes = BN * kBK * 2;
-    static constexpr int kStageBytes = kATileBytes + kBTileBytes;
+    static constexpr int kBSubBytes = BN * kBK * 2;              // one k-block of B
+    static constexpr int kASlotBytes = KS * kATileBytes;         // A part of a slot
+    static constexpr int kBTileBytes = KS * kBSubBytes;          // B part of a slot
+    static constexpr int kStageBytes = kASlotBytes + kBTileBytes;
     static constexpr int kRingBytes = STAGES * kStageBytes;
     // Epilogue staging for TMA stores: per epilogue warp two 32-row x 128-byte
     // buffers (128-byte swizzle, 1024-byte aligned).
@@ -191,6 +198,25 @@ __device__ __forceinline__ void tma_prefetch_l2_2d(const CUtensorMap* map, int32
     asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(
                      reinterpret_cast<uint64_t>(map)),
                  "r"(x), "r"(y)
+                 : "memory");
+}
+
+// 3-D forms for an operand map viewed as (64 elements, rows, k-blocks): one copy
+// brings several consecutive 64-wide k-blocks of a tile, stacked k-block-major
+// in shared memory (the same image as one 2-D copy per k-block).
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map, uint32_t bar,
+                                            int32_t x, int32_t y, int32_t z) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(x), "r"(y), "r"(z)
+        : "memory");
+}
+__device__ __forceinline__ void tma_prefetch_l2_3d(const CUtensorMap* map, int32_t x, int32_t y,
+                                                   int32_t z) {
+    asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];" ::"l"(
+                     reinterpret_cast<uint64_t>(map)),
+                 "r"(x), "r"(y), "r"(z)
                  : "memory");
 }
 
@@ -676,12 +702,15 @@ __device__ __forceinline__ UnitCoord unit_at(const KParams& p, int32_t u) {
 // ----------------------------------------------------------------------------
 // the kernel
 // ----------------------------------------------------------------------------
-template <int BN, int STAGES, int OUT>
+// KS = 2: A and B are K-major and their maps are the 3-D views (the host
+// guarantees both; multicast is not combined with it).
+template <int BN, int STAGES, int OUT, int KS = 1>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_tn_kernel(const __grid_constant__ CUtensorMap tmap_a,
                    const __grid_constant__ CUtensorMap tmap_b,
                    const __grid_constant__ CUtensorMap tmap_c, const KParams p) {
-    using L = SmemLayout<BN, STAGES>;
+    using L = SmemLayout<BN, STAGES, KS>;
+    static_assert(KS == 1 || KS == 2, "k-blocks per ring slot");
     static_assert((OUT == kOutI32 ? 2 : 1) * SplitRecv<BN>::kBytes <= L::kRingBytes,
                   "split-K receive area (and parked integer sums) must fit in the ring");
     static_assert(BN == 64 || BN == 128 || BN == 256, "tile width");
@@ -693,7 +722,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t raw_addr = smem_addr(smem_raw);
     uint8_t* smem = smem_raw + ((1024u - (raw_addr & 1023u)) & 1023u);
     const uint32_t ring = smem_addr(smem);                       // A slots, then B slots
-    const uint32_t ring_b = ring + STAGES * kATileBytes;
+    const uint32_t ring_b = ring + STAGES * L::kASlotBytes;
     const uint32_t staging = ring + L::kRingBytes;              // epilogue store buffers
     SharedCtl<STAGES>* ctl =
         reinterpret_cast<SharedCtl<STAGES>*>(smem + L::kRingBytes + L::kStagingBytes);
@@ -743,15 +772,20 @@ __global__ void __launch_bounds__(kThreads, 1)
         // Only L2 is touched (the coherence point); the data is read after the
         // wait below, so this cannot observe stale values.
         const UnitCoord c = c_first;
-        const int32_t ahead = STAGES > p.l2_prefetch ? STAGES : p.l2_prefetch;
+        const int32_t ahead = STAGES * KS > p.l2_prefetch ? STAGES * KS : p.l2_prefetch;
         const int32_t kb_end = c.kb_begin + ahead < c.kb_end ? c.kb_begin + ahead : c.kb_end;
         // with multicast, this CTA's slice of the A tile (its A box is that slice)
         const int32_t a_rows = kBM >> p.mcast_shift;
         const int32_t a_row0 =
             c.m_blk * kBM + static_cast<int32_t>(blockIdx.x & ((1u << p.mcast_shift) - 1u)) * a_rows;
-        for (int32_t kb = c.kb_begin; kb < kb_end; ++kb) {
-            prefetch_operand(&tmap_a, kb, a_row0, a_rows, p.a_mn_major);
-            prefetch_operand(&tmap_b, kb, c.n_blk * BN, BN, p.b_mn_major);
+        for (int32_t kb = c.kb_begin; kb < kb_end; kb += KS) {
+            if constexpr (KS == 2) {
+                tma_prefetch_l2_3d(&tmap_a, 0, a_row0, kb);
+                tma_prefetch_l2_3d(&tmap_b, 0, c.n_blk * BN, kb);
+            } else {
+                prefetch_operand(&tmap_a, kb, a_row0, a_rows, p.a_mn_major);
+                prefetch_operand(&tmap_b, kb, c.n_blk * BN, BN, p.b_mn_major);
+            }
         }
     }
     grid_dependency_wait();
@@ -768,7 +802,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             bool ok = true;
             for (int32_t u = it.first; ok && u < p.num_units; u += it.stride) {
                 const UnitCoord c = u == it.first ? c_first : unit_at(p, u);
-                for (int32_t kb = c.kb_begin; kb < c.kb_end; ++kb) {
+                for (int32_t kb = c.kb_begin; kb < c.kb_end; kb += KS) {
                     const uint32_t full = smem_addr(&ctl->full[stage]);
                     // (the first pass over the ring finds every slot free)
                     if (issued >= STAGES &&
@@ -778,35 +812,49 @@ __global__ void __launch_bounds__(kThreads, 1)
                         break;
                     }
                     mbar_arrive_expect_tx(full, kStageTx + p.tx_extra);
-                    if (p.mcast > 1) {
-                        // this CTA's 1/mcast of the A tile, delivered to every CTA of
-                        // the cluster (the slot's bytes arrive from all of them)
-                        const int32_t rank = static_cast<int32_t>(blockIdx.x & (p.mcast - 1));
-                        const uint16_t all = static_cast<uint16_t>((1u << p.mcast) - 1u);
-                        const uint32_t a_slot = ring + stage * kATileBytes;
-                        if (p.a_mn_major) {   // mcast == 2: one 64-row M block each
-                            tma_load_2d_mcast(a_slot + static_cast<uint32_t>(rank) * 8192u, &tmap_a,
-                                              full, c.m_blk * kBM + rank * 64, kb * kBK, all);
-                        } else {
-                            const int32_t rows = kBM >> p.mcast_shift;
-                            tma_load_2d_mcast(a_slot + static_cast<uint32_t>(rank * rows * 128),
-                                              &tmap_a, full, kb * kBK, c.m_blk * kBM + rank * rows,
-                                              all);
+                    if constexpr (KS == 2) {
+                        // both k-blocks of each operand in one copy; a copy past the
+                        // end of K is zero-filled and past the slice end is unused,
+                        // but always delivers the full box
+                        tma_load_3d(ring + stage * L::kASlotBytes, &tmap_a, full, 0, c.m_blk * kBM, kb);
+                        tma_load_3d(ring_b + stage * L::kBTileBytes, &tmap_b, full, 0, c.n_blk * BN, kb);
+                        if (p.l2_prefetch > 0 && kb + p.l2_prefetch < c.kb_end) {
+                            tma_prefetch_l2_3d(&tmap_a, 0, c.m_blk * kBM, kb + p.l2_prefetch);
+                            tma_prefetch_l2_3d(&tmap_b, 0, c.n_blk * BN, kb + p.l2_prefetch);
                         }
                     } else {
-                        load_operand(ring + stage * kATileBytes, &tmap_a, full, kb, c.m_blk * kBM,
-                                     kBM, p.a_mn_major);
-                    }
-                    load_operand(ring_b + stage * L::kBTileBytes, &tmap_b, full, kb, c.n_blk * BN,
-                                 BN, p.b_mn_major);
-                    if (p.l2_prefetch > 0 && kb + p.l2_prefetch < c.kb_end) {
-                        // warm L2 with a later k-block of this tile (this CTA's A share)
-                        const int32_t a_rows = kBM >> p.mcast_shift;
-                        const int32_t a_rank =
-                            static_cast<int32_t>(blockIdx.x & ((1u << p.mcast_shift) - 1u));
-                        prefetch_operand(&tmap_a, kb + p.l2_prefetch, c.m_blk * kBM + a_rank * a_rows,
-                                         a_rows, p.a_mn_major);
-                        prefetch_operand(&tmap_b, kb + p.l2_prefetch, c.n_blk * BN, BN, p.b_mn_major);
+                        if (p.mcast > 1) {
+                            // this CTA's 1/mcast of the A tile, delivered to every CTA of
+                            // the cluster (the slot's bytes arrive from all of them)
+                            const int32_t rank = static_cast<int32_t>(blockIdx.x & (p.mcast - 1));
+                            const uint16_t all = static_cast<uint16_t>((1u << p.mcast) - 1u);
+                            const uint32_t a_slot = ring + stage * kATileBytes;
+                            if (p.a_mn_major) {   // mcast == 2: one 64-row M block each
+                                tma_load_2d_mcast(a_slot + static_cast<uint32_t>(rank) * 8192u,
+                                                  &tmap_a, full, c.m_blk * kBM + rank * 64, kb * kBK,
+                                                  all);
+                            } else {
+                                const int32_t rows = kBM >> p.mcast_shift;
+                                tma_load_2d_mcast(a_slot + static_cast<uint32_t>(rank * rows * 128),
+                                                  &tmap_a, full, kb * kBK, c.m_blk * kBM + rank * rows,
+                                                  all);
+                            }
+                        } else {
+                            load_operand(ring + stage * kATileBytes, &tmap_a, full, kb, c.m_blk * kBM,
+                                         kBM, p.a_mn_major);
+                        }
+                        load_operand(ring_b + stage * L::kBTileBytes, &tmap_b, full, kb, c.n_blk * BN,
+                                     BN, p.b_mn_major);
+                        if (p.l2_prefetch > 0 && kb + p.l2_prefetch < c.kb_end) {
+                            // warm L2 with a later k-block of this tile (this CTA's A share)
+                            const int32_t a_rows = kBM >> p.mcast_shift;
+                            const int32_t a_rank =
+                                static_cast<int32_t>(blockIdx.x & ((1u << p.mcast_shift) - 1u));
+                            prefetch_operand(&tmap_a, kb + p.l2_prefetch,
+                                             c.m_blk * kBM + a_rank * a_rows, a_rows, p.a_mn_major);
+                            prefetch_operand(&tmap_b, kb + p.l2_prefetch, c.n_blk * BN, BN,
+                                             p.b_mn_major);
+                        }
                     }
                     ++issued;
                     if (++stage == STAGES) {
@@ -858,21 +906,28 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                     tc_fence_after();
                     const uint32_t d_tmem = tmem_base + buf * BN;
-                    for (int32_t kb = k0; kb < k1; ++kb) {
+                    // (a slot never straddles chunks: chunk_kb is a multiple of KS)
+                    for (int32_t kb = k0; kb < k1; kb += KS) {
+                        const int32_t nsub = k1 - kb < KS ? k1 - kb : KS;
                         if (!wait_phase(smem_addr(&ctl->full[stage]), phase, watch, kSiteMmaFull)) {
                             ok = false;
                             break;
                         }
                         tc_fence_after();
-                        const uint64_t a_desc = operand_desc(ring + stage * kATileBytes, p.a_mn_major);
-                        const uint64_t b_desc =
-                            operand_desc(ring_b + stage * L::kBTileBytes, p.b_mn_major);
                         const uint32_t a_step = desc_k_step(p.a_mn_major);
                         const uint32_t b_step = desc_k_step(p.b_mn_major);
 #pragma unroll
-                        for (int k = 0; k < kBK / 16; ++k) {
-                            umma_f16(d_tmem, a_desc + a_step * k, b_desc + b_step * k, p.idesc,
-                                     (kb > k0 || k > 0) ? 1u : 0u);
+                        for (int32_t j = 0; j < KS; ++j) {
+                            if (j >= nsub) break;   // the slot's second k-block lies past the slice
+                            const uint64_t a_desc = operand_desc(
+                                ring + stage * L::kASlotBytes + j * kATileBytes, p.a_mn_major);
+                            const uint64_t b_desc = operand_desc(
+                                ring_b + stage * L::kBTileBytes + j * L::kBSubBytes, p.b_mn_major);
+#pragma unroll
+                            for (int k = 0; k < kBK / 16; ++k) {
+                                umma_f16(d_tmem, a_desc + a_step * k, b_desc + b_step * k, p.idesc,
+                                         (kb > k0 || j > 0 || k > 0) ? 1u : 0u);
+                            }
                         }
                         if (p.mcast > 1)   // every CTA's copy of A in this slot is consumed
                             umma_commit_mcast(smem_addr(&ctl->empty[stage]),

@@ -30,10 +30,14 @@
 
 namespace gbg {
 
-template <int BN, int STAGES>
+// KS = 64-wide k-blocks per ring slot (2: each operand's two k-blocks in one
+// 3-D copy, as in the one-SM kernel).
+template <int BN, int STAGES, int KS = 1>
 struct SmemLayout2 {
-    static constexpr int kBTileBytes = (BN / 2) * kBK * 2;   // this CTA's half of B
-    static constexpr int kStageBytes = kATileBytes + kBTileBytes;
+    static constexpr int kBSubBytes = (BN / 2) * kBK * 2;    // this CTA's half of B, one k-block
+    static constexpr int kASlotBytes = KS * kATileBytes;
+    static constexpr int kBTileBytes = KS * kBSubBytes;
+    static constexpr int kStageBytes = kASlotBytes + kBTileBytes;
     static constexpr int kRingBytes = STAGES * kStageBytes;
     static constexpr int kStoreBufBytes = 32 * 128;
     static constexpr int kStagingBytes = kEpiWarps * 2 * kStoreBufBytes;
@@ -93,6 +97,16 @@ __device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap
         : "memory");
 }
 
+// 3-D form (operand map viewed as 64 elements x rows x k-blocks).
+__device__ __forceinline__ void tma_load_3d_pair(uint32_t dst, const CUtensorMap* map,
+                                                 uint32_t bar_cluster, int32_t x, int32_t y, int32_t z) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(bar_cluster), "r"(x), "r"(y), "r"(z)
+        : "memory");
+}
+
 // load_operand for the pair kernel (bytes counted on the leader's barrier).
 __device__ __forceinline__ void load_operand_pair(uint32_t dst, const CUtensorMap* map,
                                                   uint32_t bar_cluster, int32_t kb, int32_t row0,
@@ -149,12 +163,13 @@ __device__ __forceinline__ uint32_t ld_dsmem_u32(uint32_t cluster_addr) {
     return v;
 }
 
-template <int BN, int STAGES, int OUT>
+template <int BN, int STAGES, int OUT, int KS = 1>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_tn_pair_kernel(const __grid_constant__ CUtensorMap tmap_a,
                         const __grid_constant__ CUtensorMap tmap_b,
                         const __grid_constant__ CUtensorMap tmap_c, const KParams p) {
-    using L = SmemLayout2<BN, STAGES>;
+    using L = SmemLayout2<BN, STAGES, KS>;
+    static_assert(KS == 1 || KS == 2, "k-blocks per ring slot");
     static_assert((OUT == kOutI32 ? 2 : 1) * SplitRecv<BN>::kBytes <= L::kRingBytes,
                   "split-K receive area (and parked integer sums) must fit in the ring");
     static_assert(BN == 128 || BN == 256, "pair tile width");
@@ -166,7 +181,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t raw_addr = smem_addr(smem_raw);
     uint8_t* smem = smem_raw + ((1024u - (raw_addr & 1023u)) & 1023u);
     const uint32_t ring = smem_addr(smem);
-    const uint32_t ring_b = ring + STAGES * kATileBytes;
+    const uint32_t ring_b = ring + STAGES * L::kASlotBytes;
     const uint32_t staging = ring + L::kRingBytes;
     SharedCtl<STAGES>* ctl =
         reinterpret_cast<SharedCtl<STAGES>*>(smem + L::kRingBytes + L::kStagingBytes);
@@ -221,13 +236,18 @@ __global__ void __launch_bounds__(kThreads, 1)
     const UnitCoord c_first = unit_coord_fast(pair, p);
     if (warp == 0 && lane == 0 && pair < p.num_units) {
         const UnitCoord c = c_first;
-        const int32_t ahead = STAGES > p.l2_prefetch ? STAGES : p.l2_prefetch;
+        const int32_t ahead = STAGES * KS > p.l2_prefetch ? STAGES * KS : p.l2_prefetch;
         const int32_t kb_end = c.kb_begin + ahead < c.kb_end ? c.kb_begin + ahead : c.kb_end;
-        for (int32_t kb = c.kb_begin; kb < kb_end; ++kb) {
-            prefetch_operand(&tmap_a, kb, c.m_blk * 2 * kBM + static_cast<int32_t>(rank) * kBM, kBM,
-                             p.a_mn_major);
-            prefetch_operand(&tmap_b, kb, c.n_blk * BN + static_cast<int32_t>(rank) * (BN / 2),
-                             BN / 2, p.b_mn_major);
+        const int32_t a_row = c.m_blk * 2 * kBM + static_cast<int32_t>(rank) * kBM;
+        const int32_t b_row = c.n_blk * BN + static_cast<int32_t>(rank) * (BN / 2);
+        for (int32_t kb = c.kb_begin; kb < kb_end; kb += KS) {
+            if constexpr (KS == 2) {
+                tma_prefetch_l2_3d(&tmap_a, 0, a_row, kb);
+                tma_prefetch_l2_3d(&tmap_b, 0, b_row, kb);
+            } else {
+                prefetch_operand(&tmap_a, kb, a_row, kBM, p.a_mn_major);
+                prefetch_operand(&tmap_b, kb, b_row, BN / 2, p.b_mn_major);
+            }
         }
     }
     grid_dependency_wait();
@@ -244,7 +264,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const UnitCoord c = u == pair ? c_first : unit_coord_fast(u, p);
                 const int32_t a_row = c.m_blk * 2 * kBM + static_cast<int32_t>(rank) * kBM;
                 const int32_t b_row = c.n_blk * BN + static_cast<int32_t>(rank) * (BN / 2);
-                for (int32_t kb = c.kb_begin; kb < c.kb_end; ++kb) {
+                for (int32_t kb = c.kb_begin; kb < c.kb_end; kb += KS) {
                     // (the first pass over the ring finds every slot free)
                     if (issued >= STAGES &&
                         !wait_phase(smem_addr(&ctl->empty[stage]), phase ^ 1u, watch,
@@ -255,13 +275,25 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const uint32_t full_local = smem_addr(&ctl->full[stage]);
                     if (leader) mbar_arrive_expect_tx(full_local, kPairTx + p.tx_extra);
                     const uint32_t full_lead = map_to_rank(full_local, lead);
-                    load_operand_pair(ring + stage * kATileBytes, &tmap_a, full_lead, kb, a_row, kBM,
-                                      p.a_mn_major);
-                    load_operand_pair(ring_b + stage * L::kBTileBytes, &tmap_b, full_lead, kb, b_row,
-                                      BN / 2, p.b_mn_major);
-                    if (p.l2_prefetch > 0 && kb + p.l2_prefetch < c.kb_end) {
-                        prefetch_operand(&tmap_a, kb + p.l2_prefetch, a_row, kBM, p.a_mn_major);
-                        prefetch_operand(&tmap_b, kb + p.l2_prefetch, b_row, BN / 2, p.b_mn_major);
+                    if constexpr (KS == 2) {
+                        // both k-blocks of each operand in one copy (full box always)
+                        tma_load_3d_pair(ring + stage * L::kASlotBytes, &tmap_a, full_lead, 0, a_row, kb);
+                        tma_load_3d_pair(ring_b + stage * L::kBTileBytes, &tmap_b, full_lead, 0, b_row,
+                                         kb);
+                        if (p.l2_prefetch > 0 && kb + p.l2_prefetch < c.kb_end) {
+                            tma_prefetch_l2_3d(&tmap_a, 0, a_row, kb + p.l2_prefetch);
+                            tma_prefetch_l2_3d(&tmap_b, 0, b_row, kb + p.l2_prefetch);
+                        }
+                    } else {
+                        load_operand_pair(ring + stage * kATileBytes, &tmap_a, full_lead, kb, a_row,
+                                          kBM, p.a_mn_major);
+                        load_operand_pair(ring_b + stage * L::kBTileBytes, &tmap_b, full_lead, kb,
+                                          b_row, BN / 2, p.b_mn_major);
+                        if (p.l2_prefetch > 0 && kb + p.l2_prefetch < c.kb_end) {
+                            prefetch_operand(&tmap_a, kb + p.l2_prefetch, a_row, kBM, p.a_mn_major);
+                            prefetch_operand(&tmap_b, kb + p.l2_prefetch, b_row, BN / 2,
+                                             p.b_mn_major);
+                        }
                     }
                     ++issued;
                     if (++stage == STAGES) {
@@ -311,21 +343,28 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                     tc_fence_after();
                     const uint32_t d_tmem = tmem_base + buf * BN;
-                    for (int32_t kb = k0; kb < k1; ++kb) {
+                    // (a slot never straddles chunks: chunk_kb is a multiple of KS)
+                    for (int32_t kb = k0; kb < k1; kb += KS) {
+                        const int32_t nsub = k1 - kb < KS ? k1 - kb : KS;
                         if (!wait_phase(smem_addr(&ctl->full[stage]), phase, watch, kSiteMmaFull)) {
                             ok = false;
                             break;
                         }
                         tc_fence_after();
-                        const uint64_t a_desc = operand_desc(ring + stage * kATileBytes, p.a_mn_major);
-                        const uint64_t b_desc =
-                            operand_desc(ring_b + stage * L::kBTileBytes, p.b_mn_major);
                         const uint32_t a_step = desc_k_step(p.a_mn_major);
                         const uint32_t b_step = desc_k_step(p.b_mn_major);
 #pragma unroll
-                        for (int k = 0; k < kBK / 16; ++k)
-                            umma_f16_pair(d_tmem, a_desc + a_step * k, b_desc + b_step * k, p.idesc,
-                                          (kb > k0 || k > 0) ? 1u : 0u);
+                        for (int32_t j = 0; j < KS; ++j) {
+                            if (j >= nsub) break;   // the slot's second k-block lies past the slice
+                            const uint64_t a_desc = operand_desc(
+                                ring + stage * L::kASlotBytes + j * kATileBytes, p.a_mn_major);
+                            const uint64_t b_desc = operand_desc(
+                                ring_b + stage * L::kBTileBytes + j * L::kBSubBytes, p.b_mn_major);
+#pragma unroll
+                            for (int k = 0; k < kBK / 16; ++k)
+                                umma_f16_pair(d_tmem, a_desc + a_step * k, b_desc + b_step * k,
+                                              p.idesc, (kb > k0 || j > 0 || k > 0) ? 1u : 0u);
+                        }
                         umma_commit_pair(smem_addr(&ctl->empty[stage]), pair_mask);
                         if (++stage == STAGES) {
                             stage = 0;

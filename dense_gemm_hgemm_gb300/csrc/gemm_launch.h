@@ -10,7 +10,10 @@ namespace gbg {
 
 // Default ring depth per tile width (all near 192 KiB of the 227 KiB a CTA may use).
 constexpr int default_stages(int bn) { return bn == 256 ? 4 : (bn == 128 ? 6 : 8); }
+// Two k-blocks per ring slot (one-SM kernel, BN 64 / 128): the same ~192 KiB ring.
+constexpr int default_stages_ks2(int bn) { return bn == 128 ? 3 : 4; }
 // SM-pair kernel: each CTA holds A 128 x 64 and half of B per stage.
+constexpr int default_pair_stages_ks2(int bn) { return bn == 256 ? 3 : 4; }
 constexpr int default_pair_stages(int bn) { return bn == 256 ? 6 : 8; }
 
 struct LaunchShape {

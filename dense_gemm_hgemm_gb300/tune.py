@@ -69,7 +69,14 @@ def candidates(M, N, K, dtype, sms):
                         and pair_tiles * ps * 2 <= sms and pair_tiles < sms // 2):
                     out.append({"block_n": bn, "split_k": ps, "raster_group": 8,
                                 "split_mode": 1, "cta_pair": 1})
-    return out
+    # the one-SM narrow-tile candidates again with two k-blocks per ring slot
+    two = []
+    if K % 64 == 0:
+        for c in out:
+            if ((c.get("cta_pair") or c["block_n"] <= 128) and not c.get("multicast")
+                    and -(-num_kb // c["split_k"]) >= 2):
+                two.append({**c, "kblocks_per_stage": 2})
+    return out + two
 
 
 def _time(plan, copies, stream, flush, batches=5, reps_warm=20):
@@ -152,9 +159,10 @@ def sweep(out_path, only=None, dtype=None):
                 seq, warm = _time(plan, copies, stream, flush)
             rec["candidates"].append({**cfg, "seq_us": round(seq, 3), "warm_us": round(warm, 3)})
         best = min(rec["candidates"], key=lambda c: (c["seq_us"], c["warm_us"]))
-        rec["best"] = {k: best.get(k, 0) for k in ("block_n", "split_k", "raster_group",
+        rec["best"] = {k: best.get(k, 1 if k == "kblocks_per_stage" else 0)
+                       for k in ("block_n", "split_k", "raster_group",
                                                    "split_mode", "cta_pair", "direct_store",
-                                                   "multicast")}
+                                                   "multicast", "kblocks_per_stage")}
         rec["model"] = g.gemm_select_config(M, N, K, dtype, sms)
         results.append(rec)
         del copies
@@ -179,9 +187,13 @@ def compact(full_json, out_json=TUNED_JSON):
         key = lambda c: (c["seq_us"], c["warm_us"])
         b = min(r["candidates"], key=key)
         plain = [c for c in r["candidates"] if c["split_k"] == 1 and not c.get("cta_pair")
-                 and not c.get("direct_store") and not c.get("multicast")]
+                 and not c.get("direct_store") and not c.get("multicast")
+                 and c.get("kblocks_per_stage", 1) == 1]
+        best = dict(r["best"])
+        if not best.get("kblocks_per_stage"):
+            best["kblocks_per_stage"] = 1
         rows.append({"M": r["M"], "N": r["N"], "K": r["K"], "dtype": r["dtype"],
-                     "best": r["best"], "seq_us": b["seq_us"], "warm_us": b["warm_us"],
+                     "best": best, "seq_us": b["seq_us"], "warm_us": b["warm_us"],
                      "plain_seq_us": min(plain, key=key)["seq_us"] if plain else None,
                      "candidates": len(r["candidates"])})
     with open(out_json, "w") as f:
@@ -202,16 +214,16 @@ def emit(json_path, table_path=TABLE):
         "// Fields: M, N, K, dtype (0 f16, 1 bf16, 2 i8), block_n, split_k, raster_group,",
         "// split_mode (0 workspace, 1 cluster), cta_pair (0 one SM, 1 SM pair),",
         "// direct_store (0 TMA store, 1 per-thread stores), multicast (0 off, 2/4 CTAs",
-        "// sharing each A tile).",
+        "// sharing each A tile), kblocks_per_stage (64-wide k-blocks per ring slot).",
         "static const TableEntry kTunedTable[] = {",
     ]
     n = 0
     for r in doc["shapes"]:
         b = r["best"]
-        lines.append("    {%d, %d, %d, %d, %d, %d, %d, %d, %d, %d, %d}," % (
+        lines.append("    {%d, %d, %d, %d, %d, %d, %d, %d, %d, %d, %d, %d}," % (
             r["M"], r["N"], r["K"], code[r["dtype"]], b["block_n"], b["split_k"],
             b["raster_group"], b.get("split_mode", 0), b.get("cta_pair", 0),
-            b.get("direct_store", 0), b.get("multicast", 0)))
+            b.get("direct_store", 0), b.get("multicast", 0), b.get("kblocks_per_stage", 1)))
         n += 1
     lines.append("};")
     lines.append("static const int kTunedCount = %d;" % n)

@@ -106,6 +106,11 @@ typedef enum {
  *                  adjacent N-tiles of the same rows, each loading 1/multicast
  *                  of the shared A tile and multicasting it to the others
  *                  (one-SM kernel, split_k 1; 4 needs A stored M x K)
+ *   kblocks_per_stage : 0 = the table's choice; 1 or 2 = 64-wide k-blocks per
+ *                  ring slot.  2: one-SM kernel with block_n 64 or 128 or the
+ *                  SM-pair kernel, both operands K-contiguous (layout TN),
+ *                  K % 64 == 0, no multicast; each operand's two k-blocks
+ *                  arrive in one copy
  *   l2_prefetch  : 0 = off; d in 1..64 = while loading k-block kb, also ask L2
  *                  to fetch k-block kb + d of the same tile (hides DRAM latency
  *                  on long K)
@@ -121,6 +126,7 @@ typedef struct {
     int32_t direct_store;
     int32_t multicast;
     int32_t l2_prefetch;
+    int32_t kblocks_per_stage;
 } gemm_config_t;
 
 typedef struct gemm_plan *gemm_plan_t;

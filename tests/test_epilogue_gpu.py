@@ -27,6 +27,7 @@ MODES = [
     ("multicast4", (200, 520, 640), {"block_n": 128, "multicast": 4}),
     ("pair_split", (300, 264, 1024), {"block_n": 256, "cta_pair": 1, "split_k": 4,
                                       "split_mode": 1}),
+    ("two_kblock_slots", (300, 264, 1088), {"block_n": 128, "kblocks_per_stage": 2}),
 ]
 
 

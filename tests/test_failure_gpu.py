@@ -24,6 +24,9 @@ CONFIGS = [
     ("sm_pair_split", (512, 512, 1024), {"block_n": 256, "cta_pair": 1, "split_k": 4,
                                          "split_mode": 1}),
     ("multicast", (256, 512, 512), {"block_n": 64, "multicast": 4}),
+    ("two_kblock_slots", (256, 512, 1024), {"block_n": 64, "kblocks_per_stage": 2}),
+    ("sm_pair_two_kblock_slots", (512, 512, 1024), {"block_n": 256, "cta_pair": 1,
+                                                    "kblocks_per_stage": 2}),
 ]
 
 
