@@ -600,21 +600,36 @@ __device__ __forceinline__ uint4 ld_shared_u4(uint32_t saddr) {
     return v;
 }
 
-// Store 32 partial values of block row `row`, columns [col, col+32), of K-slice
-// `slice` into the receive area of the row's owner.
+// Store 32 partial values (columns [col, col+32)) of each of a warp's 32
+// consecutive block rows (warp_row0 + lane holds its row in v) of K-slice `slice`
+// into the receive areas of the rows' owners.  The values pass through the
+// warp's staging buffer (36-word row stride: both passes are free of bank
+// conflicts) so that each remote store instruction writes 4 rows x 128
+// contiguous bytes instead of 32 scattered 16-byte pieces.
 template <int BN>
-__device__ __forceinline__ void push_row32(uint32_t recv, int S, int slice, int row, int col,
-                                           const uint32_t* v, uint32_t rank_stride,
-                                           uint32_t rank_offset) {
-    const int rows = kBM / S;
-    const int owner = row / rows;
-    const int lr = row - owner * rows;
-    const uint32_t local =
-        recv + static_cast<uint32_t>(((slice * rows + lr) * SplitRecv<BN>::kRowWords + col) * 4);
-    const uint32_t dst = map_to_rank(local, static_cast<uint32_t>(owner) * rank_stride + rank_offset);
+__device__ __forceinline__ void push_warp_rows32(uint32_t recv, uint32_t stg, int log2_rows,
+                                                 int slice, int warp_row0, int lane, int col,
+                                                 const uint32_t* v, uint32_t rank_stride,
+                                                 uint32_t rank_offset) {
 #pragma unroll
     for (int g = 0; g < 8; ++g)
-        st_dsmem_u4(dst + g * 16, make_uint4(v[g * 4 + 0], v[g * 4 + 1], v[g * 4 + 2], v[g * 4 + 3]));
+        st_shared_u4(stg + static_cast<uint32_t>((lane * 36 + 4 * g) * 4),
+                     make_uint4(v[g * 4 + 0], v[g * 4 + 1], v[g * 4 + 2], v[g * 4 + 3]));
+    __syncwarp();
+    const int ch = lane & 7;
+#pragma unroll
+    for (int s = 0; s < 8; ++s) {
+        const int r = 4 * s + (lane >> 3);
+        const uint4 q = ld_shared_u4(stg + static_cast<uint32_t>((r * 36 + 4 * ch) * 4));
+        const int row = warp_row0 + r;
+        const int owner = row >> log2_rows;
+        const int lr = row - (owner << log2_rows);
+        const uint32_t local =
+            recv + static_cast<uint32_t>((((slice << log2_rows) + lr) * SplitRecv<BN>::kRowWords +
+                                          col + 4 * ch) * 4);
+        st_dsmem_u4(map_to_rank(local, static_cast<uint32_t>(owner) * rank_stride + rank_offset), q);
+    }
+    __syncwarp();   // the staging buffer is rewritten by the next call
 }
 
 // The owner's half: sum its S slots in slice order, apply the epilogue, store
@@ -627,32 +642,46 @@ __device__ __forceinline__ void cluster_sum_store(const KParams& p, int32_t bloc
     const int S = p.split_k;
     const int rows = kBM / S;
     constexpr int kVec = BN / 4;
-    for (int t = tid; t < rows * kVec; t += nthreads) {
-        const int lr = t / kVec;
-        const int c4 = (t % kVec) * 4;
-        const int32_t grow = block_row + part * rows + lr;
-        const int32_t gcol = col_base + c4;
-        if (grow >= p.M || gcol >= p.N) continue;
-        const uint32_t off = recv + static_cast<uint32_t>((lr * SplitRecv<BN>::kRowWords + c4) * 4);
-        const uint32_t slot = static_cast<uint32_t>(rows * SplitRecv<BN>::kRowWords * 4);
-        uint4 q[8];
+    constexpr int kU = 4;   // groups in flight per thread (their loads issued together)
+    const int total = rows * kVec;
+    const uint32_t slot = static_cast<uint32_t>(rows * SplitRecv<BN>::kRowWords * 4);
+    for (int t0 = tid; t0 < total; t0 += kU * nthreads) {
+        uint4 q[kU][8];
 #pragma unroll
-        for (int s = 0; s < 8; ++s)
-            if (s < S) q[s] = ld_shared_u4(off + static_cast<uint32_t>(s) * slot);
-        uint32_t v[4] = {0u, 0u, 0u, 0u};
+        for (int u = 0; u < kU; ++u) {
+            const int t = t0 + u * nthreads;
+            if (t >= total) break;
+            const int lr = t / kVec;
+            const int c4 = (t % kVec) * 4;
+            const uint32_t off = recv + static_cast<uint32_t>((lr * SplitRecv<BN>::kRowWords + c4) * 4);
 #pragma unroll
-        for (int s = 0; s < 8; ++s)
-            if (s < S) add_u4<OUT>(v, q[s]);
-        const int64_t idx = static_cast<int64_t>(grow) * p.N + gcol;
-        if constexpr (OUT != kOutI32) apply_bias_act<1>(v, p, gcol);
-        if constexpr (OUT == kOutI32) {
-            *reinterpret_cast<uint4*>(reinterpret_cast<uint32_t*>(p.C) + idx) =
-                make_uint4(v[0], v[1], v[2], v[3]);
-        } else {
-            uint2 h;
-            h.x = pack2<OUT>(__uint_as_float(v[0]), __uint_as_float(v[1]));
-            h.y = pack2<OUT>(__uint_as_float(v[2]), __uint_as_float(v[3]));
-            *reinterpret_cast<uint2*>(reinterpret_cast<uint16_t*>(p.C) + idx) = h;
+            for (int s = 0; s < 8; ++s)
+                if (s < S) q[u][s] = ld_shared_u4(off + static_cast<uint32_t>(s) * slot);
+        }
+#pragma unroll
+        for (int u = 0; u < kU; ++u) {
+            const int t = t0 + u * nthreads;
+            if (t >= total) break;
+            const int lr = t / kVec;
+            const int c4 = (t % kVec) * 4;
+            const int32_t grow = block_row + part * rows + lr;
+            const int32_t gcol = col_base + c4;
+            if (grow >= p.M || gcol >= p.N) continue;
+            uint32_t v[4] = {0u, 0u, 0u, 0u};
+#pragma unroll
+            for (int s = 0; s < 8; ++s)
+                if (s < S) add_u4<OUT>(v, q[u][s]);
+            const int64_t idx = static_cast<int64_t>(grow) * p.N + gcol;
+            if constexpr (OUT != kOutI32) apply_bias_act<1>(v, p, gcol);
+            if constexpr (OUT == kOutI32) {
+                *reinterpret_cast<uint4*>(reinterpret_cast<uint32_t*>(p.C) + idx) =
+                    make_uint4(v[0], v[1], v[2], v[3]);
+            } else {
+                uint2 h;
+                h.x = pack2<OUT>(__uint_as_float(v[0]), __uint_as_float(v[1]));
+                h.y = pack2<OUT>(__uint_as_float(v[2]), __uint_as_float(v[3]));
+                *reinterpret_cast<uint2*>(reinterpret_cast<uint16_t*>(p.C) + idx) = h;
+            }
         }
     }
 }
@@ -1148,6 +1177,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (warp >= 2 && epi_ok) {
             const int quad = warp & 3;
             const int row = quad * 32 + lane;
+            // this warp's (idle) TMA-store buffers serve as its transpose staging
+            const uint32_t stg = staging + static_cast<uint32_t>((warp - 2) * 2 * L::kStoreBufBytes);
+            const int log2_rows = 7 - (31 - __clz(p.split_k));   // rows per owner = 128 / S
 #pragma unroll 1
             for (int j = 0; j < BN / 32; ++j) {
                 uint32_t v[32];
@@ -1166,7 +1198,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     tmem_ld_32x32b_x32(tmem_base + (static_cast<uint32_t>(quad * 32) << 16) + j * 32, v);
                     tmem_ld_wait();
                 }
-                push_row32<BN>(ring, p.split_k, c.split, row, j * 32, v, 1u, 0u);
+                push_warp_rows32<BN>(ring, stg, log2_rows, c.split, quad * 32, lane, j * 32, v, 1u,
+                                     0u);
             }
         }
         cluster_sync_all();         // every slice has arrived at its owner

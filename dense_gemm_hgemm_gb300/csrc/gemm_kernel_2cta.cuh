@@ -509,6 +509,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             // rows of this CTA's half go to the CTAs (s', same half) of the cluster
             const int quad = warp & 3;
             const int row = quad * 32 + lane;
+            // this warp's (idle) TMA-store buffers serve as its transpose staging
+            const uint32_t stg = staging + static_cast<uint32_t>((warp - 2) * 2 * L::kStoreBufBytes);
+            const int log2_rows = 7 - (31 - __clz(p.split_k));   // rows per owner = 128 / S
 #pragma unroll 1
             for (int j = 0; j < BN / 32; ++j) {
                 uint32_t v[32];
@@ -527,7 +530,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     tmem_ld_32x32b_x32(tmem_base + (static_cast<uint32_t>(quad * 32) << 16) + j * 32, v);
                     tmem_ld_wait();
                 }
-                push_row32<BN>(ring, p.split_k, c.split, row, j * 32, v, 2u, rank);
+                push_warp_rows32<BN>(ring, stg, log2_rows, c.split, quad * 32, lane, j * 32, v, 2u,
+                                     rank);
             }
         }
         cluster_sync_all();         // every slice has arrived at its owner
