@@ -100,8 +100,7 @@ gemm_status_t normalise_config(int64_t M, int64_t N, int64_t K, gemm_dtype_t dty
     if (c.l2_prefetch < 0 || c.l2_prefetch > 64) return GEMM_ERR_INVALID_ARG;
     if (c.kblocks_per_stage == 0) c.kblocks_per_stage = 1;
     if (c.kblocks_per_stage != 1 && c.kblocks_per_stage != 2) return GEMM_ERR_INVALID_ARG;
-    if (c.kblocks_per_stage == 2 &&
-        ((!c.cta_pair && c.block_n > 128) || c.multicast > 1 || K % gbg::kBK != 0))
+    if (c.kblocks_per_stage == 2 && ((!c.cta_pair && c.block_n > 128) || c.multicast > 1))
         return GEMM_ERR_INVALID_ARG;
     if (c.cta_pair) {
         // SM pair: 256-row tiles; K is sliced only across the pairs of a cluster.
@@ -218,12 +217,13 @@ gemm_status_t encode_output(CUtensorMap* map, void* base, int64_t M, int64_t N, 
 // (128 bytes) x 64 K-rows with 128-byte swizzle, the M/N-major tile blocks the
 // kernels' descriptors expect.
 gemm_status_t encode_mnmajor(CUtensorMap* map, const void* base, int64_t rows, int64_t K,
-                             CUtensorMapDataType dt) {
+                             CUtensorMapDataType dt, int kblocks = 1) {
     PFN_cuTensorMapEncodeTiled_v12000 fn = encode_fn();
     if (!fn) return GEMM_ERR_TENSORMAP;
     const cuuint64_t dims[2] = {static_cast<cuuint64_t>(rows), static_cast<cuuint64_t>(K)};
     const cuuint64_t strides[1] = {static_cast<cuuint64_t>(rows) * 2};
-    const cuuint32_t box[2] = {64, static_cast<cuuint32_t>(gbg::kBK)};
+    // kblocks consecutive 64-row K blocks per box (two-k-block ring slots)
+    const cuuint32_t box[2] = {64, static_cast<cuuint32_t>(gbg::kBK * kblocks)};
     const cuuint32_t estr[2] = {1, 1};
     const CUresult r = fn(map, dt, 2, const_cast<void*>(base), dims, strides, box, estr,
                           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -252,13 +252,14 @@ gemm_status_t encode_kmajor3d(CUtensorMap* map, const void* base, int64_t rows, 
 }
 
 // Map for operand A (rows = M) or B (rows = N) in the plan's storage; kblocks = 2
-// selects the 3-D two-k-block view (K-contiguous operands only).
+// selects the two-k-block boxes (3-D view of a K-contiguous operand, or 128-row
+// boxes of an M/N-contiguous one).
 gemm_status_t encode_operand_map(CUtensorMap* map, const void* base, int64_t rows, int64_t K,
                                  int box_rows, bool mn_major, CUtensorMapDataType dt,
                                  int kblocks = 1) {
+    if (mn_major) return encode_mnmajor(map, base, rows, K, dt, kblocks);
     if (kblocks > 1) return encode_kmajor3d(map, base, rows, K, box_rows, kblocks, dt);
-    return mn_major ? encode_mnmajor(map, base, rows, K, dt)
-                    : encode_kmajor(map, base, rows, K, box_rows, dt);
+    return encode_kmajor(map, base, rows, K, box_rows, dt);
 }
 
 CUtensorMapDataType operand_type(gemm_dtype_t dt) {
@@ -292,8 +293,10 @@ gemm_status_t create_plan(int64_t M, int64_t N, int64_t K, gemm_dtype_t dtype,
     if (st != GEMM_OK) return st;
     // A stored K x M is copied in 64-column blocks: at most two multicast slices
     if (user_cfg && user_cfg->multicast > 2 && a_mn_major(layout)) return GEMM_ERR_INVALID_ARG;
-    // two k-blocks per slot come as 3-D copies of K-contiguous operands only
-    if (user_cfg && user_cfg->kblocks_per_stage == 2 && layout != GEMM_LAYOUT_TN)
+    // two k-blocks per slot of a K-contiguous operand come from its 3-D view,
+    // which needs K % 64 == 0
+    const bool some_k_major = !a_mn_major(layout) || !b_mn_major(layout);
+    if (user_cfg && user_cfg->kblocks_per_stage == 2 && some_k_major && K % gbg::kBK != 0)
         return GEMM_ERR_INVALID_ARG;
     if (user_cfg) {
         gemm_config_t tmp;
@@ -307,7 +310,7 @@ gemm_status_t create_plan(int64_t M, int64_t N, int64_t K, gemm_dtype_t dtype,
 
     gemm_config_t want = user_cfg ? *user_cfg : gbg::select_config(M, N, K, dtype, sms);
     if (want.multicast > 2 && a_mn_major(layout)) want.multicast = 2;
-    if (want.kblocks_per_stage == 2 && (layout != GEMM_LAYOUT_TN || K % gbg::kBK != 0)) {
+    if (want.kblocks_per_stage == 2 && some_k_major && K % gbg::kBK != 0) {
         want.kblocks_per_stage = 1;
         want.stages = 0;
     }

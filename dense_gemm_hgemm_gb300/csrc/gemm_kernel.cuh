@@ -313,18 +313,26 @@ __device__ __forceinline__ uint64_t sw128_kmajor_desc(uint32_t saddr) {
 }
 
 // Shared-memory descriptor for an MN-major operand tile written by TMA as
-// 64-element (128-byte) wide blocks of 64 K-rows (8 KiB each, 128-byte swizzle):
-// 8-row K groups 1024 bytes apart (stride byte offset), 64-element MN blocks
-// 8 KiB apart (leading byte offset).
+// 64-element (128-byte) wide blocks of KS*64 K-rows (KS*8 KiB each, 128-byte
+// swizzle): 8-row K groups 1024 bytes apart (stride byte offset), 64-element MN
+// blocks KS*8 KiB apart (leading byte offset).
+template <int KS = 1>
 __device__ __forceinline__ uint64_t sw128_mnmajor_desc(uint32_t saddr) {
     return static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4)
-           | (static_cast<uint64_t>(8192 >> 4) << 16)       // leading byte offset: next 64 MN
-           | (static_cast<uint64_t>(1024 >> 4) << 32)       // stride byte offset: next 8 K rows
+           | (static_cast<uint64_t>((KS * 8192) >> 4) << 16)  // leading byte offset: next 64 MN
+           | (static_cast<uint64_t>(1024 >> 4) << 32)         // stride byte offset: next 8 K rows
            | (static_cast<uint64_t>(1) << 46)
            | (static_cast<uint64_t>(2) << 61);
 }
+template <int KS = 1>
 __device__ __forceinline__ uint64_t operand_desc(uint32_t saddr, int32_t mn_major) {
-    return mn_major ? sw128_mnmajor_desc(saddr) : sw128_kmajor_desc(saddr);
+    return mn_major ? sw128_mnmajor_desc<KS>(saddr) : sw128_kmajor_desc(saddr);
+}
+// Offset of k-block j of a slot within an operand's part of the slot: K-major
+// parts hold KS whole rows x 64 tiles (tile_bytes each); MN-major parts hold
+// 64-element blocks of KS*64 K-rows, where k-block j starts 64 K-rows (8 KiB) in.
+__device__ __forceinline__ uint32_t kblock_offset(int32_t mn_major, uint32_t tile_bytes, int j) {
+    return static_cast<uint32_t>(j) * (mn_major ? 8192u : tile_bytes);
 }
 // Descriptor advance per K=16 MMA: 32 bytes along a K-major row, or 16 rows of
 // 128 bytes of an MN-major tile (start address is encoded >> 4).
@@ -346,6 +354,28 @@ __device__ __forceinline__ void prefetch_operand(const CUtensorMap* map, int32_t
                                                  int32_t rows, int32_t mn_major) {
     if (!mn_major) {
         tma_prefetch_l2_2d(map, kb * kBK, row0);
+        return;
+    }
+    for (int32_t i = 0; i < rows / 64; ++i) tma_prefetch_l2_2d(map, row0 + i * 64, kb * kBK);
+}
+
+// Both k-blocks kb, kb+1 of an operand tile for a two-k-block slot: K-major =
+// one 3-D box {64, rows, 2} of the (64, rows, K/64) view; MN-major = rows/64 boxes
+// {64 MN, 128 K} (the map's box is 128 K-rows high), 16 KiB apart.
+__device__ __forceinline__ void load_operand_2kb(uint32_t dst, const CUtensorMap* map, uint32_t bar,
+                                                 int32_t kb, int32_t row0, int32_t rows,
+                                                 int32_t mn_major) {
+    if (!mn_major) {
+        tma_load_3d(dst, map, bar, 0, row0, kb);
+        return;
+    }
+    for (int32_t i = 0; i < rows / 64; ++i)
+        tma_load_2d(dst + static_cast<uint32_t>(i) * 16384u, map, bar, row0 + i * 64, kb * kBK);
+}
+__device__ __forceinline__ void prefetch_operand_2kb(const CUtensorMap* map, int32_t kb, int32_t row0,
+                                                     int32_t rows, int32_t mn_major) {
+    if (!mn_major) {
+        tma_prefetch_l2_3d(map, 0, row0, kb);
         return;
     }
     for (int32_t i = 0; i < rows / 64; ++i) tma_prefetch_l2_2d(map, row0 + i * 64, kb * kBK);
@@ -809,8 +839,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             c.m_blk * kBM + static_cast<int32_t>(blockIdx.x & ((1u << p.mcast_shift) - 1u)) * a_rows;
         for (int32_t kb = c.kb_begin; kb < kb_end; kb += KS) {
             if constexpr (KS == 2) {
-                tma_prefetch_l2_3d(&tmap_a, 0, a_row0, kb);
-                tma_prefetch_l2_3d(&tmap_b, 0, c.n_blk * BN, kb);
+                prefetch_operand_2kb(&tmap_a, kb, a_row0, a_rows, p.a_mn_major);
+                prefetch_operand_2kb(&tmap_b, kb, c.n_blk * BN, BN, p.b_mn_major);
             } else {
                 prefetch_operand(&tmap_a, kb, a_row0, a_rows, p.a_mn_major);
                 prefetch_operand(&tmap_b, kb, c.n_blk * BN, BN, p.b_mn_major);
@@ -845,11 +875,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                         // both k-blocks of each operand in one copy; a copy past the
                         // end of K is zero-filled and past the slice end is unused,
                         // but always delivers the full box
-                        tma_load_3d(ring + stage * L::kASlotBytes, &tmap_a, full, 0, c.m_blk * kBM, kb);
-                        tma_load_3d(ring_b + stage * L::kBTileBytes, &tmap_b, full, 0, c.n_blk * BN, kb);
+                        load_operand_2kb(ring + stage * L::kASlotBytes, &tmap_a, full, kb,
+                                         c.m_blk * kBM, kBM, p.a_mn_major);
+                        load_operand_2kb(ring_b + stage * L::kBTileBytes, &tmap_b, full, kb,
+                                         c.n_blk * BN, BN, p.b_mn_major);
                         if (p.l2_prefetch > 0 && kb + p.l2_prefetch < c.kb_end) {
-                            tma_prefetch_l2_3d(&tmap_a, 0, c.m_blk * kBM, kb + p.l2_prefetch);
-                            tma_prefetch_l2_3d(&tmap_b, 0, c.n_blk * BN, kb + p.l2_prefetch);
+                            prefetch_operand_2kb(&tmap_a, kb + p.l2_prefetch, c.m_blk * kBM, kBM,
+                                                 p.a_mn_major);
+                            prefetch_operand_2kb(&tmap_b, kb + p.l2_prefetch, c.n_blk * BN, BN,
+                                                 p.b_mn_major);
                         }
                     } else {
                         if (p.mcast > 1) {
@@ -948,10 +982,13 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                         for (int32_t j = 0; j < KS; ++j) {
                             if (j >= nsub) break;   // the slot's second k-block lies past the slice
-                            const uint64_t a_desc = operand_desc(
-                                ring + stage * L::kASlotBytes + j * kATileBytes, p.a_mn_major);
-                            const uint64_t b_desc = operand_desc(
-                                ring_b + stage * L::kBTileBytes + j * L::kBSubBytes, p.b_mn_major);
+                            const uint64_t a_desc = operand_desc<KS>(
+                                ring + stage * L::kASlotBytes + kblock_offset(p.a_mn_major, kATileBytes, j),
+                                p.a_mn_major);
+                            const uint64_t b_desc = operand_desc<KS>(
+                                ring_b + stage * L::kBTileBytes +
+                                    kblock_offset(p.b_mn_major, L::kBSubBytes, j),
+                                p.b_mn_major);
 #pragma unroll
                             for (int k = 0; k < kBK / 16; ++k) {
                                 umma_f16(d_tmem, a_desc + a_step * k, b_desc + b_step * k, p.idesc,

@@ -107,6 +107,19 @@ __device__ __forceinline__ void tma_load_3d_pair(uint32_t dst, const CUtensorMap
         : "memory");
 }
 
+// load_operand_2kb for the pair kernel (bytes counted on the leader's barrier).
+__device__ __forceinline__ void load_operand_2kb_pair(uint32_t dst, const CUtensorMap* map,
+                                                      uint32_t bar_cluster, int32_t kb, int32_t row0,
+                                                      int32_t rows, int32_t mn_major) {
+    if (!mn_major) {
+        tma_load_3d_pair(dst, map, bar_cluster, 0, row0, kb);
+        return;
+    }
+    for (int32_t i = 0; i < rows / 64; ++i)
+        tma_load_2d_pair(dst + static_cast<uint32_t>(i) * 16384u, map, bar_cluster, row0 + i * 64,
+                         kb * kBK);
+}
+
 // load_operand for the pair kernel (bytes counted on the leader's barrier).
 __device__ __forceinline__ void load_operand_pair(uint32_t dst, const CUtensorMap* map,
                                                   uint32_t bar_cluster, int32_t kb, int32_t row0,
@@ -242,8 +255,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int32_t b_row = c.n_blk * BN + static_cast<int32_t>(rank) * (BN / 2);
         for (int32_t kb = c.kb_begin; kb < kb_end; kb += KS) {
             if constexpr (KS == 2) {
-                tma_prefetch_l2_3d(&tmap_a, 0, a_row, kb);
-                tma_prefetch_l2_3d(&tmap_b, 0, b_row, kb);
+                prefetch_operand_2kb(&tmap_a, kb, a_row, kBM, p.a_mn_major);
+                prefetch_operand_2kb(&tmap_b, kb, b_row, BN / 2, p.b_mn_major);
             } else {
                 prefetch_operand(&tmap_a, kb, a_row, kBM, p.a_mn_major);
                 prefetch_operand(&tmap_b, kb, b_row, BN / 2, p.b_mn_major);
@@ -277,12 +290,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const uint32_t full_lead = map_to_rank(full_local, lead);
                     if constexpr (KS == 2) {
                         // both k-blocks of each operand in one copy (full box always)
-                        tma_load_3d_pair(ring + stage * L::kASlotBytes, &tmap_a, full_lead, 0, a_row, kb);
-                        tma_load_3d_pair(ring_b + stage * L::kBTileBytes, &tmap_b, full_lead, 0, b_row,
-                                         kb);
+                        load_operand_2kb_pair(ring + stage * L::kASlotBytes, &tmap_a, full_lead, kb,
+                                              a_row, kBM, p.a_mn_major);
+                        load_operand_2kb_pair(ring_b + stage * L::kBTileBytes, &tmap_b, full_lead, kb,
+                                              b_row, BN / 2, p.b_mn_major);
                         if (p.l2_prefetch > 0 && kb + p.l2_prefetch < c.kb_end) {
-                            tma_prefetch_l2_3d(&tmap_a, 0, a_row, kb + p.l2_prefetch);
-                            tma_prefetch_l2_3d(&tmap_b, 0, b_row, kb + p.l2_prefetch);
+                            prefetch_operand_2kb(&tmap_a, kb + p.l2_prefetch, a_row, kBM, p.a_mn_major);
+                            prefetch_operand_2kb(&tmap_b, kb + p.l2_prefetch, b_row, BN / 2,
+                                                 p.b_mn_major);
                         }
                     } else {
                         load_operand_pair(ring + stage * kATileBytes, &tmap_a, full_lead, kb, a_row,
@@ -356,10 +371,13 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                         for (int32_t j = 0; j < KS; ++j) {
                             if (j >= nsub) break;   // the slot's second k-block lies past the slice
-                            const uint64_t a_desc = operand_desc(
-                                ring + stage * L::kASlotBytes + j * kATileBytes, p.a_mn_major);
-                            const uint64_t b_desc = operand_desc(
-                                ring_b + stage * L::kBTileBytes + j * L::kBSubBytes, p.b_mn_major);
+                            const uint64_t a_desc = operand_desc<KS>(
+                                ring + stage * L::kASlotBytes + kblock_offset(p.a_mn_major, kATileBytes, j),
+                                p.a_mn_major);
+                            const uint64_t b_desc = operand_desc<KS>(
+                                ring_b + stage * L::kBTileBytes +
+                                    kblock_offset(p.b_mn_major, L::kBSubBytes, j),
+                                p.b_mn_major);
 #pragma unroll
                             for (int k = 0; k < kBK / 16; ++k)
                                 umma_f16_pair(d_tmem, a_desc + a_step * k, b_desc + b_step * k,

@@ -108,9 +108,9 @@ typedef enum {
  *                  (one-SM kernel, split_k 1; 4 needs A stored M x K)
  *   kblocks_per_stage : 0 = the table's choice; 1 or 2 = 64-wide k-blocks per
  *                  ring slot.  2: one-SM kernel with block_n 64 or 128 or the
- *                  SM-pair kernel, both operands K-contiguous (layout TN),
- *                  K % 64 == 0, no multicast; each operand's two k-blocks
- *                  arrive in one copy
+ *                  SM-pair kernel, no multicast, and K % 64 == 0 when an
+ *                  operand is K-contiguous; each operand's two k-blocks arrive
+ *                  in one copy per 64-element block
  *   l2_prefetch  : 0 = off; d in 1..64 = while loading k-block kb, also ask L2
  *                  to fetch k-block kb + d of the same tile (hides DRAM latency
  *                  on long K)

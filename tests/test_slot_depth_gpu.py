@@ -1,6 +1,6 @@
 """Two 64-wide k-blocks per ring slot (kblocks_per_stage = 2: one-SM kernel,
 block_n 64 / 128, each operand's two k-blocks brought by one 3-D copy) against
-the oracle: odd k-block counts (the last slot's second k-block is past K and
+the oracle (every operand storage): odd k-block counts (the last slot's second k-block is past K and
 zero-filled), split-K slices of odd length (the second k-block belongs to the
 next slice and is skipped), integer mode (bit-exact), the direct-store and fused
 epilogues, the bounded-wait failure path, and the configurations it refuses."""
@@ -66,7 +66,7 @@ def test_two_kblock_slots_refused_where_it_does_not_apply(gemm_lib):
     for shape, layout, bad in (((256, 256, 1024), "TN", {"block_n": 256, **KS2}),
                                ((256, 256, 1024), "TN", {"block_n": 64, "multicast": 2, **KS2}),
                                ((256, 256, 1000), "TN", {"block_n": 64, **KS2}),       # K % 64
-                               ((256, 256, 1024), "NN", {"block_n": 64, **KS2}),       # layout
+                               ((256, 256, 1000), "TT", {"block_n": 64, **KS2}),       # B K-major
                                ((256, 256, 1024), "TN", {"block_n": 64, "kblocks_per_stage": 3}),
                                ((256, 256, 1024), "TN", {"block_n": 64, "stages": 8, **KS2})):
         with pytest.raises(g.GemmError):
@@ -114,3 +114,29 @@ def test_two_kblock_slots_sm_pair_int8():
         A, B = inputs.make_operands(M, N, K, "i8")
         C = pu.run_gpu(A, B, "i8", {"block_n": 128, "cta_pair": 1, **KS2})
         pu.check_full(A, B, "i8", C, "i8 pair ks2 %s" % ((M, N, K),))
+
+
+@pytest.mark.parametrize("layout", ["NN", "TT", "NT"])
+def test_two_kblock_slots_layouts(layout):
+    """M/N-contiguous operands: two k-blocks per 128-K-row box (K need not be a
+    multiple of 64 when both operands are M/N-contiguous)."""
+    shapes = [(136, 72, 192), (384, 264, 1088), (1000, 520, 1024)]
+    if layout == "NT":
+        shapes.append((264, 136, 1000))
+    for dtype in ("f16", "bf16"):
+        for M, N, K in shapes:
+            A, B = inputs.make_operands(M, N, K, dtype)
+            for cfg in ({"block_n": 64, **KS2}, {"block_n": 128, **KS2},
+                        {"block_n": 256, "cta_pair": 1, **KS2},
+                        {"block_n": 64, "split_k": 3, **KS2}):
+                C = pu.run_gpu_layout(A, B, dtype, cfg, layout)
+                pu.check_full(A, B, dtype, C, "%s ks2 %s %s %s" % (layout, cfg, (M, N, K), dtype))
+
+
+@pytest.mark.parametrize("layout", ["NN", "TT", "NT"])
+def test_two_kblock_slots_layouts_int8(layout):
+    for M, N, K in ((144, 80, 192), (512, 272, 1088)):
+        A, B = inputs.make_operands(M, N, K, "i8")
+        for cfg in ({"block_n": 64, **KS2}, {"block_n": 128, "cta_pair": 1, **KS2}):
+            C = pu.run_gpu_layout(A, B, "i8", cfg, layout)
+            pu.check_full(A, B, "i8", C, "i8 %s ks2 %s %s" % (layout, cfg, (M, N, K)))
