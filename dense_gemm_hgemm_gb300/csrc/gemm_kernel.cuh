@@ -630,83 +630,133 @@ __device__ __forceinline__ uint4 ld_shared_u4(uint32_t saddr) {
     return v;
 }
 
-// Store 32 partial values (columns [col, col+32)) of each of a warp's 32
-// consecutive block rows (warp_row0 + lane holds its row in v) of K-slice `slice`
+// Push phase, S K-slices (S fixed at compile time).  Epilogue warp `quad` sends
+// its 32 partial rows [32*quad, 32*quad+32) of K-slice `slice` (from TMEM, or
+// for integer outputs from the parked sums at `parked`), 32 columns at a time,
 // into the receive areas of the rows' owners.  The values pass through the
 // warp's staging buffer (36-word row stride: both passes are free of bank
 // conflicts) so that each remote store instruction writes 4 rows x 128
-// contiguous bytes instead of 32 scattered 16-byte pieces.
-template <int BN>
-__device__ __forceinline__ void push_warp_rows32(uint32_t recv, uint32_t stg, int log2_rows,
-                                                 int slice, int warp_row0, int lane, int col,
-                                                 const uint32_t* v, uint32_t rank_stride,
-                                                 uint32_t rank_offset) {
-#pragma unroll
-    for (int g = 0; g < 8; ++g)
-        st_shared_u4(stg + static_cast<uint32_t>((lane * 36 + 4 * g) * 4),
-                     make_uint4(v[g * 4 + 0], v[g * 4 + 1], v[g * 4 + 2], v[g * 4 + 3]));
-    __syncwarp();
+// contiguous bytes instead of 32 scattered 16-byte pieces.  With S known, the
+// owner of every group of 4 rows is known too: the warp maps each owner's
+// destination once and every later address is that base plus an immediate
+// (the loop is issue-bound: one warp per SM sub-partition runs it).
+template <int BN, int OUT, int S>
+__device__ __forceinline__ void cluster_push(uint32_t recv, uint32_t stg, uint32_t tmem_base,
+                                             uint32_t parked, int quad, int lane, int slice,
+                                             uint32_t rank_stride, uint32_t rank_offset) {
+    constexpr int kRows = kBM / S;                       // rows per owner: 64, 32 or 16
+    constexpr int kOwners = kRows >= 32 ? 1 : 32 / kRows;   // owners of one warp's rows
+    constexpr int kSpan = 32 / kOwners;                  // warp rows per owner
+    constexpr int kRowB = SplitRecv<BN>::kRowWords * 4;
     const int ch = lane & 7;
+    const int sub = lane >> 3;
+    uint32_t dst[kOwners];
 #pragma unroll
-    for (int s = 0; s < 8; ++s) {
-        const int r = 4 * s + (lane >> 3);
-        const uint4 q = ld_shared_u4(stg + static_cast<uint32_t>((r * 36 + 4 * ch) * 4));
-        const int row = warp_row0 + r;
-        const int owner = row >> log2_rows;
-        const int lr = row - (owner << log2_rows);
+    for (int k = 0; k < kOwners; ++k) {
+        const int row0 = quad * 32 + k * kSpan;
+        const int owner = row0 / kRows;
         const uint32_t local =
-            recv + static_cast<uint32_t>((((slice << log2_rows) + lr) * SplitRecv<BN>::kRowWords +
-                                          col + 4 * ch) * 4);
-        st_dsmem_u4(map_to_rank(local, static_cast<uint32_t>(owner) * rank_stride + rank_offset), q);
+            recv + static_cast<uint32_t>((slice * kRows + row0 % kRows + sub) * kRowB + ch * 16);
+        dst[k] = map_to_rank(local, static_cast<uint32_t>(owner) * rank_stride + rank_offset);
     }
-    __syncwarp();   // the staging buffer is rewritten by the next call
-}
-
-// The owner's half: sum its S slots in slice order, apply the epilogue, store
-// rows [part*128/S, (part+1)*128/S) of the block whose first global row is
-// block_row (threads take consecutive 4-column groups: coalesced stores).
-template <int BN, int OUT>
-__device__ __forceinline__ void cluster_sum_store(const KParams& p, int32_t block_row,
-                                                  int32_t col_base, int part, uint32_t recv,
-                                                  int tid, int nthreads) {
-    const int S = p.split_k;
-    const int rows = kBM / S;
-    constexpr int kVec = BN / 4;
-    constexpr int kU = 4;   // groups in flight per thread (their loads issued together)
-    const int total = rows * kVec;
-    const uint32_t slot = static_cast<uint32_t>(rows * SplitRecv<BN>::kRowWords * 4);
-    for (int t0 = tid; t0 < total; t0 += kU * nthreads) {
-        uint4 q[kU][8];
+    const uint32_t stg_w = stg + static_cast<uint32_t>(lane * 36 * 4);
+    const uint32_t stg_r = stg + static_cast<uint32_t>((sub * 36 + 4 * ch) * 4);
+#pragma unroll 1
+    for (int j = 0; j < BN / 32; ++j) {
+        uint32_t v[32];
+        if constexpr (OUT == kOutI32) {
+            const uint32_t src =
+                parked + static_cast<uint32_t>(((quad * 32 + lane) * (BN + 4) + j * 32) * 4);
 #pragma unroll
-        for (int u = 0; u < kU; ++u) {
-            const int t = t0 + u * nthreads;
-            if (t >= total) break;
-            const int lr = t / kVec;
-            const int c4 = (t % kVec) * 4;
-            const uint32_t off = recv + static_cast<uint32_t>((lr * SplitRecv<BN>::kRowWords + c4) * 4);
-#pragma unroll
-            for (int s = 0; s < 8; ++s)
-                if (s < S) q[u][s] = ld_shared_u4(off + static_cast<uint32_t>(s) * slot);
+            for (int g = 0; g < 8; ++g) {
+                const uint4 q = ld_shared_u4(src + g * 16);
+                v[g * 4 + 0] = q.x;
+                v[g * 4 + 1] = q.y;
+                v[g * 4 + 2] = q.z;
+                v[g * 4 + 3] = q.w;
+            }
+        } else {
+            tmem_ld_32x32b_x32(tmem_base + (static_cast<uint32_t>(quad * 32) << 16) + j * 32, v);
+            tmem_ld_wait();
         }
 #pragma unroll
-        for (int u = 0; u < kU; ++u) {
-            const int t = t0 + u * nthreads;
-            if (t >= total) break;
-            const int lr = t / kVec;
-            const int c4 = (t % kVec) * 4;
-            const int32_t grow = block_row + part * rows + lr;
-            const int32_t gcol = col_base + c4;
-            if (grow >= p.M || gcol >= p.N) continue;
-            uint32_t v[4] = {0u, 0u, 0u, 0u};
+        for (int g = 0; g < 8; ++g)
+            st_shared_u4(stg_w + g * 16,
+                         make_uint4(v[g * 4 + 0], v[g * 4 + 1], v[g * 4 + 2], v[g * 4 + 3]));
+        __syncwarp();
 #pragma unroll
-            for (int s = 0; s < 8; ++s)
-                if (s < S) add_u4<OUT>(v, q[u][s]);
-            const int64_t idx = static_cast<int64_t>(grow) * p.N + gcol;
-            if constexpr (OUT != kOutI32) apply_bias_act<1>(v, p, gcol);
+        for (int s = 0; s < 8; ++s) {   // rows 4s + sub of the warp
+            const uint4 q = ld_shared_u4(stg_r + static_cast<uint32_t>(s * 4 * 36 * 4));
+            const int k = (4 * s) / kSpan;
+            st_dsmem_u4(dst[k] + static_cast<uint32_t>((4 * s - k * kSpan) * kRowB + j * 128), q);
+        }
+        __syncwarp();   // the staging buffer is rewritten in the next round
+    }
+}
+
+template <int BN, int OUT, int kMaxS>
+__device__ __forceinline__ void cluster_push_any(int S, uint32_t recv, uint32_t stg,
+                                                 uint32_t tmem_base, uint32_t parked, int quad,
+                                                 int lane, int slice, uint32_t rank_stride,
+                                                 uint32_t rank_offset) {
+    if (S == 2)
+        cluster_push<BN, OUT, 2>(recv, stg, tmem_base, parked, quad, lane, slice, rank_stride,
+                                 rank_offset);
+    else if (S == 4)
+        cluster_push<BN, OUT, 4>(recv, stg, tmem_base, parked, quad, lane, slice, rank_stride,
+                                 rank_offset);
+    else if constexpr (kMaxS >= 8)
+        cluster_push<BN, OUT, 8>(recv, stg, tmem_base, parked, quad, lane, slice, rank_stride,
+                                 rank_offset);
+}
+
+// The owner's half, S slices (compile-time): sum its S slots in slice order
+// 0..S-1, apply the epilogue, store rows [part*128/S, (part+1)*128/S) of the
+// block whose first global row is block_row.  The 128 epilogue threads take
+// consecutive 4-column groups (coalesced stores); a thread's groups are
+// 128/(BN/4) rows apart, so every shared-memory address is the thread's base
+// plus an immediate, and a batch issues up to 16 loads before its first add.
+template <int BN, int OUT, int S, bool EPI>
+__device__ __forceinline__ void cluster_sum_store_s(const KParams& p, int32_t block_row,
+                                                    int32_t col_base, int part, uint32_t recv,
+                                                    int tid) {
+    constexpr int kRows = kBM / S;
+    constexpr int kVec = BN / 4;                      // 4-column groups per row
+    constexpr int kRowStep = kEpiWarps * 32 / kVec;   // rows between a thread's groups
+    constexpr int kG = kRows / kRowStep;              // groups per thread
+    constexpr int kB = (16 / S) < kG ? (16 / S) : kG;  // groups per batch
+    constexpr uint32_t kSlot = kRows * SplitRecv<BN>::kRowWords * 4;
+    constexpr uint32_t kStepB = kRowStep * SplitRecv<BN>::kRowWords * 4;
+    static_assert(kG % kB == 0, "whole batches");
+    const int c4 = (tid % kVec) * 4;
+    const int lr0 = tid / kVec;
+    const int32_t gcol = col_base + c4;
+    if (gcol >= p.N) return;
+    const int32_t grow0 = block_row + part * kRows + lr0;
+    const uint32_t src = recv + static_cast<uint32_t>((lr0 * SplitRecv<BN>::kRowWords + c4) * 4);
+    const int64_t step = static_cast<int64_t>(kRowStep) * p.N;
+    const int64_t idx0 = static_cast<int64_t>(grow0) * p.N + gcol;
+#pragma unroll
+    for (int b = 0; b < kG; b += kB) {
+        if (grow0 + b * kRowStep >= p.M) break;   // later groups lie further down
+        uint4 q[kB][S];
+#pragma unroll
+        for (int i = 0; i < kB; ++i)
+#pragma unroll
+            for (int s = 0; s < S; ++s)
+                q[i][s] = ld_shared_u4(src + (b + i) * kStepB + s * kSlot);
+#pragma unroll
+        for (int i = 0; i < kB; ++i) {
+            if (grow0 + (b + i) * kRowStep >= p.M) break;
+            uint32_t v[4] = {q[i][0].x, q[i][0].y, q[i][0].z, q[i][0].w};
+#pragma unroll
+            for (int s = 1; s < S; ++s) add_u4<OUT>(v, q[i][s]);
+            const int64_t idx = idx0 + (b + i) * step;
             if constexpr (OUT == kOutI32) {
                 *reinterpret_cast<uint4*>(reinterpret_cast<uint32_t*>(p.C) + idx) =
                     make_uint4(v[0], v[1], v[2], v[3]);
             } else {
+                if constexpr (EPI) apply_bias_act<1>(v, p, gcol);
                 uint2 h;
                 h.x = pack2<OUT>(__uint_as_float(v[0]), __uint_as_float(v[1]));
                 h.y = pack2<OUT>(__uint_as_float(v[2]), __uint_as_float(v[3]));
@@ -714,6 +764,29 @@ __device__ __forceinline__ void cluster_sum_store(const KParams& p, int32_t bloc
             }
         }
     }
+}
+
+template <int BN, int OUT, int S>
+__device__ __forceinline__ void cluster_sum_store_e(const KParams& p, int32_t block_row,
+                                                    int32_t col_base, int part, uint32_t recv,
+                                                    int tid) {
+    // (the loop without the bias/activation code when the plan has none)
+    if (OUT == kOutI32 || (p.bias == nullptr && p.act == 0))
+        cluster_sum_store_s<BN, OUT, S, false>(p, block_row, col_base, part, recv, tid);
+    else
+        cluster_sum_store_s<BN, OUT, S, OUT != kOutI32>(p, block_row, col_base, part, recv, tid);
+}
+
+template <int BN, int OUT, int kMaxS>
+__device__ __forceinline__ void cluster_sum_store(const KParams& p, int32_t block_row,
+                                                  int32_t col_base, int part, uint32_t recv,
+                                                  int tid) {
+    if (p.split_k == 2)
+        cluster_sum_store_e<BN, OUT, 2>(p, block_row, col_base, part, recv, tid);
+    else if (p.split_k == 4)
+        cluster_sum_store_e<BN, OUT, 4>(p, block_row, col_base, part, recv, tid);
+    else if constexpr (kMaxS >= 8)
+        cluster_sum_store_e<BN, OUT, 8>(p, block_row, col_base, part, recv, tid);
 }
 
 __device__ __forceinline__ void grid_dependency_wait() {
@@ -1212,38 +1285,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
         const UnitCoord c = unit_coord_fast(blockIdx.x, p);
         if (warp >= 2 && epi_ok) {
-            const int quad = warp & 3;
-            const int row = quad * 32 + lane;
             // this warp's (idle) TMA-store buffers serve as its transpose staging
             const uint32_t stg = staging + static_cast<uint32_t>((warp - 2) * 2 * L::kStoreBufBytes);
-            const int log2_rows = 7 - (31 - __clz(p.split_k));   // rows per owner = 128 / S
-#pragma unroll 1
-            for (int j = 0; j < BN / 32; ++j) {
-                uint32_t v[32];
-                if constexpr (OUT == kOutI32) {
-                    const uint32_t src = ring + SplitRecv<BN>::kBytes +
-                                         static_cast<uint32_t>((row * (BN + 4) + j * 32) * 4);
-#pragma unroll
-                    for (int g = 0; g < 8; ++g) {
-                        const uint4 q = ld_shared_u4(src + g * 16);
-                        v[g * 4 + 0] = q.x;
-                        v[g * 4 + 1] = q.y;
-                        v[g * 4 + 2] = q.z;
-                        v[g * 4 + 3] = q.w;
-                    }
-                } else {
-                    tmem_ld_32x32b_x32(tmem_base + (static_cast<uint32_t>(quad * 32) << 16) + j * 32, v);
-                    tmem_ld_wait();
-                }
-                push_warp_rows32<BN>(ring, stg, log2_rows, c.split, quad * 32, lane, j * 32, v, 1u,
-                                     0u);
-            }
+            cluster_push_any<BN, OUT, 8>(p.split_k, ring, stg, tmem_base,
+                                         ring + SplitRecv<BN>::kBytes, warp & 3, lane, c.split,
+                                         1u, 0u);
         }
         cluster_sync_all();         // every slice has arrived at its owner
         if (warp >= 2)
-            cluster_sum_store<BN, OUT>(p, c.m_blk * kBM, c.n_blk * BN,
-                                       static_cast<int>(cluster_ctarank()), ring,
-                                       static_cast<int>(threadIdx.x) - 64, kEpiWarps * 32);
+            cluster_sum_store<BN, OUT, 8>(p, c.m_blk * kBM, c.n_blk * BN,
+                                          static_cast<int>(cluster_ctarank()), ring,
+                                          static_cast<int>(threadIdx.x) - 64);
     }
 
     // ---------------------------------------------------------------- teardown

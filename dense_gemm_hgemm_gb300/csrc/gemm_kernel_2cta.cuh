@@ -524,39 +524,18 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
         const UnitCoord c = c_first;
         if (warp >= 2 && epi_ok) {
-            // rows of this CTA's half go to the CTAs (s', same half) of the cluster
-            const int quad = warp & 3;
-            const int row = quad * 32 + lane;
+            // rows of this CTA's half go to the CTAs (s', same half) of the cluster;
             // this warp's (idle) TMA-store buffers serve as its transpose staging
             const uint32_t stg = staging + static_cast<uint32_t>((warp - 2) * 2 * L::kStoreBufBytes);
-            const int log2_rows = 7 - (31 - __clz(p.split_k));   // rows per owner = 128 / S
-#pragma unroll 1
-            for (int j = 0; j < BN / 32; ++j) {
-                uint32_t v[32];
-                if constexpr (OUT == kOutI32) {
-                    const uint32_t src = ring + SplitRecv<BN>::kBytes +
-                                         static_cast<uint32_t>((row * (BN + 4) + j * 32) * 4);
-#pragma unroll
-                    for (int g = 0; g < 8; ++g) {
-                        const uint4 q = ld_shared_u4(src + g * 16);
-                        v[g * 4 + 0] = q.x;
-                        v[g * 4 + 1] = q.y;
-                        v[g * 4 + 2] = q.z;
-                        v[g * 4 + 3] = q.w;
-                    }
-                } else {
-                    tmem_ld_32x32b_x32(tmem_base + (static_cast<uint32_t>(quad * 32) << 16) + j * 32, v);
-                    tmem_ld_wait();
-                }
-                push_warp_rows32<BN>(ring, stg, log2_rows, c.split, quad * 32, lane, j * 32, v, 2u,
-                                     rank);
-            }
+            cluster_push_any<BN, OUT, 4>(p.split_k, ring, stg, tmem_base,
+                                         ring + SplitRecv<BN>::kBytes, warp & 3, lane, c.split,
+                                         2u, rank);
         }
         cluster_sync_all();         // every slice has arrived at its owner
         if (warp >= 2)
-            cluster_sum_store<BN, OUT>(p, c.m_blk * 2 * kBM + static_cast<int32_t>(rank) * kBM,
-                                       c.n_blk * BN, static_cast<int>(crank >> 1), ring,
-                                       static_cast<int>(threadIdx.x) - 64, kEpiWarps * 32);
+            cluster_sum_store<BN, OUT, 4>(p, c.m_blk * 2 * kBM + static_cast<int32_t>(rank) * kBM,
+                                          c.n_blk * BN, static_cast<int>(crank >> 1), ring,
+                                          static_cast<int>(threadIdx.x) - 64);
     }
 
     // ---------------------------------------------------------------- teardown
