@@ -661,34 +661,44 @@ __device__ __forceinline__ void cluster_push(uint32_t recv, uint32_t stg, uint32
     }
     const uint32_t stg_w = stg + static_cast<uint32_t>(lane * 36 * 4);
     const uint32_t stg_r = stg + static_cast<uint32_t>((sub * 36 + 4 * ch) * 4);
-#pragma unroll 1
-    for (int j = 0; j < BN / 32; ++j) {
-        uint32_t v[32];
+    const uint32_t src_t = tmem_base + (static_cast<uint32_t>(quad * 32) << 16);
+    const uint32_t src_p = parked + static_cast<uint32_t>((quad * 32 + lane) * (BN + 4) * 4);
+    // 32 partial values of this thread's row, columns [32j, 32j+32)
+    auto fetch = [&](int j, uint32_t (&v)[32]) {
         if constexpr (OUT == kOutI32) {
-            const uint32_t src =
-                parked + static_cast<uint32_t>(((quad * 32 + lane) * (BN + 4) + j * 32) * 4);
 #pragma unroll
             for (int g = 0; g < 8; ++g) {
-                const uint4 q = ld_shared_u4(src + g * 16);
+                const uint4 q = ld_shared_u4(src_p + static_cast<uint32_t>(j * 128 + g * 16));
                 v[g * 4 + 0] = q.x;
                 v[g * 4 + 1] = q.y;
                 v[g * 4 + 2] = q.z;
                 v[g * 4 + 3] = q.w;
             }
         } else {
-            tmem_ld_32x32b_x32(tmem_base + (static_cast<uint32_t>(quad * 32) << 16) + j * 32, v);
-            tmem_ld_wait();
+            tmem_ld_32x32b_x32(src_t + static_cast<uint32_t>(j * 32), v);
         }
+    };
+    // (fully unrolled: no loop-carried copy of v can be placed between an
+    // asynchronous TMEM read and its wait)
+    uint32_t v[32];
+    fetch(0, v);
+#pragma unroll
+    for (int j = 0; j < BN / 32; ++j) {
+        if constexpr (OUT != kOutI32) tmem_ld_wait();
 #pragma unroll
         for (int g = 0; g < 8; ++g)
             st_shared_u4(stg_w + g * 16,
                          make_uint4(v[g * 4 + 0], v[g * 4 + 1], v[g * 4 + 2], v[g * 4 + 3]));
         __syncwarp();
+        // the next block's TMEM read overlaps this block's sends
+        if (j + 1 < BN / 32) fetch(j + 1, v);
+        uint4 q[8];   // rows 4s + sub of the warp: all loads before the first send
 #pragma unroll
-        for (int s = 0; s < 8; ++s) {   // rows 4s + sub of the warp
-            const uint4 q = ld_shared_u4(stg_r + static_cast<uint32_t>(s * 4 * 36 * 4));
+        for (int s = 0; s < 8; ++s) q[s] = ld_shared_u4(stg_r + static_cast<uint32_t>(s * 4 * 36 * 4));
+#pragma unroll
+        for (int s = 0; s < 8; ++s) {
             const int k = (4 * s) / kSpan;
-            st_dsmem_u4(dst[k] + static_cast<uint32_t>((4 * s - k * kSpan) * kRowB + j * 128), q);
+            st_dsmem_u4(dst[k] + static_cast<uint32_t>((4 * s - k * kSpan) * kRowB + j * 128), q[s]);
         }
         __syncwarp();   // the staging buffer is rewritten in the next round
     }
