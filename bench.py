@@ -334,7 +334,7 @@ def e2e_sweep(items, stream, steps, groups=8):
     ev_out = [torch.cuda.Event() for _ in range(groups)]
     torch.cuda.synchronize()
 
-    def one():
+    def one(compute=True):
         for g in range(groups):
             lo, hi = rng_in[g]
             with torch.cuda.stream(s_in):
@@ -343,8 +343,9 @@ def e2e_sweep(items, stream, steps, groups=8):
                 ev_in[g].record(s_in)
             stream.wait_event(ev_in[g])
             stream.wait_event(ev_out[g])           # the previous step's copy-out of this range
-            for plan, dA, dB, dC in views[bounds[g]:bounds[g + 1]]:
-                plan.run(dA, dB, dC, stream)
+            if compute:
+                for plan, dA, dB, dC in views[bounds[g]:bounds[g + 1]]:
+                    plan.run(dA, dB, dC, stream)
             ev_mm[g].record(stream)
             lo, hi = rng_out[g]
             with torch.cuda.stream(s_out):
@@ -359,14 +360,24 @@ def e2e_sweep(items, stream, steps, groups=8):
         one()
     torch.cuda.synchronize()
     wall = time.perf_counter() - t0
+    # the same copies alone: the floor the host link sets for this step
+    one(compute=False)
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for _ in range(steps):
+        one(compute=False)
+    torch.cuda.synchronize()
+    copy_ms = (time.perf_counter() - t0) * 1e3 / steps
     # results came back: spot-check one C against the device copy of the eager run
     mid = len(items) // 2
     w, plan, A, B, C = items[mid]
     oc = out_off[mid]
     got = h_out[oc:oc + C.numel() * 2].view(torch.float16).view(C.shape)
+    one()   # leave every result in place for the check below
+    torch.cuda.synchronize()
     if not torch.equal(got.view(torch.int16), C.cpu().view(torch.int16)):
         raise RuntimeError("e2e: copied-back result differs from the device result")
-    return wall * 1e3 / steps, h2d, d2h
+    return wall * 1e3 / steps, h2d, d2h, copy_ms
 
 
 def launch_floor_us(stream, sms, n=2000, graph=False):
@@ -701,10 +712,14 @@ def ours(args):
                     "launch overlap)",
             "headline_128x2048x128_us_in_sweep": round(times.get("sweep_128x2048x128_f16", 0) * 1e3, 3),
         }
-        e2e_ms, h2d, d2h = e2e_sweep(items, stream, steps=max(3, min(20, args.steps)))
+        e2e_ms, h2d, d2h, copy_ms = e2e_sweep(items, stream, steps=max(3, min(20, args.steps)))
         line["e2e"] = {"value": round(flops_step / (e2e_ms * 1e-3) / 1e12, 3), "unit": UNIT,
                        "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                       "ms_per_step": round(e2e_ms, 3)}
+                       "ms_per_step": round(e2e_ms, 3),
+                       "copy_only_ms_per_step": round(copy_ms, 3),
+                       "frac_of_copy_floor": round(copy_ms / e2e_ms, 4),
+                       "note": "copy_only: the same host<->device copies with no GEMM; the "
+                               "step is bound by the host link when the fraction is near 1"}
         del graph
         for _, plan, *_ in items:
             plan.close()

@@ -22,11 +22,15 @@ MODES = [
     ("one_sm_direct", (130, 72, 208), {"block_n": 64, "direct_store": 1}),
     ("workspace_split", (200, 136, 1024), {"block_n": 64, "split_k": 3}),
     ("cluster_split", (128, 256, 2048), {"block_n": 64, "split_k": 4, "split_mode": 1}),
+    ("cluster_split2", (260, 200, 1536), {"block_n": 128, "split_k": 2, "split_mode": 1}),
+    ("cluster_split8", (136, 520, 2048), {"block_n": 256, "split_k": 8, "split_mode": 1}),
     ("sm_pair", (1000, 520, 512), {"block_n": 256, "cta_pair": 1}),
     ("multicast2", (300, 264, 1000), {"block_n": 64, "multicast": 2}),
     ("multicast4", (200, 520, 640), {"block_n": 128, "multicast": 4}),
     ("pair_split", (300, 264, 1024), {"block_n": 256, "cta_pair": 1, "split_k": 4,
                                       "split_mode": 1}),
+    ("pair_split2", (520, 136, 1024), {"block_n": 128, "cta_pair": 1, "split_k": 2,
+                                       "split_mode": 1}),
     ("two_kblock_slots", (300, 264, 1088), {"block_n": 128, "kblocks_per_stage": 2}),
 ]
 
