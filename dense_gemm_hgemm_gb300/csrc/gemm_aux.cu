@@ -15,36 +15,62 @@
 namespace gbg {
 namespace {
 
-__device__ __forceinline__ uint32_t widen_pair(int8_t lo, int8_t hi) {
-    __half2 h = __halves2half2(__int2half_rn(lo), __int2half_rn(hi));
-    return *reinterpret_cast<uint32_t*>(&h);
+// Four int8 values (one 32-bit word, element 0 in the low byte) -> four fp16
+// values (two 32-bit words, element 0 in the low half), exactly.  With
+// u = x + 128 in [0, 255] (the byte with its top bit flipped), the fp16 bit
+// pattern 0x64 followed by the byte u is 1024 + u: exponent 10, and u fills the
+// low eight of the ten fraction bits, one unit in the last place apart.
+// Subtracting 1152 = 1024 + 128 (0x6480) leaves x; both operands and the
+// difference are integers of at most 11 significant bits, so nothing rounds.
+__device__ __forceinline__ void widen4(uint32_t w, uint32_t& lo, uint32_t& hi) {
+    const uint32_t u = w ^ 0x80808080u;
+    const uint32_t l = __byte_perm(u, 0x64646464u, 0x5140);   // u0 | 0x64 << 8 | u1 << 16 | 0x64 << 24
+    const uint32_t h = __byte_perm(u, 0x64646464u, 0x7362);   // u2, 0x64, u3, 0x64
+    const __half2 off = __half2half2(__ushort_as_half(static_cast<unsigned short>(0x6480u)));
+    const __half2 rl = __hsub2(*reinterpret_cast<const __half2*>(&l), off);
+    const __half2 rh = __hsub2(*reinterpret_cast<const __half2*>(&h), off);
+    lo = *reinterpret_cast<const uint32_t*>(&rl);
+    hi = *reinterpret_cast<const uint32_t*>(&rh);
 }
 
-// na, nb: number of 16-element groups of A and of B.
-__global__ void __launch_bounds__(256) widen_i8_kernel(const int4* __restrict__ a, int64_t na,
-                                                       const int4* __restrict__ b, int64_t nb,
+__device__ __forceinline__ void widen16(const uint4& v, uint4& lo, uint4& hi) {
+    widen4(v.x, lo.x, lo.y);
+    widen4(v.y, lo.z, lo.w);
+    widen4(v.z, hi.x, hi.y);
+    widen4(v.w, hi.z, hi.w);
+}
+
+// na, nb: number of 16-element groups of A and of B.  Each thread has four
+// independent 16-byte loads in flight before it converts and stores.
+__global__ void __launch_bounds__(256) widen_i8_kernel(const uint4* __restrict__ a, int64_t na,
+                                                       const uint4* __restrict__ b, int64_t nb,
                                                        uint4* __restrict__ a16,
                                                        uint4* __restrict__ b16) {
+    constexpr int kU = 4;
     const int64_t total = na + nb;
     const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
-    for (int64_t g = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; g < total;
-         g += stride) {
-        const bool in_a = g < na;
-        const int64_t i = in_a ? g : g - na;
-        const int4 v = __ldg((in_a ? a : b) + i);
-        const int8_t* x = reinterpret_cast<const int8_t*>(&v);
+    int64_t g = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+    auto src = [&](int64_t e) { return e < na ? a + e : b + (e - na); };
+    auto dst = [&](int64_t e) { return e < na ? a16 + 2 * e : b16 + 2 * (e - na); };
+    for (; g + (kU - 1) * stride < total; g += kU * stride) {
+        uint4 v[kU];
+#pragma unroll
+        for (int u = 0; u < kU; ++u) v[u] = __ldg(src(g + u * stride));
+#pragma unroll
+        for (int u = 0; u < kU; ++u) {
+            uint4 lo, hi;
+            widen16(v[u], lo, hi);
+            uint4* d = dst(g + u * stride);
+            d[0] = lo;
+            d[1] = hi;
+        }
+    }
+    for (; g < total; g += stride) {
         uint4 lo, hi;
-        lo.x = widen_pair(x[0], x[1]);
-        lo.y = widen_pair(x[2], x[3]);
-        lo.z = widen_pair(x[4], x[5]);
-        lo.w = widen_pair(x[6], x[7]);
-        hi.x = widen_pair(x[8], x[9]);
-        hi.y = widen_pair(x[10], x[11]);
-        hi.z = widen_pair(x[12], x[13]);
-        hi.w = widen_pair(x[14], x[15]);
-        uint4* dst = (in_a ? a16 : b16) + 2 * i;
-        dst[0] = lo;
-        dst[1] = hi;
+        widen16(__ldg(src(g)), lo, hi);
+        uint4* d = dst(g);
+        d[0] = lo;
+        d[1] = hi;
     }
 }
 
@@ -101,7 +127,7 @@ cudaError_t launch_widen_i8(const int8_t* a, int64_t na, const int8_t* b, int64_
     // na, nb are element counts, multiples of 16 (K % 16 == 0).
     const int64_t ga = na / 16, gb = nb / 16;
     widen_i8_kernel<<<grid_for(ga + gb, num_sms), 256, 0, stream>>>(
-        reinterpret_cast<const int4*>(a), ga, reinterpret_cast<const int4*>(b), gb,
+        reinterpret_cast<const uint4*>(a), ga, reinterpret_cast<const uint4*>(b), gb,
         reinterpret_cast<uint4*>(a16), reinterpret_cast<uint4*>(b16));
     return cudaGetLastError();
 }
