@@ -4,8 +4,8 @@
 //   * zero_fill: C = 0 for K == 0 (the empty sum); fill_bias_act: C = act(bias)
 //     for K == 0 with a bias;
 //   * empty: a kernel with no body, for measuring the launch-latency floor.
-// Both are grid-stride loops over 16-byte vectors sized to a whole number of
-// waves of the SMs.
+// The widening and fill kernels are grid-stride loops over 16-byte vectors,
+// launched with at most eight 256-thread blocks per SM.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <stdint.h>
