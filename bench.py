@@ -170,8 +170,9 @@ class ClockSampler:
 
 
 # Sources that build no kernel a GEMM launch runs (the int8 widening / fill /
-# empty kernels, the TMA intensity sweep): left out of the digest.
-_DIGEST_SKIP = ("gemm_aux.cu", "tma_intensity.cu")
+# empty kernels, the TMA intensity sweep, the CPython entry points): left out
+# of the digest.
+_DIGEST_SKIP = ("gemm_aux.cu", "tma_intensity.cu", "gemm_pycall.c")
 
 
 def source_digest() -> str:
@@ -555,8 +556,9 @@ def server_mode(stream, calls=2000):
         out["graph_calls_per_s"] = round(reps * per_graph / (time.perf_counter() - t0), 1)
         plan.check(stream)
     out["shape"] = [w.M, w.N, w.K, w.dtype]
-    out["note"] = ("host wall clock over %d calls; eager = one gemm_run (ctypes) per call, "
-                   "graph = %d captured calls per replay" % (calls, per_graph))
+    out["note"] = ("host wall clock over %d calls; eager = one Plan.run -> gemm_run per call "
+                   "(the package's vectorcall entry point), graph = %d captured calls per "
+                   "replay" % (calls, per_graph))
     return out
 
 

@@ -12,7 +12,8 @@ import ctypes
 import os
 import threading
 
-from ._build import LIB_PATH, build_library
+from ._build import LIB_PATH, build_pycall
+from ._build import build_library as _build_cuda_library
 
 __all__ = [
     "GEMM_F16", "GEMM_BF16", "GEMM_I8_I32", "GEMM_LAYOUT_TN", "GEMM_LAYOUT_NN", "GEMM_LAYOUT_TT",
@@ -60,6 +61,15 @@ class gemm_config_t(ctypes.Structure):
 
 _lock = threading.Lock()
 _lib = None
+_pycall = None   # CPython entry points for gemm_run / gemm_launch_empty, when built
+
+
+def build_library(force: bool = False, verbose: bool = False, ptxas_info: bool = False) -> str:
+    """Build libgemm_gb300.so (nvcc, sm_103a) if stale, and the CPython entry points
+    for the per-call functions (gcc); return the library's path."""
+    path = _build_cuda_library(force=force, verbose=verbose, ptxas_info=ptxas_info)
+    build_pycall(force=force)
+    return path
 
 
 def library() -> ctypes.CDLL:
@@ -101,6 +111,14 @@ def library() -> ctypes.CDLL:
                 fn = getattr(lib, name)
                 fn.argtypes = args
                 fn.restype = res
+            global _pycall
+            try:
+                from . import _gemm_pycall as pc
+                addr = lambda f: ctypes.cast(f, ctypes.c_void_p).value
+                pc.set_targets(addr(lib.gemm_run), addr(lib.gemm_launch_empty))
+                _pycall = pc
+            except ImportError:
+                _pycall = None
             _lib = lib
     return _lib
 
@@ -159,6 +177,9 @@ def gemm_abi_version() -> int:
 
 
 def gemm_launch_empty(grid: int, stream=None) -> None:
+    if library() is not None and _pycall is not None:
+        _check(_pycall.launch_empty(int(grid), _stream(stream) or 0), "gemm_launch_empty")
+        return
     _check(library().gemm_launch_empty(int(grid), _stream(stream)), "gemm_launch_empty")
 
 
@@ -201,7 +222,12 @@ def gemm_plan_create_with_config(M, N, K, dtype, config, layout: int = GEMM_LAYO
 
 
 def gemm_run(plan: int, A, B, C, stream=None) -> None:
-    _check(library().gemm_run(plan, _ptr(A), _ptr(B), _ptr(C), _stream(stream)), "gemm_run")
+    lib = library()
+    if _pycall is not None:
+        _check(_pycall.run(plan or 0, _ptr(A) or 0, _ptr(B) or 0, _ptr(C) or 0,
+                           _stream(stream) or 0), "gemm_run")
+        return
+    _check(lib.gemm_run(plan, _ptr(A), _ptr(B), _ptr(C), _stream(stream)), "gemm_run")
 
 
 ACT_NONE, ACT_RELU, ACT_GELU, ACT_SILU = 0, 1, 2, 3
@@ -286,10 +312,21 @@ class Plan:
         return gemm_plan_get_launch(self.handle)
 
     def run(self, A, B, C, stream=None, bias=None, act=ACT_NONE) -> None:
-        if bias is None and act in (ACT_NONE, "none"):
-            gemm_run(self.handle, A, B, C, stream)
-        else:
+        if bias is not None or act not in (ACT_NONE, "none"):
             gemm_run_bias_act(self.handle, A, B, C, bias, act, stream)
+            return
+        pc = _pycall
+        if pc is None:
+            gemm_run(self.handle, A, B, C, stream)
+            return
+        try:   # tensors and a stream object: the per-call path, kept short
+            st = pc.run(self.handle or 0, A.data_ptr(), B.data_ptr(), C.data_ptr(),
+                        stream.cuda_stream)
+        except AttributeError:   # addresses or a stream handle given as ints, or no stream
+            st = pc.run(self.handle or 0, _ptr(A) or 0, _ptr(B) or 0, _ptr(C) or 0,
+                        _stream(stream) or 0)
+        if st:
+            raise GemmError(st, "gemm_run")
 
     def check(self, stream=None) -> None:
         gemm_plan_check(self.handle, stream)

@@ -2,12 +2,15 @@
 
 Translation units compile in parallel; the link uses nvcc's static CUDA runtime,
 so the library depends only on the driver (loaded lazily by the runtime).
+Beside it, gcc builds _gemm_pycall (CPython entry points for the per-call
+functions; the binding uses ctypes for them when it cannot be built).
 """
 from __future__ import annotations
 
 import os
 import subprocess
 import sys
+import sysconfig
 from concurrent.futures import ThreadPoolExecutor
 
 PKG = os.path.dirname(os.path.abspath(__file__))
@@ -19,6 +22,8 @@ LIB_PATH = os.path.join(PKG, "libgemm_gb300.so")
 
 SOURCES = ["gemm_api.cu", "gemm_aux.cu", "gemm_inst_f16.cu", "gemm_inst_bf16.cu",
            "gemm_inst_i32.cu", "gemm_noalloc.cu", "tma_intensity.cu"]
+PYCALL_SRC = os.path.join(CSRC, "gemm_pycall.c")
+PYCALL_PATH = os.path.join(PKG, "_gemm_pycall" + (sysconfig.get_config_var("EXT_SUFFIX") or ".so"))
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 
@@ -33,7 +38,7 @@ def _flags(extra=()):
 
 
 def _deps():
-    files = [os.path.join(CSRC, f) for f in os.listdir(CSRC)]
+    files = [os.path.join(CSRC, f) for f in os.listdir(CSRC) if not f.endswith(".c")]
     files += [os.path.join(INCLUDE, f) for f in os.listdir(INCLUDE)]
     files.append(os.path.abspath(__file__))
     return files
@@ -76,6 +81,27 @@ def build_library(force: bool = False, verbose: bool = False, ptxas_info: bool =
     return LIB_PATH
 
 
+def build_pycall(force: bool = False) -> str | None:
+    """Compile the CPython entry-point module; None (with a note on stderr) if this
+    interpreter's headers or a C compiler are missing."""
+    if (not force and os.path.exists(PYCALL_PATH)
+            and os.path.getmtime(PYCALL_PATH) >= os.path.getmtime(PYCALL_SRC)):
+        return PYCALL_PATH
+    inc = sysconfig.get_paths().get("include", "")
+    if not os.path.exists(os.path.join(inc, "Python.h")):
+        sys.stderr.write("_gemm_pycall not built: no Python.h in %s\n" % inc)
+        return None
+    tmp = PYCALL_PATH + ".tmp.%d" % os.getpid()
+    cmd = [os.environ.get("CC", "gcc"), "-O2", "-shared", "-fPIC", "-I", inc, PYCALL_SRC, "-o", tmp]
+    r = subprocess.run(cmd, capture_output=True, text=True)
+    if r.returncode != 0:
+        sys.stderr.write("_gemm_pycall not built:\n%s\n%s" % (" ".join(cmd), r.stderr))
+        return None
+    os.replace(tmp, PYCALL_PATH)
+    return PYCALL_PATH
+
+
 if __name__ == "__main__":
     print(build_library(force="--force" in sys.argv, verbose=True,
                         ptxas_info="--ptxas-info" in sys.argv))
+    print(build_pycall(force="--force" in sys.argv))

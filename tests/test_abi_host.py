@@ -83,6 +83,24 @@ def test_create_without_gpu_reports_no_device(gemm_lib):
     assert _create_status(gemm_lib, 128, 128, 64, 0) == 4
 
 
+def test_vectorcall_entry_points_match_ctypes(gemm_lib):
+    """The CPython entry points of gemm_run / gemm_launch_empty are built with the
+    library and return what the ctypes calls return (no device needed)."""
+    import dense_gemm_hgemm_gb300 as g
+    lib = g.library()                                         # loads both
+    pc = g._pycall
+    assert pc is not None, "_gemm_pycall was not built"
+    assert pc.run(0, 0, 0, 0, 0) == lib.gemm_run(None, None, None, None, None) == 1
+    assert pc.run(0, 16, 32, 48, 0) == 1                      # null plan: invalid argument
+    with pytest.raises(TypeError):
+        pc.run(0, 0, 0)
+    with pytest.raises(TypeError):
+        pc.run(0, "A", 0, 0, 0)                                 # not an address
+    with pytest.raises(g.GemmError) as e:
+        g.gemm_run(0, None, None, None, 0)
+    assert e.value.status == 1
+
+
 def test_null_handles(gemm_lib):
     lib = gemm_lib.library()
     assert lib.gemm_plan_destroy(None) == 0
