@@ -299,13 +299,15 @@ def per_shape_times(items, stream, reps=3):
     return {k: statistics.median(v) for k, v in res.items()}
 
 
-def e2e_sweep(items, stream, steps, groups=8):
+def e2e_sweep(items, stream, steps, groups=32):
     """The sweep through the public API with host operands, end to end: every step
     copies all A, B from pinned host memory to the device, runs gemm_run per shape
     and copies every C back.  Operands are packed in one pinned buffer per
     direction and the step is pipelined over groups of shapes on three streams
     (host-to-device copy of group g+1 and device-to-host copy of group g-1 overlap
-    the GEMMs of group g), as a user feeding the GPU from host memory would."""
+    the GEMMs of group g), as a user feeding the GPU from host memory would.  Groups
+    are consecutive shapes of about equal bytes (in + out), so that neither the
+    first copy in nor the last copy back is a large exposed share of the step."""
     align = 256
     in_off, out_off, n_in, n_out = [], [], 0, 0
     for w, plan, A, B, C in items:
@@ -330,9 +332,17 @@ def e2e_sweep(items, stream, steps, groups=8):
         views.append((plan, dA, dB, dC))
         h2d += a_b + b_b
         d2h += c_b
-    # groups of consecutive shapes with contiguous byte ranges
+    # groups of consecutive shapes (contiguous byte ranges) of about equal bytes
     n = len(items)
-    bounds = [round(i * n / groups) for i in range(groups + 1)]
+    sizes = [A.numel() * 2 + B.numel() * 2 + C.numel() * 2 for _, _, A, B, C in items]
+    total = float(sum(sizes))
+    bounds, acc = [0], 0
+    for i, sz in enumerate(sizes):
+        acc += sz
+        if acc >= total * len(bounds) / groups and i + 1 < n and len(bounds) < groups:
+            bounds.append(i + 1)
+    bounds.append(n)
+    groups = len(bounds) - 1
     rng_in = [(in_off[bounds[g]][0], in_off[bounds[g + 1]][0] if bounds[g + 1] < n else n_in)
               for g in range(groups)]
     rng_out = [(out_off[bounds[g]], out_off[bounds[g + 1]] if bounds[g + 1] < n else n_out)
