@@ -40,3 +40,33 @@ def test_graph_capture_and_replay(gemm_lib, dtype):
         torch.cuda.synchronize()
         plan.check()
         pu.check_full(A2, B2, dtype, C, "graph replay 2")
+
+
+def test_vectorcall_and_ctypes_paths_agree(gemm_lib, monkeypatch):
+    """Plan.run through the vectorcall entry point and through ctypes (the path used
+    when the module cannot be built) launch the same kernel: identical bytes, for
+    every way of passing the stream."""
+    M, N, K = 192, 320, 384
+    A, B = inputs.make_operands(M, N, K, "f16")
+    dA, dB = A.cuda(), B.cuda()
+    s = torch.cuda.Stream()
+    outs = []
+    for fast in (True, False):
+        if not fast:
+            monkeypatch.setattr(g, "_pycall", None)
+        with g.Plan(M, N, K, "f16") as plan:
+            for stream in (s, s.cuda_stream, None):
+                C = torch.zeros(M, N, dtype=torch.float16, device="cuda")
+                with torch.cuda.stream(s):
+                    plan.run(dA, dB, C, stream)
+                plan.check(s)
+                torch.cuda.synchronize()
+                outs.append(C)
+            # raw device addresses as ints
+            C = torch.zeros(M, N, dtype=torch.float16, device="cuda")
+            plan.run(dA.data_ptr(), dB.data_ptr(), C.data_ptr(), s)
+            plan.check(s)
+            outs.append(C)
+    for C in outs[1:]:
+        assert torch.equal(C.view(torch.int16), outs[0].view(torch.int16))
+    pu.check_full(A, B, "f16", outs[0], "vectorcall vs ctypes")
