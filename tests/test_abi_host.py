@@ -280,3 +280,16 @@ def test_raster_matches_its_definition(gemm_lib, mb, nb, g):
     ts |= {rng.randrange(total) for _ in range(3000)}
     for t in sorted(ts):
         assert gemm_lib.gemm_tile_coords(mb, nb, g, t) == _raster_reference(mb, nb, g, t), (t,)
+
+
+def test_tuner_proposes_only_configs_the_library_accepts(gemm_lib):
+    """Every candidate the sweep tuner times, for every sweep and named shape, passes
+    the library's own validation (the tuner does not catch plan errors)."""
+    from dense_gemm_hgemm_gb300 import tune
+    shapes = [(w.M, w.N, w.K, w.dtype) for w in workloads.NAMED + tuple(workloads.sweep_shapes())]
+    n = 0
+    for M, N, K, dt in shapes:
+        for c in tune.candidates(M, N, K, dt, 152):
+            gemm_lib.gemm_workspace_bytes(M, N, K, dt, c)   # raises on a rejected config
+            n += 1
+    assert n > 10000
