@@ -1,24 +1,29 @@
 #!/usr/bin/env python
-"""Benchmark: the fp16 TN GEMM shape sweep (343 shapes, M, N, K in {64..4096}).
+"""Benchmark: the fp16 TN GEMM shape sweep (343 shapes, M, N, K in {64..4096}) on one GPU.
 
 One step = one gemm_run for every shape of the sweep, each on its own
 device-resident A, B, C (2.77 GB of distinct operands per step, more than the
 129 MB L2, so no step finds the previous step's data in L2).  `value` is the
-whole-job throughput sum(2*M*N*K) / step time in TFLOP/s, over all ranks.
+throughput sum(2*M*N*K) / step time in TFLOP/s.
 
-  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+  python bench.py [--gpus 1] [--steps K] [--warmup W] [--impl ours|reference]
 
-Prints one JSON line (rank 0).  Also reported on that line (measured outside
-the timed region): `e2e` (the same sweep through the C ABI with operands copied
-from pinned host memory and C copied back inside the timed region), `named`
-(µs/call and TFLOP/s of the named workloads: 64x4096x64 and 128x2048x128 fp16,
-8192^3 fp16, the 4096x14336x4096 bf16 FFN shape, 4096^3 int8->int32), the
-roofline of the sweep, GPU clocks sampled during the timed region, and the CPU
-oracle timed on a bounded sample (`cpu_baseline`).
+Prints one JSON line.  `roofline` is the step's roofline: per shape the largest
+of tensor time, compulsory-byte HBM time and the launch floor, summed over the
+343 shapes and divided by the timed step (also per class of shapes).  Also on
+the line (measured outside the timed region): `e2e` (the same sweep through the
+C ABI with operands copied from pinned host memory and C copied back inside the
+timed region), `named` (µs/call and TFLOP/s of the named workloads: 64x4096x64
+and 128x2048x128 fp16, 8192^3 fp16, the 4096x14336x4096 bf16 FFN shape,
+4096^3 int8->int32), GPU clocks sampled during the timed region, and the CPU
+oracle timed on bounded samples (`cpu_baseline`).
+
+The library runs on one GPU: with --gpus > 1 (or WORLD_SIZE > 1) the GEMM arm
+prints one "unavailable" line and does no work.
 
 --impl reference times the CPU oracle (the only reference this method has) on a
 bounded sample of the same sweep, on the host cores, and prints the same line
-with "impl": "reference".
+with "impl": "reference" (rank 0 only under torchrun).
 """
 from __future__ import annotations
 
@@ -76,40 +81,17 @@ def load_peaks():
         return dict(FALLBACK_PEAKS), "fallback"
 
 
-class Dist:
-    """Rank bookkeeping; torch.distributed only when launched with WORLD_SIZE > 1."""
-
-    def __init__(self, backend=None):
-        self.world = int(os.environ.get("WORLD_SIZE", "1"))
-        self.rank = int(os.environ.get("RANK", "0"))
-        self.local_rank = int(os.environ.get("LOCAL_RANK", "0"))
-        self.pg = None
-        if self.world > 1:
-            import torch.distributed as dist
-            if backend is None:
-                backend = "nccl" if torch.cuda.is_available() else "gloo"
-            dist.init_process_group(backend=backend)
-            self.pg = dist
-            self.backend = backend
-
-    def barrier(self):
-        if self.pg is not None:
-            if self.backend == "nccl":
-                self.pg.barrier(device_ids=[self.local_rank])
-            else:
-                self.pg.barrier()
-
-    def max(self, x: float) -> float:
-        if self.pg is None:
-            return x
-        dev = "cuda" if self.backend == "nccl" else "cpu"
-        t = torch.tensor([x], dtype=torch.float64, device=dev)
-        self.pg.all_reduce(t, op=self.pg.ReduceOp.MAX)
-        return float(t.item())
-
-    def close(self):
-        if self.pg is not None:
-            self.pg.destroy_process_group()
+def one_gpu_only(args) -> bool:
+    """The library runs on one GPU; a multi-GPU launch of the GEMM arm prints one
+    'unavailable' line (rank 0) and does no work on any rank.  True if so."""
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    if args.gpus <= 1 and world <= 1:
+        return False
+    if int(os.environ.get("RANK", "0")) == 0:
+        print(json.dumps({"metric": METRIC, "impl": "ours", "n_gpus": max(args.gpus, world),
+                          "unavailable": "one-GPU library: the GEMM runs on a single GPU and "
+                                         "has no multi-GPU path"}), flush=True)
+    return True
 
 
 class ClockSampler:
@@ -169,10 +151,11 @@ class ClockSampler:
                 "samples": len(rows), "power_w_max": max(power) if power else None}
 
 
-# Sources that build no kernel a GEMM launch runs (the int8 widening / fill /
-# empty kernels, the TMA intensity sweep, the CPython entry points): left out
-# of the digest.
-_DIGEST_SKIP = ("gemm_aux.cu", "tma_intensity.cu", "gemm_pycall.c")
+# Sources that build no kernel a sweep launch runs (the int8 widening / fill /
+# empty kernels, the TMA intensity sweep, the CPython entry points, the MMA
+# rate probe, the allocation-free entry point): left out of the digest.
+_DIGEST_SKIP = ("gemm_aux.cu", "tma_intensity.cu", "gemm_pycall.c", "gemm_probe.cu",
+                "gemm_noalloc.cu")
 
 
 def source_digest() -> str:
@@ -224,11 +207,10 @@ def run_step(items, stream):
         plan.run(A, B, C, stream)
 
 
-def time_sweep(items, dist, steps, warmup, stream, sampler=None):
+def time_sweep(items, steps, warmup, stream, sampler=None):
+    """Eager steps: one gemm_run per shape, timed with CUDA events on `stream`."""
     for _ in range(warmup):
         run_step(items, stream)
-    torch.cuda.synchronize()
-    dist.barrier()
     torch.cuda.synchronize()
     if sampler:
         sampler.start()
@@ -242,14 +224,12 @@ def time_sweep(items, dist, steps, warmup, stream, sampler=None):
     torch.cuda.synchronize()
     wall = time.perf_counter() - t0
     clocks = sampler.stop() if sampler else None
-    dist.barrier()
-    ms = e0.elapsed_time(e1)
-    return ms, wall, clocks
+    return e0.elapsed_time(e1), wall, clocks
 
 
 def capture_step(items, stream):
-    """One sweep step (all 343 gemm_run launches) captured as a CUDA graph: the
-    same kernels, parameters and buffers, replayed without per-launch host work."""
+    """One sweep step (all of `items`' gemm_run launches) captured as a CUDA graph:
+    the same kernels, parameters and buffers, replayed without per-launch host work."""
     graph = torch.cuda.CUDAGraph()
     with torch.cuda.graph(graph, stream=stream):
         run_step(items, stream)
@@ -257,12 +237,10 @@ def capture_step(items, stream):
     return graph
 
 
-def time_graph(graph, dist, steps, warmup, stream, sampler=None):
+def time_graph(graph, steps, warmup, stream, sampler=None):
     with torch.cuda.stream(stream):
         for _ in range(warmup):
             graph.replay()
-    torch.cuda.synchronize()
-    dist.barrier()
     torch.cuda.synchronize()
     if sampler:
         sampler.start()
@@ -277,7 +255,6 @@ def time_graph(graph, dist, steps, warmup, stream, sampler=None):
     torch.cuda.synchronize()
     wall = time.perf_counter() - t0
     clocks = sampler.stop() if sampler else None
-    dist.barrier()
     return e0.elapsed_time(e1), wall, clocks
 
 
@@ -434,10 +411,13 @@ def launch_floor_us(stream, sms, n=2000, graph=False):
     return e0.elapsed_time(e1) * 1e3 / n
 
 
-def named_workloads(stream, peaks, floor_us, sms):
+def named_workloads(stream, peaks, p_tensor, floor_us, sms, sm_max_mhz):
     """Warm µs/call (back-to-back on the same buffers, median of 5 repeats of a
-    >= 20 ms loop) and TFLOP/s with the roofline fraction for each named shape;
-    cold µs/call (L2 flushed before every call) for the two skinny shapes."""
+    >= 20 ms loop; >= 200 ms for the large shapes, with SM clocks sampled) and
+    TFLOP/s with the roofline fraction for each named shape; cold µs/call (L2
+    flushed before every call) for the two skinny shapes.  Large shapes also
+    report the throughput scaled to the maximum SM clock (x max / median sampled
+    clock), which separates a box's power-capped clock from the kernel."""
     import dense_gemm_hgemm_gb300 as g
     out = {}
     flush = torch.empty(512 * 1024 * 1024, dtype=torch.uint8, device="cuda")
@@ -452,6 +432,7 @@ def named_workloads(stream, peaks, floor_us, sms):
             A = (torch.randn(w.M, w.K, generator=gen, device="cuda") * w.a_scale).to(td)
             B = (torch.randn(w.N, w.K, generator=gen, device="cuda") * w.b_scale).to(td)
         C = torch.empty(w.M, w.N, device="cuda", dtype=inputs.OUT_DTYPE[w.dtype])
+        large = w.flops >= 1e11
         with g.Plan(w.M, w.N, w.K, w.dtype) as plan:
             for _ in range(20):
                 plan.run(A, B, C, stream)
@@ -463,7 +444,10 @@ def named_workloads(stream, peaks, floor_us, sms):
             e1.record(stream)
             torch.cuda.synchronize()
             one = max(e0.elapsed_time(e1), 1e-3)
-            reps = max(10, min(5000, int(20.0 / one)))
+            reps = max(10, min(5000, int((200.0 if large else 20.0) / one)))
+            sampler = ClockSampler(0) if large else None
+            if sampler:
+                sampler.start()
             samples = []
             for _ in range(5):
                 e0.record(stream)
@@ -472,6 +456,7 @@ def named_workloads(stream, peaks, floor_us, sms):
                 e1.record(stream)
                 torch.cuda.synchronize()
                 samples.append(e0.elapsed_time(e1) * 1e3 / reps)
+            clk = sampler.stop() if sampler else None
             us = statistics.median(samples)
             cold = None
             if w.flops < 1e9:
@@ -488,19 +473,23 @@ def named_workloads(stream, peaks, floor_us, sms):
             plan.check(stream)
             cfg = plan.config
         tflops = w.flops / (us * 1e-6) / 1e12
-        t_tensor = w.flops / (peaks["bf16_tflops"] * 1e12) * 1e6
+        t_tensor = w.flops / (p_tensor * 1e12) * 1e6
         t_hbm = w.compulsory_bytes / (peaks["hbm_gbs"] * 1e9) * 1e6
         t_roof = max(t_tensor, t_hbm, floor_us)
         bound = "tensor" if t_roof == t_tensor else ("hbm" if t_roof == t_hbm else "launch")
+        key = "TOPS" if w.dtype == "i8" else "TFLOPS"
         out[w.name] = {
             "M": w.M, "N": w.N, "K": w.K, "dtype": w.dtype, "us_per_call": round(us, 3),
             "us_per_call_cold_l2": round(cold, 3) if cold is not None else None,
-            ("TOPS" if w.dtype == "i8" else "TFLOPS"): round(tflops, 2),
+            key: round(tflops, 2),
             "roofline_bound": bound, "roofline_us": round(t_roof, 3),
             "roofline_frac": round(t_roof / us, 4),
-            "tensor_frac_of_measured_peak": round(tflops / peaks["bf16_tflops"], 4),
+            "frac_of_measured_burst_peak": round(tflops / peaks["bf16_tflops"], 4),
             "config": cfg,
         }
+        if clk and clk.get("sm_mhz"):
+            out[w.name]["clocks"] = clk
+            out[w.name][key + "_at_max_clock"] = round(tflops * sm_max_mhz / clk["sm_mhz"], 2)
         if w.dtype == "i8":
             out[w.name]["note"] = ("int8 runs on the fp16 tensor path (sm_103a has no tcgen05 "
                                    "kind::i8); peak is the fp16/bf16 rate")
@@ -572,7 +561,7 @@ def server_mode(stream, calls=2000):
     return out
 
 
-def cpu_oracle_sample(budget_s: float = 15.0, rows: int = 64):
+def cpu_oracle_sample(budget_s: float = 10.0, rows: int = 64):
     """Time the CPU oracle on rows [0, rows) of the sweep's shapes, in seeded
     random shape order, until `budget_s` seconds of work; TFLOP/s achieved."""
     import numpy as np
@@ -602,6 +591,55 @@ def cpu_oracle_sample(budget_s: float = 15.0, rows: int = 64):
                       "%.1f s" % (rows, done, flops, elapsed)}
 
 
+def _oracle_time(w, rows, threads):
+    """Seconds the oracle takes for rows [0, rows) of workload w (all of B)."""
+    import numpy as np
+
+    import oracle
+    A, B = inputs.make_operands(rows, w.N, w.K, w.dtype, w.a_scale, w.b_scale,
+                                seed=inputs.shape_seed(w.M, w.N, w.K, w.dtype))
+    if w.dtype == "i8":
+        a, b = A.numpy(), B.numpy()
+        t0 = time.perf_counter()
+        oracle.gemm_tn_i8(a, b, threads)
+    else:
+        a = A.view(torch.int16).numpy().view(np.uint16)
+        b = B.view(torch.int16).numpy().view(np.uint16)
+        t0 = time.perf_counter()
+        oracle.gemm_tn_half(a, b, oracle.FMT_BF16 if w.dtype == "bf16" else oracle.FMT_F16,
+                            threads)
+    return time.perf_counter() - t0
+
+
+def cpu_oracle_named(full_limit_s: float = 2.0, block_rows: int = 64):
+    """The oracle per named workload on the host cores: the full problem when a
+    64-row block predicts it under `full_limit_s`, else that row block timed and
+    extrapolated linearly in M (marked).  Plus one single-thread figure on the
+    sweep's headline shape 128x2048x128."""
+    import oracle
+    oracle.build()
+    threads = oracle.max_threads()
+    out = {}
+    for w in workloads.NAMED:
+        rows = min(block_rows, w.M)
+        t_blk = _oracle_time(w, rows, threads)
+        est = t_blk * w.M / rows
+        if rows < w.M and est <= full_limit_s:
+            rows, t_full, extrapolated = w.M, _oracle_time(w, w.M, threads), False
+        elif rows < w.M:
+            t_full, extrapolated = est, True
+        else:
+            t_full, extrapolated = t_blk, False
+        out[w.name] = {"seconds": round(t_full, 4), "extrapolated": extrapolated,
+                       "timed_rows": rows,
+                       ("TOPS" if w.dtype == "i8" else "TFLOPS"): round(w.flops / t_full / 1e12, 5)}
+    w = workloads.HEADLINE_SWEEP
+    t1 = _oracle_time(w, w.M, 1)
+    single = {"shape": [w.M, w.N, w.K, w.dtype], "cores": 1, "seconds": round(t1, 4),
+              "TFLOPS": round(w.flops / t1 / 1e12, 6)}
+    return out, single, threads
+
+
 def profile_one(spec, calls, stream):
     """`calls` launches of one shape with the table's configuration (for ncu)."""
     import dense_gemm_hgemm_gb300 as g
@@ -623,14 +661,37 @@ def profile_one(spec, calls, stream):
         print(json.dumps({"shape": [M, N, K, dtype], "config": plan.config, "calls": calls}))
 
 
+def mma_probe(sms, stream, iters=4096):
+    """tcgen05.mma issue rate (gemm_probe_mma_rate): dense FLOP per clock per SM
+    from one CTA alone and from one CTA on every SM (median over CTAs)."""
+    import dense_gemm_hgemm_gb300 as g
+    out = {}
+    for grid in (1, sms):
+        cyc = torch.zeros(grid, dtype=torch.int64, device="cuda")
+        ns = torch.zeros(grid, dtype=torch.int64, device="cuda")
+        err = torch.zeros(1, dtype=torch.int32, device="cuda")
+        for _ in range(3):
+            g.gemm_probe_mma_rate(grid, iters, cyc, ns, err, stream)
+        torch.cuda.synchronize()
+        if int(err.item()) != 0:
+            raise RuntimeError("gemm_probe_mma_rate: a completion wait ran out")
+        c = sorted(cyc.cpu().tolist())
+        t = sorted(ns.cpu().tolist())
+        med_c, med_t = c[len(c) // 2], t[len(t) // 2]
+        out["grid_%d" % grid] = {"flop_per_clk_per_sm": round(iters * 1048576 / med_c, 1),
+                                 "clock_mhz_seen": round(med_c / med_t * 1e3, 1)}
+    return out
+
+
 def ours(args):
-    dist = Dist()
-    torch.cuda.set_device(dist.local_rank)
+    if one_gpu_only(args):
+        return
+    torch.cuda.set_device(0)
     import dense_gemm_hgemm_gb300 as g
     g.build_library()
     peaks, peak_src = load_peaks()
     stream = torch.cuda.Stream()
-    sms = torch.cuda.get_device_properties(dist.local_rank).multi_processor_count
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
     if args.ncu_steps and args.shape:
         profile_one(args.shape, args.ncu_steps, stream)
         return
@@ -647,25 +708,23 @@ def ours(args):
             plan.check(stream)
         return
 
-    # Eager: one gemm_run (ctypes -> C ABI -> cudaLaunchKernelEx) per shape.
-    ms_e, wall_e, _ = time_sweep(items, dist, args.steps, args.warmup, stream)
+    # Eager: one Plan.run -> gemm_run per shape.
+    ms_e, _, _ = time_sweep(items, args.steps, args.warmup, stream)
     for _, plan, *_ in items:
         plan.check(stream)     # raises if any kernel gave up on a wait
-    ms_step_eager = dist.max(ms_e) / args.steps
+    ms_step_eager = ms_e / args.steps
     # Headline: the same step launched from a captured CUDA graph (the launch
     # overhead of 343 mostly tiny GEMMs is host work, not GEMM work).
     graph = capture_step(items, stream)
-    sampler = ClockSampler(dist.local_rank)
-    ms, wall, clocks = time_graph(graph, dist, args.steps, args.warmup, stream, sampler)
+    sampler = ClockSampler(0)
+    ms, wall, clocks = time_graph(graph, args.steps, args.warmup, stream, sampler)
     for _, plan, *_ in items:
         plan.check(stream)
-    ms_max = dist.max(ms)
-    ms_step = ms_max / args.steps
-    value = dist.world * flops_step / (ms_step * 1e-3) / 1e12
-    per_gpu = flops_step / (ms_step * 1e-3) / 1e12
+    ms_step = ms / args.steps
+    value = flops_step / (ms_step * 1e-3) / 1e12
 
     line = {
-        "metric": METRIC, "value": round(value, 3), "unit": UNIT, "n_gpus": dist.world,
+        "metric": METRIC, "value": round(value, 3), "unit": UNIT, "n_gpus": 1,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 4),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f16",
         "data": "synthetic (seeded N(0,1) fp16 operands per shape, generated on the device)",
@@ -673,67 +732,79 @@ def ours(args):
                    "compulsory_bytes_per_step": bytes_step,
                    "l2": "inputs larger than L2: each shape has its own A, B, C "
                          "(%.2f GB per step vs 129 MB L2); no explicit flush" % (bytes_step / 1e9),
-                   "replicas": dist.world, "layout": "TN", "accumulate": "fp32",
+                   "layout": "TN", "accumulate": "fp32",
                    "launch": "one step = the 343 gemm_run launches captured once as a CUDA "
                              "graph and replayed; eager = one gemm_run call per shape"},
-        "eager": {"value": round(dist.world * flops_step / (ms_step_eager * 1e-3) / 1e12, 3),
+        "eager": {"value": round(flops_step / (ms_step_eager * 1e-3) / 1e12, 3),
                   "unit": UNIT, "ms_per_step": round(ms_step_eager, 4)},
         "gpu_launches": len(items) * args.steps,
         "clocks": clocks,
         "wall_s_timed_region": round(wall, 3),
     }
+
+    # ---- roofline of the step: per shape max(tensor, HBM, launch floor), summed.
+    probe = mma_probe(sms, stream)
+    per_clk = probe["grid_%d" % sms]["flop_per_clk_per_sm"]
+    sm_max = (clocks or {}).get("sm_max_mhz") or 2070.0
+    theo = sms * sm_max * 1e6 * per_clk / 1e12
+    p_tensor = max(theo, peaks["bf16_tflops"])          # the stricter denominator
+    floor_graph = launch_floor_us(stream, sms, graph=True)
+    classes = {}
+    t_roof = 0.0
+    t_roof_meas = 0.0
+    for item in items:
+        w = item[0]
+        tt = w.flops / (p_tensor * 1e12) * 1e6
+        th = w.compulsory_bytes / (peaks["hbm_gbs"] * 1e9) * 1e6
+        tr = max(tt, th, floor_graph)
+        t_roof += tr
+        t_roof_meas += max(w.flops / (peaks["bf16_tflops"] * 1e12) * 1e6, th, floor_graph)
+        kind = "tensor" if tr == tt else ("hbm" if tr == th else "launch")
+        c = classes.setdefault(kind, {"shapes": 0, "t_roof_us": 0.0, "items": []})
+        c["shapes"] += 1
+        c["t_roof_us"] += tr
+        c["items"].append(item)
+    for kind, c in classes.items():
+        # each class's shapes alone, in sweep order, as one graph (same launch regime)
+        sub = capture_step(c.pop("items"), stream)
+        ms_c, _, _ = time_graph(sub, max(5, args.steps), 3, stream)
+        c["t_graph_us"] = round(ms_c * 1e3 / max(5, args.steps), 1)
+        c["frac"] = round(c["t_roof_us"] / c["t_graph_us"], 4)
+        c["t_roof_us"] = round(c["t_roof_us"], 1)
+        del sub
     traffic, traffic_note = stored_traffic()
     line["roofline"] = {
-        "bound": "tensor", "achieved": round(per_gpu, 2),
-        "peak": peaks["bf16_tflops_sustained"], "unit": "TFLOP/s",
-        "frac": round(per_gpu / peaks["bf16_tflops_sustained"], 4),
+        "bound": "mixed",
+        "achieved": round(value, 2),
+        "peak": round(flops_step / (t_roof * 1e-6) / 1e12, 2),
+        "unit": "TFLOP/s",
+        "frac": round(t_roof / (ms_step * 1e3), 4),
         "traffic": traffic,
-        "peak_source": "bf16_tflops_sustained of %s (fp16 dense rate equals bf16)" % peak_src,
-        "frac_of_burst_peak": round(per_gpu / peaks["bf16_tflops"], 4),
-        "kernel": "gemm_tn_kernel (all sweep launches; average launch = step/343)",
+        "rule": "per shape t_roof = max(2MNK / tensor peak, compulsory bytes / HBM, launch "
+                "floor); peak = step FLOP / sum t_roof (the throughput the 343-shape mix "
+                "allows), frac = sum t_roof / timed step = achieved / peak",
+        "tensor_peak_tflops": round(p_tensor, 1),
+        "tensor_peak_source": "stricter of measured bf16 burst (%s, %.1f) and theoretical "
+                              "%d SMs x %.0f MHz x %.1f FLOP/clk/SM (tcgen05 issue-rate probe, "
+                              "%.1f)" % (peak_src, peaks["bf16_tflops"], sms, sm_max, per_clk, theo),
+        "hbm_gbs": peaks["hbm_gbs"],
+        "launch_floor_graph_us": round(floor_graph, 3),
+        "frac_with_measured_tensor_peak": round(t_roof_meas / (ms_step * 1e3), 4),
+        "frac_of_tensor_peak": round(value / p_tensor, 4),
+        "by_class": classes,
         "traffic_note": traffic_note,
+        "mma_probe": probe,
     }
 
-    if not args.skip_extras and dist.rank == 0:
+    if not args.skip_extras:
         floor = launch_floor_us(stream, sms)
-        floor_graph = launch_floor_us(stream, sms, graph=True)
         times = per_shape_times(items, stream)
-        t_meas = t_roof = t_roof_graph = 0.0
-        classes = {}
-        for w, *_ in items:
-            us = times[w.name] * 1e3
-            tt = w.flops / (peaks["bf16_tflops"] * 1e12) * 1e6
-            th = w.compulsory_bytes / (peaks["hbm_gbs"] * 1e9) * 1e6
-            tr = max(tt, th, floor)
-            t_roof_graph += max(tt, th, floor_graph)
-            kind = "tensor" if tr == tt else ("hbm" if tr == th else "launch")
-            c = classes.setdefault(kind, {"shapes": 0, "t_meas_us": 0.0, "t_roof_us": 0.0})
-            c["shapes"] += 1
-            c["t_meas_us"] += us
-            c["t_roof_us"] += tr
-            t_meas += us
-            t_roof += tr
-        for c in classes.values():
-            c["frac"] = round(c["t_roof_us"] / c["t_meas_us"], 4)
-            c["t_meas_us"] = round(c["t_meas_us"], 1)
-            c["t_roof_us"] = round(c["t_roof_us"], 1)
-        head = workloads.HEADLINE_SWEEP.name.replace("hgemm_tn_", "sweep_").replace("_f16", "_f16")
-        line["sweep_roofline"] = {
-            "launch_floor_us": round(floor, 3),
-            "launch_floor_graph_us": round(floor_graph, 3),
-            "t_roof_us_sum": round(t_roof_graph, 1),
-            "frac_of_timed_step": round(t_roof_graph / (ms_step * 1e3), 4),
-            "t_roof_us_sum_eager_floor": round(t_roof, 1),
-            "frac_of_eager_step": round(t_roof / (ms_step_eager * 1e3), 4),
-            "t_meas_us_sum_isolated": round(t_meas, 1),
-            "frac_isolated": round(t_roof / t_meas, 4), "by_bound_isolated": classes,
-            "rule": "per shape t_roof = max(2MNK/bf16 burst peak, compulsory bytes/HBM, "
-                    "launch floor of an empty kernel launched like the GEMM: from a graph "
-                    "for the timed (graph) step, one call at a time for the eager step and "
-                    "the isolated times); frac_of_timed_step = sum t_roof / timed "
-                    "ms_per_step; *_isolated = each launch timed alone between events (no "
-                    "launch overlap)",
-            "headline_128x2048x128_us_in_sweep": round(times.get("sweep_128x2048x128_f16", 0) * 1e3, 3),
+        line["sweep_isolated"] = {
+            "launch_floor_eager_us": round(floor, 3),
+            "t_meas_us_sum": round(sum(times.values()) * 1e3, 1),
+            "headline_128x2048x128_us": round(times.get("sweep_128x2048x128_f16", 0) * 1e3, 3),
+            "skinny_64x4096x64_us": round(times.get("sweep_64x4096x64_f16", 0) * 1e3, 3),
+            "note": "each launch alone between CUDA events (no launch overlap)",
         }
         e2e_ms, h2d, d2h, copy_ms = e2e_sweep(items, stream, steps=max(3, min(20, args.steps)))
         line["e2e"] = {"value": round(flops_step / (e2e_ms * 1e-3) / 1e12, 3), "unit": UNIT,
@@ -749,12 +820,18 @@ def ours(args):
             plan.close()
         del items
         torch.cuda.empty_cache()
-        line["named"] = named_workloads(stream, peaks, floor, sms)
+        line["named"] = named_workloads(stream, peaks, p_tensor, floor, sms,
+                                        (clocks or {}).get("sm_max_mhz") or 2070.0)
         line["server_mode"] = server_mode(stream)
-        line["cpu_baseline"] = cpu_oracle_sample()
-    if dist.rank == 0:
-        print(json.dumps(line), flush=True)
-    dist.close()
+        cpu = cpu_oracle_sample()
+        named_cpu, single, threads = cpu_oracle_named()
+        cpu["single_thread_headline"] = single
+        cpu["named"] = named_cpu
+        cpu["note"] = ("the oracle as it stands (fp64, plain i-j-k loop, rows over %d host "
+                       "threads); named: full problem where it takes under 2 s, else a 64-row "
+                       "block extrapolated linearly in M" % threads)
+        line["cpu_baseline"] = cpu
+    print(json.dumps(line), flush=True)
 
 
 # --------------------------------------------------------------------------- reference arm
