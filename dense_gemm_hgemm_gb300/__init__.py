@@ -24,7 +24,8 @@ __all__ = [
     "gemm_plan_set_timeout",
     "gemm_plan_set_wait_test",
     "gemm_select_config", "gemm_tile_coords", "gemm_workspace_bytes", "gemm_status_string",
-    "gemm_abi_version", "gemm_launch_empty", "gemm_run_splitk_noalloc", "library", "DTYPES",
+    "gemm_abi_version", "gemm_launch_empty", "gemm_run_splitk_noalloc", "gemm_noalloc_check",
+    "gemm_noalloc_set_wait_test", "gemm_probe_mma_rate", "library", "DTYPES",
 ]
 
 GEMM_F16, GEMM_BF16, GEMM_I8_I32 = 0, 1, 2
@@ -104,6 +105,9 @@ def library() -> ctypes.CDLL:
                 "gemm_abi_version": ([], i32),
                 "gemm_launch_empty": ([i32, vp], i32),
                 "gemm_run_splitk_noalloc": ([i64, i64, i64, i32, i32, vp, vp, vp, vp], i32),
+                "gemm_noalloc_check": ([vp], i32),
+                "gemm_noalloc_set_wait_test": ([ctypes.c_uint32, ctypes.c_uint64], i32),
+                "gemm_probe_mma_rate": ([i32, i32, vp, vp, vp, vp], i32),
                 "tma_intensity_run": ([i32, i32, ctypes.c_float, ctypes.c_float, vp, vp, i64, i32,
                                        vp, vp], i32),
             }
@@ -191,6 +195,26 @@ def gemm_run_splitk_noalloc(M: int, N: int, K: int, dtype, split_k: int, A, B, C
     _check(library().gemm_run_splitk_noalloc(M, N, K, _dtype_code(dtype), int(split_k), _ptr(A),
                                              _ptr(B), _ptr(C), _stream(stream)),
            "gemm_run_splitk_noalloc")
+
+
+def gemm_noalloc_check(stream=None) -> None:
+    """Synchronise `stream`; raise GemmError(GEMM_ERR_DEVICE_TIMEOUT) if a no-alloc call
+    since the last check gave up on a wait (the record is cleared by this call)."""
+    _check(library().gemm_noalloc_check(_stream(stream)), "gemm_noalloc_check")
+
+
+def gemm_noalloc_set_wait_test(extra_bytes: int, timeout_ns: int = 0) -> None:
+    """Failure-test hook of the no-alloc path (process-wide): ring slots wait for
+    `extra_bytes` that never arrive; 0 restores normal operation."""
+    _check(library().gemm_noalloc_set_wait_test(int(extra_bytes), int(timeout_ns)),
+           "gemm_noalloc_set_wait_test")
+
+
+def gemm_probe_mma_rate(grid: int, iters: int, cycles, ns, error_word, stream=None) -> None:
+    """Back-to-back tcgen05.mma (M=128, N=256, K=16) issue-rate probe: per CTA, SM cycles
+    and ns from the first issue to completion (see include/gemm_probe.h)."""
+    _check(library().gemm_probe_mma_rate(int(grid), int(iters), _ptr(cycles), _ptr(ns),
+                                         _ptr(error_word), _stream(stream)), "gemm_probe_mma_rate")
 
 
 TMA_MODES = {"sync": 0, "bulk1d": 1, "tensor2d": 2, "pipe2": 3}

@@ -17,9 +17,11 @@
 // device (with that device current) asks the runtime for the address with
 // cudaGetSymbolAddress and caches it; make that first call before any stream
 // capture.  All calls share the array and it keeps the last call's contents:
-// each call clears the error word and split-K counters on its stream before
-// the kernel runs (the partials are fully written before they are read), and
-// calls whose kernels overlap on the GPU race on the array.
+// each call clears the split-K counters on its stream before the kernel runs
+// (the partials are fully written before they are read), and calls whose
+// kernels overlap on the GPU race on the array.  The error word is not cleared
+// by a call: a wait that ran out stays recorded until gemm_noalloc_check reads
+// and clears it, so one check after several calls sees a failure in any of them.
 //
 // Nothing here calls cudaMalloc, cudaFree or an allocating library routine.
 #include <cuda.h>
@@ -28,6 +30,7 @@
 #include <stdint.h>
 #include <string.h>
 
+#include <atomic>
 #include <mutex>
 
 #include "gemm.h"
@@ -54,8 +57,14 @@ struct DeviceSetup {
     gemm_status_t status = GEMM_ERR_CUDA;
     unsigned char* scratch = nullptr;
     int num_sms = 0;
+    std::atomic<int> ready{0};   // 1 once the set-up succeeded (read without the once flag)
 };
 DeviceSetup g_setup[kMaxDevices];
+
+// Failure-test hook (gemm_noalloc_set_wait_test): extra bytes every ring slot
+// waits for, and the wait limit.  Process-wide; 0 = normal operation.
+uint32_t g_wait_test_bytes = 0;
+uint64_t g_timeout_ns = kTimeoutNs;
 
 template <int OUT>
 cudaError_t allow_smem() {
@@ -82,6 +91,7 @@ void setup_device(int dev, DeviceSetup* s) {
     s->scratch = static_cast<unsigned char*>(ptr);
     s->num_sms = sms;
     s->status = GEMM_OK;
+    s->ready.store(1, std::memory_order_release);
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_entry() {
@@ -178,8 +188,10 @@ extern "C" gemm_status_t gemm_run_splitk_noalloc(int64_t M, int64_t N, int64_t K
         return GEMM_OK;
     }
 
-    // Error word and split-K counters start at zero for this call.
-    if (cudaMemsetAsync(su.scratch, 0, kPartialsOff, stream) != cudaSuccess) {
+    // Split-K counters start at zero for this call (the error word is sticky
+    // until gemm_noalloc_check).
+    if (cudaMemsetAsync(su.scratch + kCountersOff, 0, kPartialsOff - kCountersOff, stream) !=
+        cudaSuccess) {
         cudaGetLastError();
         return GEMM_ERR_CUDA;
     }
@@ -209,12 +221,12 @@ extern "C" gemm_status_t gemm_run_splitk_noalloc(int64_t M, int64_t N, int64_t K
     kp.idesc = (1u << 4) | (fmt << 7) | (fmt << 10) |
                (static_cast<uint32_t>(kBlockN >> 3) << 17) |
                (static_cast<uint32_t>(gbg::kBM >> 4) << 24);
-    kp.tx_extra = 0;
+    kp.tx_extra = g_wait_test_bytes;
     kp.C = C;
     kp.workspace = su.scratch + kPartialsOff;
     kp.counters = reinterpret_cast<uint32_t*>(su.scratch + kCountersOff);
     kp.error_word = reinterpret_cast<int32_t*>(su.scratch + kErrorOff);
-    kp.timeout_ns = kTimeoutNs;
+    kp.timeout_ns = g_timeout_ns;
 
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(kp.num_units < su.num_sms ? kp.num_units : su.num_sms));
@@ -231,5 +243,43 @@ extern "C" gemm_status_t gemm_run_splitk_noalloc(int64_t M, int64_t N, int64_t K
         cudaGetLastError();
         return GEMM_ERR_LAUNCH;
     }
+    return GEMM_OK;
+}
+
+extern "C" gemm_status_t gemm_noalloc_check(void* stream_ptr) {
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess) {
+        cudaGetLastError();
+        return GEMM_ERR_NO_DEVICE;
+    }
+    if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream_ptr)) != cudaSuccess) {
+        cudaGetLastError();
+        return GEMM_ERR_CUDA;
+    }
+    if (dev < 0 || dev >= kMaxDevices) return GEMM_ERR_UNSUPPORTED;
+    DeviceSetup& su = g_setup[dev];
+    // No call has run on this device yet (the set-up of the first call is what
+    // resolves the array's address): nothing can have failed.
+    if (su.ready.load(std::memory_order_acquire) == 0) return GEMM_OK;
+    int32_t word = 0;
+    if (cudaMemcpy(&word, su.scratch + kErrorOff, sizeof(word), cudaMemcpyDeviceToHost) !=
+        cudaSuccess) {
+        cudaGetLastError();
+        return GEMM_ERR_CUDA;
+    }
+    if (word == 0) return GEMM_OK;
+    const int32_t zero = 0;
+    if (cudaMemcpy(su.scratch + kErrorOff, &zero, sizeof(zero), cudaMemcpyHostToDevice) !=
+        cudaSuccess) {
+        cudaGetLastError();
+        return GEMM_ERR_CUDA;
+    }
+    return GEMM_ERR_DEVICE_TIMEOUT;
+}
+
+extern "C" gemm_status_t gemm_noalloc_set_wait_test(uint32_t extra_bytes, uint64_t timeout_ns) {
+    if (extra_bytes > 4096 || (extra_bytes & 15u)) return GEMM_ERR_INVALID_ARG;
+    g_wait_test_bytes = extra_bytes;
+    g_timeout_ns = timeout_ns ? timeout_ns : kTimeoutNs;
     return GEMM_OK;
 }

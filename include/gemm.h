@@ -106,11 +106,13 @@ typedef enum {
  *                  adjacent N-tiles of the same rows, each loading 1/multicast
  *                  of the shared A tile and multicasting it to the others
  *                  (one-SM kernel, split_k 1; 4 needs A stored M x K)
- *   kblocks_per_stage : 0 = the table's choice; 1 or 2 = 64-wide k-blocks per
- *                  ring slot.  2: one-SM kernel with block_n 64 or 128 or the
- *                  SM-pair kernel, no multicast, and K % 64 == 0 when an
- *                  operand is K-contiguous; each operand's two k-blocks arrive
- *                  in one copy per 64-element block
+ *   kblocks_per_stage : 0 = the table's choice; 1, 2 or 4 = 64-wide k-blocks
+ *                  per ring slot.  2: one-SM kernel with block_n 64 or 128 or
+ *                  the SM-pair kernel; 4: one-SM kernel with block_n 64 or the
+ *                  SM-pair kernel with block_n 128 (two slots).  Both need no
+ *                  multicast and K % 64 == 0 when an operand is K-contiguous;
+ *                  each operand's k-blocks of a slot arrive in one copy per
+ *                  64-element block
  *   l2_prefetch  : 0 = off; d in 1..64 = while loading k-block kb, also ask L2
  *                  to fetch k-block kb + d of the same tile (hides DRAM latency
  *                  on long K)
@@ -279,15 +281,37 @@ gemm_status_t gemm_launch_empty(int32_t grid, void *stream);
  * loaded, until the process exits.  The first call on a device (that device
  * current) looks up the array's device address (cudaGetSymbolAddress) and
  * prepares the kernel; make it before any stream capture.  Every call clears
- * the array's error word and counters on `stream`; all calls share the one
- * array, so calls whose work overlaps on the GPU (different streams, or
- * different host threads) race and must be serialised by the caller.  A wait
- * that runs out is recorded in the array's error word only (no plan to check).
- * Calls no cudaMalloc, cudaFree or allocating library routine.
+ * the array's split-K counters on `stream`; all calls share the one array, so
+ * calls whose work overlaps on the GPU (different streams, or different host
+ * threads) race and must be serialised by the caller.  A wait that runs out
+ * sets the array's error word, which no call clears: gemm_noalloc_check
+ * reports and clears it.  Calls no cudaMalloc, cudaFree or allocating library
+ * routine.
  */
 gemm_status_t gemm_run_splitk_noalloc(int64_t M, int64_t N, int64_t K, gemm_dtype_t dtype,
                                       int32_t split_k, const void *A, const void *B, void *C,
                                       void *stream);
+
+/*
+ * The failure report of gemm_run_splitk_noalloc on the current device (no
+ * counterpart on the pages; the no-alloc path has no plan whose error word
+ * gemm_plan_check could read).  Synchronises `stream`, then reads and clears
+ * the fixed array's error word: GEMM_ERR_DEVICE_TIMEOUT if a kernel of any
+ * no-alloc call since the last check gave up on a wait (its C is then
+ * undefined), GEMM_ERR_CUDA if the stream or the read failed, else GEMM_OK
+ * (also when no no-alloc call has run on this device).  Allocates nothing.
+ */
+gemm_status_t gemm_noalloc_check(void *stream);
+
+/*
+ * Failure-test hook of gemm_run_splitk_noalloc, process-wide (no counterpart on
+ * the pages): later no-alloc calls make every ring slot wait for `extra_bytes`
+ * (a multiple of 16, at most 4096) more than its copies deliver, so the slot
+ * never completes and the kernel's bounded wait runs out after `timeout_ns`
+ * (0 = the default 2 s); the kernel unwinds, frees its TMEM and records the
+ * failure for gemm_noalloc_check.  extra_bytes = 0 restores normal operation.
+ */
+gemm_status_t gemm_noalloc_set_wait_test(uint32_t extra_bytes, uint64_t timeout_ns);
 
 #ifdef __cplusplus
 }
