@@ -99,8 +99,12 @@ gemm_status_t normalise_config(int64_t M, int64_t N, int64_t K, gemm_dtype_t dty
     if (c.multicast != 0 && c.multicast != 2 && c.multicast != 4) return GEMM_ERR_INVALID_ARG;
     if (c.l2_prefetch < 0 || c.l2_prefetch > 64) return GEMM_ERR_INVALID_ARG;
     if (c.kblocks_per_stage == 0) c.kblocks_per_stage = 1;
-    if (c.kblocks_per_stage != 1 && c.kblocks_per_stage != 2) return GEMM_ERR_INVALID_ARG;
-    if (c.kblocks_per_stage == 2 && ((!c.cta_pair && c.block_n > 128) || c.multicast > 1))
+    if (c.kblocks_per_stage != 1 && c.kblocks_per_stage != 2 && c.kblocks_per_stage != 4)
+        return GEMM_ERR_INVALID_ARG;
+    if (c.kblocks_per_stage > 1 && c.multicast > 1) return GEMM_ERR_INVALID_ARG;
+    if (c.kblocks_per_stage == 2 && !c.cta_pair && c.block_n > 128) return GEMM_ERR_INVALID_ARG;
+    // four k-blocks per slot: two 96 KiB slots, one-SM 64-wide or SM-pair 128-wide tiles
+    if (c.kblocks_per_stage == 4 && c.block_n != (c.cta_pair ? 128 : 64))
         return GEMM_ERR_INVALID_ARG;
     if (c.cta_pair) {
         // SM pair: 256-row tiles; K is sliced only across the pairs of a cluster.
@@ -108,11 +112,7 @@ gemm_status_t normalise_config(int64_t M, int64_t N, int64_t K, gemm_dtype_t dty
         if (dtype == GEMM_I8_I32 && c.block_n != 128) return GEMM_ERR_INVALID_ARG;
         if (c.split_k != 1 && c.split_mode != 1) return GEMM_ERR_INVALID_ARG;
     }
-    const bool ks2 = c.kblocks_per_stage == 2;
-    const int want_stages = c.cta_pair ? (ks2 ? gbg::default_pair_stages_ks2(c.block_n)
-                                              : gbg::default_pair_stages(c.block_n))
-                                       : (ks2 ? gbg::default_stages_ks2(c.block_n)
-                                              : gbg::default_stages(c.block_n));
+    const int want_stages = gbg::default_ring_stages(c.cta_pair, c.block_n, c.kblocks_per_stage);
     if (c.stages == 0) c.stages = want_stages;
     if (c.stages != want_stages) return GEMM_ERR_INVALID_ARG;
     if (c.split_k < 1 || c.raster_group < 1 || c.max_ctas < 0) return GEMM_ERR_INVALID_ARG;
@@ -293,10 +293,10 @@ gemm_status_t create_plan(int64_t M, int64_t N, int64_t K, gemm_dtype_t dtype,
     if (st != GEMM_OK) return st;
     // A stored K x M is copied in 64-column blocks: at most two multicast slices
     if (user_cfg && user_cfg->multicast > 2 && a_mn_major(layout)) return GEMM_ERR_INVALID_ARG;
-    // two k-blocks per slot of a K-contiguous operand come from its 3-D view,
+    // several k-blocks per slot of a K-contiguous operand come from its 3-D view,
     // which needs K % 64 == 0
     const bool some_k_major = !a_mn_major(layout) || !b_mn_major(layout);
-    if (user_cfg && user_cfg->kblocks_per_stage == 2 && some_k_major && K % gbg::kBK != 0)
+    if (user_cfg && user_cfg->kblocks_per_stage > 1 && some_k_major && K % gbg::kBK != 0)
         return GEMM_ERR_INVALID_ARG;
     if (user_cfg) {
         gemm_config_t tmp;
@@ -310,7 +310,7 @@ gemm_status_t create_plan(int64_t M, int64_t N, int64_t K, gemm_dtype_t dtype,
 
     gemm_config_t want = user_cfg ? *user_cfg : gbg::select_config(M, N, K, dtype, sms);
     if (want.multicast > 2 && a_mn_major(layout)) want.multicast = 2;
-    if (want.kblocks_per_stage == 2 && some_k_major && K % gbg::kBK != 0) {
+    if (want.kblocks_per_stage > 1 && some_k_major && K % gbg::kBK != 0) {
         want.kblocks_per_stage = 1;
         want.stages = 0;
     }
@@ -350,12 +350,7 @@ gemm_status_t create_plan(int64_t M, int64_t N, int64_t K, gemm_dtype_t dtype,
 
     size_t smem = 0;
     const cudaError_t prep =
-        cfg.cta_pair ? (p->out_kind == gbg::kOutF16
-                            ? gbg::gemm_prepare_pair_f16(cfg.block_n, cfg.stages, &smem)
-                        : p->out_kind == gbg::kOutBF16
-                            ? gbg::gemm_prepare_pair_bf16(cfg.block_n, cfg.stages, &smem)
-                            : gbg::gemm_prepare_pair_i32(cfg.block_n, cfg.stages, &smem))
-                     : gbg::gemm_prepare(cfg.block_n, cfg.stages, p->out_kind, &smem);
+        gbg::gemm_prepare(cfg.block_n, cfg.stages, p->out_kind, cfg.cta_pair, &smem);
     if (prep != cudaSuccess) {
         cudaGetLastError();
         cudaFree(p->dmem);
@@ -458,20 +453,20 @@ gemm_status_t create_plan(int64_t M, int64_t N, int64_t K, gemm_dtype_t dtype,
 
 namespace gbg {
 
-cudaError_t gemm_prepare(int bn, int stages, int out, size_t* smem_bytes) {
+cudaError_t gemm_prepare(int bn, int stages, int out, int pair, size_t* smem_bytes) {
     switch (out) {
-        case kOutF16: return gemm_prepare_f16(bn, stages, smem_bytes);
-        case kOutBF16: return gemm_prepare_bf16(bn, stages, smem_bytes);
-        case kOutI32: return gemm_prepare_i32(bn, stages, smem_bytes);
+        case kOutF16: return gemm_prepare_out<kOutF16>(bn, stages, pair, smem_bytes);
+        case kOutBF16: return gemm_prepare_out<kOutBF16>(bn, stages, pair, smem_bytes);
+        case kOutI32: return gemm_prepare_out<kOutI32>(bn, stages, pair, smem_bytes);
         default: return cudaErrorInvalidValue;
     }
 }
 
 cudaError_t gemm_max_clusters(int bn, int stages, int out, int pair, const LaunchShape& shape,
                               int* n) {
-    const void* fn = out == kOutF16    ? gemm_kernel_ptr_f16(bn, stages, pair)
-                     : out == kOutBF16 ? gemm_kernel_ptr_bf16(bn, stages, pair)
-                     : out == kOutI32  ? gemm_kernel_ptr_i32(bn, stages, pair)
+    const void* fn = out == kOutF16    ? gemm_kernel_ptr_out<kOutF16>(bn, stages, pair)
+                     : out == kOutBF16 ? gemm_kernel_ptr_out<kOutBF16>(bn, stages, pair)
+                     : out == kOutI32  ? gemm_kernel_ptr_out<kOutI32>(bn, stages, pair)
                                        : nullptr;
     if (!fn) return cudaErrorInvalidValue;
     cudaLaunchConfig_t cfg = {};
@@ -488,13 +483,13 @@ cudaError_t gemm_max_clusters(int bn, int stages, int out, int pair, const Launc
     return cudaOccupancyMaxActiveClusters(n, fn, &cfg);
 }
 
-cudaError_t gemm_launch(int bn, int stages, int out, const LaunchShape& shape,
+cudaError_t gemm_launch(int bn, int stages, int out, int pair, const LaunchShape& shape,
                         const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& c,
                         const KParams& p, cudaStream_t stream) {
     switch (out) {
-        case kOutF16: return gemm_launch_f16(bn, stages, shape, a, b, c, p, stream);
-        case kOutBF16: return gemm_launch_bf16(bn, stages, shape, a, b, c, p, stream);
-        case kOutI32: return gemm_launch_i32(bn, stages, shape, a, b, c, p, stream);
+        case kOutF16: return gemm_launch_out<kOutF16>(bn, stages, pair, shape, a, b, c, p, stream);
+        case kOutBF16: return gemm_launch_out<kOutBF16>(bn, stages, pair, shape, a, b, c, p, stream);
+        case kOutI32: return gemm_launch_out<kOutI32>(bn, stages, pair, shape, a, b, c, p, stream);
         default: return cudaErrorInvalidValue;
     }
 }
@@ -592,19 +587,9 @@ gemm_status_t gemm_run_bias_act(gemm_plan_t p, const void* A, const void* B, voi
     p->kp.C = C;
     p->kp.bias = bias;
     p->kp.act = static_cast<int32_t>(act);
-    cudaError_t e;
-    if (p->cfg.cta_pair)
-        e = p->out_kind == gbg::kOutF16
-                ? gbg::gemm_launch_pair_f16(p->cfg.block_n, p->cfg.stages, p->shape, p->map_a,
-                                            p->map_b, p->map_c, p->kp, stream)
-            : p->out_kind == gbg::kOutBF16
-                ? gbg::gemm_launch_pair_bf16(p->cfg.block_n, p->cfg.stages, p->shape, p->map_a,
-                                             p->map_b, p->map_c, p->kp, stream)
-                : gbg::gemm_launch_pair_i32(p->cfg.block_n, p->cfg.stages, p->shape, p->map_a,
-                                            p->map_b, p->map_c, p->kp, stream);
-    else
-        e = gbg::gemm_launch(p->cfg.block_n, p->cfg.stages, p->out_kind, p->shape, p->map_a,
-                             p->map_b, p->map_c, p->kp, stream);
+    const cudaError_t e = gbg::gemm_launch(p->cfg.block_n, p->cfg.stages, p->out_kind,
+                                           p->cfg.cta_pair, p->shape, p->map_a, p->map_b,
+                                           p->map_c, p->kp, stream);
     if (e != cudaSuccess) {
         cudaGetLastError();
         return GEMM_ERR_LAUNCH;

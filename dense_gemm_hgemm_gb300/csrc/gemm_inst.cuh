@@ -1,0 +1,148 @@
+// gemm_inst.cuh -- the kernel variants and their launchers, one template per
+// output type (gemm_inst_f16.cu, gemm_inst_bf16.cu and gemm_inst_i32.cu each
+// instantiate it once, so the three compile in parallel).
+//
+// A variant is (tile width BN, ring depth STAGES, k-blocks per slot KS) of the
+// one-SM kernel or of the SM-pair kernel; (BN, STAGES) identifies it, because
+// every KS has its own depth for a given BN.  The integer output mode keeps BN int32 sums per
+// thread in registers, so it has the narrower variants only.
+#pragma once
+
+#include "gemm_kernel.cuh"
+#include "gemm_kernel_2cta.cuh"
+#include "gemm_launch.h"
+
+// X(BN, STAGES, KS) for every variant of each kernel.
+#define GBG_ONE_SM_VARIANTS(X) \
+    X(64, 8, 1) X(128, 6, 1) X(256, 4, 1) X(64, 4, 2) X(128, 3, 2) X(64, 2, 4)
+#define GBG_PAIR_VARIANTS(X) X(256, 6, 1) X(128, 8, 1) X(256, 3, 2) X(128, 4, 2) X(128, 2, 4)
+
+namespace gbg {
+namespace inst {
+
+template <int OUT, int BN>
+constexpr bool one_sm_ok() { return OUT != kOutI32 || BN <= 128; }
+template <int OUT, int BN>
+constexpr bool pair_ok() { return OUT != kOutI32 || BN == 128; }
+
+template <bool PAIR, int BN, int STAGES, int OUT, int KS>
+const void* kernel_fn() {
+    if constexpr (PAIR)
+        return reinterpret_cast<const void*>(gemm_tn_pair_kernel<BN, STAGES, OUT, KS>);
+    else
+        return reinterpret_cast<const void*>(gemm_tn_kernel<BN, STAGES, OUT, KS>);
+}
+
+template <bool PAIR, int BN, int STAGES, int KS>
+constexpr size_t smem_bytes() {
+    if constexpr (PAIR)
+        return SmemLayout2<BN, STAGES, KS>::kTotal;
+    else
+        return SmemLayout<BN, STAGES, KS>::kTotal;
+}
+
+template <bool PAIR, int BN, int STAGES, int OUT, int KS>
+cudaError_t prepare(size_t* smem) {
+    *smem = smem_bytes<PAIR, BN, STAGES, KS>();
+    if constexpr (PAIR)
+        return cudaFuncSetAttribute(gemm_tn_pair_kernel<BN, STAGES, OUT, KS>,
+                                    cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    static_cast<int>(*smem));
+    else
+        return cudaFuncSetAttribute(gemm_tn_kernel<BN, STAGES, OUT, KS>,
+                                    cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    static_cast<int>(*smem));
+}
+
+// Programmatic dependent launch on every launch: the kernel's set-up may overlap
+// the tail of the previous kernel in the stream (it waits with
+// griddepcontrol.wait before touching global memory).  Clusters: SM pairs,
+// split-K slices of a tile, or CTAs sharing an A tile by multicast.
+template <bool PAIR, int BN, int STAGES, int OUT, int KS>
+cudaError_t launch(const LaunchShape& s, const CUtensorMap& a, const CUtensorMap& b,
+                   const CUtensorMap& c, const KParams& p, cudaStream_t stream) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(s.grid));
+    cfg.blockDim = dim3(static_cast<unsigned>(s.block));
+    cfg.dynamicSmemBytes = s.smem_bytes;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    unsigned n = 1;
+    if (PAIR || s.cluster > 1) {
+        attr[1].id = cudaLaunchAttributeClusterDimension;
+        attr[1].val.clusterDim.x = static_cast<unsigned>(s.cluster);
+        attr[1].val.clusterDim.y = 1;
+        attr[1].val.clusterDim.z = 1;
+        n = 2;
+    }
+    cfg.attrs = attr;
+    cfg.numAttrs = n;
+    if constexpr (PAIR)
+        return cudaLaunchKernelEx(&cfg, gemm_tn_pair_kernel<BN, STAGES, OUT, KS>, a, b, c, p);
+    else
+        return cudaLaunchKernelEx(&cfg, gemm_tn_kernel<BN, STAGES, OUT, KS>, a, b, c, p);
+}
+
+}  // namespace inst
+
+template <int OUT>
+cudaError_t gemm_prepare_out(int bn, int stages, int pair, size_t* smem) {
+#define X(B, S, K)                                                          \
+    if constexpr (inst::one_sm_ok<OUT, B>())                                \
+        if (!pair && bn == B && stages == S) return inst::prepare<false, B, S, OUT, K>(smem);
+    GBG_ONE_SM_VARIANTS(X)
+#undef X
+#define X(B, S, K)                                                          \
+    if constexpr (inst::pair_ok<OUT, B>())                                  \
+        if (pair && bn == B && stages == S) return inst::prepare<true, B, S, OUT, K>(smem);
+    GBG_PAIR_VARIANTS(X)
+#undef X
+    return cudaErrorInvalidValue;
+}
+
+template <int OUT>
+cudaError_t gemm_launch_out(int bn, int stages, int pair, const LaunchShape& s,
+                            const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& c,
+                            const KParams& p, cudaStream_t stream) {
+#define X(B, S, K)                                                          \
+    if constexpr (inst::one_sm_ok<OUT, B>())                                \
+        if (!pair && bn == B && stages == S)                                \
+            return inst::launch<false, B, S, OUT, K>(s, a, b, c, p, stream);
+    GBG_ONE_SM_VARIANTS(X)
+#undef X
+#define X(B, S, K)                                                          \
+    if constexpr (inst::pair_ok<OUT, B>())                                  \
+        if (pair && bn == B && stages == S)                                 \
+            return inst::launch<true, B, S, OUT, K>(s, a, b, c, p, stream);
+    GBG_PAIR_VARIANTS(X)
+#undef X
+    return cudaErrorInvalidValue;
+}
+
+template <int OUT>
+const void* gemm_kernel_ptr_out(int bn, int stages, int pair) {
+#define X(B, S, K)                                                          \
+    if constexpr (inst::one_sm_ok<OUT, B>())                                \
+        if (!pair && bn == B && stages == S) return inst::kernel_fn<false, B, S, OUT, K>();
+    GBG_ONE_SM_VARIANTS(X)
+#undef X
+#define X(B, S, K)                                                          \
+    if constexpr (inst::pair_ok<OUT, B>())                                  \
+        if (pair && bn == B && stages == S) return inst::kernel_fn<true, B, S, OUT, K>();
+    GBG_PAIR_VARIANTS(X)
+#undef X
+    return nullptr;
+}
+
+// One explicit instantiation per output type, in that type's translation unit.
+#define GBG_INSTANTIATE_OUTPUT(OUT)                                                        \
+    template cudaError_t gemm_prepare_out<OUT>(int, int, int, size_t*);                   \
+    template cudaError_t gemm_launch_out<OUT>(int, int, int, const LaunchShape&,          \
+                                              const CUtensorMap&, const CUtensorMap&,      \
+                                              const CUtensorMap&, const KParams&,          \
+                                              cudaStream_t);                               \
+    template const void* gemm_kernel_ptr_out<OUT>(int, int, int);
+
+}  // namespace gbg

@@ -15,6 +15,14 @@ constexpr int default_stages_ks2(int bn) { return bn == 128 ? 3 : 4; }
 // SM-pair kernel: each CTA holds A 128 x 64 and half of B per stage.
 constexpr int default_pair_stages_ks2(int bn) { return bn == 256 ? 3 : 4; }
 constexpr int default_pair_stages(int bn) { return bn == 256 ? 6 : 8; }
+// Four k-blocks per ring slot (one-SM BN 64, SM-pair BN 128): two 96 KiB slots.
+constexpr int default_stages_ks4(int) { return 2; }
+// Ring depth of a variant: one-SM or pair kernel, tile width, k-blocks per slot.
+constexpr int default_ring_stages(int pair, int bn, int ks) {
+    return ks == 4 ? default_stages_ks4(bn)
+           : pair  ? (ks == 2 ? default_pair_stages_ks2(bn) : default_pair_stages(bn))
+                   : (ks == 2 ? default_stages_ks2(bn) : default_stages(bn));
+}
 
 struct LaunchShape {
     int grid;
@@ -23,43 +31,28 @@ struct LaunchShape {
     int cluster = 1;   // CTAs per thread-block cluster (x dimension)
 };
 
-// Kernel variant lookup.  `out` is kOutF16 / kOutBF16 / kOutI32.  Returns
-// cudaErrorInvalidValue if no variant exists for (bn, stages, out).
-cudaError_t gemm_prepare(int bn, int stages, int out, size_t* smem_bytes);
-cudaError_t gemm_launch(int bn, int stages, int out, const LaunchShape& shape,
+// Kernel variant lookup.  `out` is kOutF16 / kOutBF16 / kOutI32, `pair` = 1 for
+// the SM-pair kernel.  cudaErrorInvalidValue if no variant exists for
+// (bn, stages, out, pair).
+cudaError_t gemm_prepare(int bn, int stages, int out, int pair, size_t* smem_bytes);
+cudaError_t gemm_launch(int bn, int stages, int out, int pair, const LaunchShape& shape,
                         const CUtensorMap& tmap_a, const CUtensorMap& tmap_b,
                         const CUtensorMap& tmap_c, const KParams& p, cudaStream_t stream);
 
-// Per-output-type translation units.
-cudaError_t gemm_prepare_f16(int bn, int stages, size_t* smem_bytes);
-cudaError_t gemm_prepare_bf16(int bn, int stages, size_t* smem_bytes);
-cudaError_t gemm_prepare_i32(int bn, int stages, size_t* smem_bytes);
-cudaError_t gemm_launch_f16(int bn, int stages, const LaunchShape&, const CUtensorMap&, const CUtensorMap&,
-                            const CUtensorMap&, const KParams&, cudaStream_t);
-cudaError_t gemm_launch_bf16(int bn, int stages, const LaunchShape&, const CUtensorMap&, const CUtensorMap&,
-                             const CUtensorMap&, const KParams&, cudaStream_t);
-cudaError_t gemm_launch_i32(int bn, int stages, const LaunchShape&, const CUtensorMap&, const CUtensorMap&,
-                            const CUtensorMap&, const KParams&, cudaStream_t);
+// Per output type (defined in gemm_inst.cuh, instantiated in gemm_inst_<type>.cu).
+template <int OUT>
+cudaError_t gemm_prepare_out(int bn, int stages, int pair, size_t* smem_bytes);
+template <int OUT>
+cudaError_t gemm_launch_out(int bn, int stages, int pair, const LaunchShape& shape,
+                            const CUtensorMap& tmap_a, const CUtensorMap& tmap_b,
+                            const CUtensorMap& tmap_c, const KParams& p, cudaStream_t stream);
+template <int OUT>
+const void* gemm_kernel_ptr_out(int bn, int stages, int pair);
 
 // Co-resident clusters of shape.cluster CTAs of a kernel variant (pair = 1: the
 // SM-pair kernel).
 cudaError_t gemm_max_clusters(int bn, int stages, int out, int pair, const LaunchShape& shape,
                               int* n);
-const void* gemm_kernel_ptr_f16(int bn, int stages, int pair);
-const void* gemm_kernel_ptr_bf16(int bn, int stages, int pair);
-const void* gemm_kernel_ptr_i32(int bn, int stages, int pair);
-
-// SM-pair (cta_group::2) kernels, 16-bit outputs.
-cudaError_t gemm_prepare_pair_f16(int bn, int stages, size_t* smem_bytes);
-cudaError_t gemm_prepare_pair_bf16(int bn, int stages, size_t* smem_bytes);
-cudaError_t gemm_launch_pair_f16(int bn, int stages, const LaunchShape&, const CUtensorMap&,
-                                 const CUtensorMap&, const CUtensorMap&, const KParams&, cudaStream_t);
-cudaError_t gemm_prepare_pair_i32(int bn, int stages, size_t* smem_bytes);
-cudaError_t gemm_launch_pair_i32(int bn, int stages, const LaunchShape&, const CUtensorMap&,
-                                 const CUtensorMap&, const CUtensorMap&, const KParams&, cudaStream_t);
-cudaError_t gemm_launch_pair_bf16(int bn, int stages, const LaunchShape&, const CUtensorMap&,
-                                  const CUtensorMap&, const CUtensorMap&, const KParams&,
-                                  cudaStream_t);
 
 // Auxiliary kernels (gemm_aux.cu).
 cudaError_t launch_widen_i8(const int8_t* a, int64_t na, const int8_t* b, int64_t nb, void* a16,
