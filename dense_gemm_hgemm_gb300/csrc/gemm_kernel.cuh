@@ -47,9 +47,9 @@ namespace gbg {
 
 // KS = 64-wide k-blocks per ring slot.  A slot's copies complete on one barrier
 // phase, and the copy engine turns a phase of one A and one B box around in
-// ~0.24 us per SM for boxes up to 32 KiB (measured on GB300), so with KS = 2 the
-// narrow tiles load each operand's two k-blocks as one 3-D box (operand maps
-// viewed as 64 elements x rows x k-blocks) and stream about twice as fast.
+// ~0.24 us per SM for boxes up to 32 KiB (measured on GB300), so with KS = 2 or
+// 4 the narrow tiles load each operand's KS k-blocks as one 3-D box (operand
+// maps viewed as 64 elements x rows x k-blocks) and stream faster.
 template <int BN, int STAGES, int KS = 1>
 struct SmemLayout {
     static constexpr int kBSubBytes = BN * kBK * 2;              // one k-block of B
@@ -359,21 +359,23 @@ __device__ __forceinline__ void prefetch_operand(const CUtensorMap* map, int32_t
     for (int32_t i = 0; i < rows / 64; ++i) tma_prefetch_l2_2d(map, row0 + i * 64, kb * kBK);
 }
 
-// Both k-blocks kb, kb+1 of an operand tile for a two-k-block slot: K-major =
-// one 3-D box {64, rows, 2} of the (64, rows, K/64) view; MN-major = rows/64 boxes
-// {64 MN, 128 K} (the map's box is 128 K-rows high), 16 KiB apart.
-__device__ __forceinline__ void load_operand_2kb(uint32_t dst, const CUtensorMap* map, uint32_t bar,
-                                                 int32_t kb, int32_t row0, int32_t rows,
-                                                 int32_t mn_major) {
+// KS consecutive k-blocks kb .. kb+KS-1 of an operand tile for a multi-k-block
+// slot: K-major = one 3-D box {64, rows, KS} of the (64, rows, K/64) view;
+// MN-major = rows/64 boxes {64 MN, KS*64 K} (the map's box is KS*64 K-rows
+// high), KS*8 KiB apart.
+template <int KS>
+__device__ __forceinline__ void load_operand_kb(uint32_t dst, const CUtensorMap* map, uint32_t bar,
+                                                int32_t kb, int32_t row0, int32_t rows,
+                                                int32_t mn_major) {
     if (!mn_major) {
         tma_load_3d(dst, map, bar, 0, row0, kb);
         return;
     }
     for (int32_t i = 0; i < rows / 64; ++i)
-        tma_load_2d(dst + static_cast<uint32_t>(i) * 16384u, map, bar, row0 + i * 64, kb * kBK);
+        tma_load_2d(dst + static_cast<uint32_t>(i * KS) * 8192u, map, bar, row0 + i * 64, kb * kBK);
 }
-__device__ __forceinline__ void prefetch_operand_2kb(const CUtensorMap* map, int32_t kb, int32_t row0,
-                                                     int32_t rows, int32_t mn_major) {
+__device__ __forceinline__ void prefetch_operand_kb(const CUtensorMap* map, int32_t kb, int32_t row0,
+                                                    int32_t rows, int32_t mn_major) {
     if (!mn_major) {
         tma_prefetch_l2_3d(map, 0, row0, kb);
         return;
@@ -844,15 +846,15 @@ __device__ __forceinline__ UnitCoord unit_at(const KParams& p, int32_t u) {
 // ----------------------------------------------------------------------------
 // the kernel
 // ----------------------------------------------------------------------------
-// KS = 2: A and B are K-major and their maps are the 3-D views (the host
-// guarantees both; multicast is not combined with it).
+// KS > 1: each K-major operand's map is the 3-D view (the host guarantees it
+// and K % 64 == 0; multicast is not combined with it).
 template <int BN, int STAGES, int OUT, int KS = 1>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_tn_kernel(const __grid_constant__ CUtensorMap tmap_a,
                    const __grid_constant__ CUtensorMap tmap_b,
                    const __grid_constant__ CUtensorMap tmap_c, const KParams p) {
     using L = SmemLayout<BN, STAGES, KS>;
-    static_assert(KS == 1 || KS == 2, "k-blocks per ring slot");
+    static_assert(KS == 1 || KS == 2 || KS == 4, "k-blocks per ring slot");
     static_assert((OUT == kOutI32 ? 2 : 1) * SplitRecv<BN>::kBytes <= L::kRingBytes,
                   "split-K receive area (and parked integer sums) must fit in the ring");
     static_assert(BN == 64 || BN == 128 || BN == 256, "tile width");
@@ -921,9 +923,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int32_t a_row0 =
             c.m_blk * kBM + static_cast<int32_t>(blockIdx.x & ((1u << p.mcast_shift) - 1u)) * a_rows;
         for (int32_t kb = c.kb_begin; kb < kb_end; kb += KS) {
-            if constexpr (KS == 2) {
-                prefetch_operand_2kb(&tmap_a, kb, a_row0, a_rows, p.a_mn_major);
-                prefetch_operand_2kb(&tmap_b, kb, c.n_blk * BN, BN, p.b_mn_major);
+            if constexpr (KS > 1) {
+                prefetch_operand_kb(&tmap_a, kb, a_row0, a_rows, p.a_mn_major);
+                prefetch_operand_kb(&tmap_b, kb, c.n_blk * BN, BN, p.b_mn_major);
             } else {
                 prefetch_operand(&tmap_a, kb, a_row0, a_rows, p.a_mn_major);
                 prefetch_operand(&tmap_b, kb, c.n_blk * BN, BN, p.b_mn_major);
@@ -954,19 +956,19 @@ __global__ void __launch_bounds__(kThreads, 1)
                         break;
                     }
                     mbar_arrive_expect_tx(full, kStageTx + p.tx_extra);
-                    if constexpr (KS == 2) {
-                        // both k-blocks of each operand in one copy; a copy past the
-                        // end of K is zero-filled and past the slice end is unused,
-                        // but always delivers the full box
-                        load_operand_2kb(ring + stage * L::kASlotBytes, &tmap_a, full, kb,
-                                         c.m_blk * kBM, kBM, p.a_mn_major);
-                        load_operand_2kb(ring_b + stage * L::kBTileBytes, &tmap_b, full, kb,
-                                         c.n_blk * BN, BN, p.b_mn_major);
+                    if constexpr (KS > 1) {
+                        // the slot's KS k-blocks of each operand in one copy; a copy
+                        // past the end of K is zero-filled and past the slice end is
+                        // unused, but always delivers the full box
+                        load_operand_kb<KS>(ring + stage * L::kASlotBytes, &tmap_a, full, kb,
+                                            c.m_blk * kBM, kBM, p.a_mn_major);
+                        load_operand_kb<KS>(ring_b + stage * L::kBTileBytes, &tmap_b, full, kb,
+                                            c.n_blk * BN, BN, p.b_mn_major);
                         if (p.l2_prefetch > 0 && kb + p.l2_prefetch < c.kb_end) {
-                            prefetch_operand_2kb(&tmap_a, kb + p.l2_prefetch, c.m_blk * kBM, kBM,
-                                                 p.a_mn_major);
-                            prefetch_operand_2kb(&tmap_b, kb + p.l2_prefetch, c.n_blk * BN, BN,
-                                                 p.b_mn_major);
+                            prefetch_operand_kb(&tmap_a, kb + p.l2_prefetch, c.m_blk * kBM, kBM,
+                                                p.a_mn_major);
+                            prefetch_operand_kb(&tmap_b, kb + p.l2_prefetch, c.n_blk * BN, BN,
+                                                p.b_mn_major);
                         }
                     } else {
                         if (p.mcast > 1) {
@@ -1064,7 +1066,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         const uint32_t b_step = desc_k_step(p.b_mn_major);
 #pragma unroll
                         for (int32_t j = 0; j < KS; ++j) {
-                            if (j >= nsub) break;   // the slot's second k-block lies past the slice
+                            if (j >= nsub) break;   // the slot's later k-blocks lie past the slice
                             const uint64_t a_desc = operand_desc<KS>(
                                 ring + stage * L::kASlotBytes + kblock_offset(p.a_mn_major, kATileBytes, j),
                                 p.a_mn_major);

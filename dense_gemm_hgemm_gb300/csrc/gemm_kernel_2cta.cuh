@@ -30,7 +30,7 @@
 
 namespace gbg {
 
-// KS = 64-wide k-blocks per ring slot (2: each operand's two k-blocks in one
+// KS = 64-wide k-blocks per ring slot (2 or 4: each operand's KS k-blocks in one
 // 3-D copy, as in the one-SM kernel).
 template <int BN, int STAGES, int KS = 1>
 struct SmemLayout2 {
@@ -107,17 +107,18 @@ __device__ __forceinline__ void tma_load_3d_pair(uint32_t dst, const CUtensorMap
         : "memory");
 }
 
-// load_operand_2kb for the pair kernel (bytes counted on the leader's barrier).
-__device__ __forceinline__ void load_operand_2kb_pair(uint32_t dst, const CUtensorMap* map,
-                                                      uint32_t bar_cluster, int32_t kb, int32_t row0,
-                                                      int32_t rows, int32_t mn_major) {
+// load_operand_kb for the pair kernel (bytes counted on the leader's barrier).
+template <int KS>
+__device__ __forceinline__ void load_operand_kb_pair(uint32_t dst, const CUtensorMap* map,
+                                                     uint32_t bar_cluster, int32_t kb, int32_t row0,
+                                                     int32_t rows, int32_t mn_major) {
     if (!mn_major) {
         tma_load_3d_pair(dst, map, bar_cluster, 0, row0, kb);
         return;
     }
     for (int32_t i = 0; i < rows / 64; ++i)
-        tma_load_2d_pair(dst + static_cast<uint32_t>(i) * 16384u, map, bar_cluster, row0 + i * 64,
-                         kb * kBK);
+        tma_load_2d_pair(dst + static_cast<uint32_t>(i * KS) * 8192u, map, bar_cluster,
+                         row0 + i * 64, kb * kBK);
 }
 
 // load_operand for the pair kernel (bytes counted on the leader's barrier).
@@ -182,7 +183,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         const __grid_constant__ CUtensorMap tmap_b,
                         const __grid_constant__ CUtensorMap tmap_c, const KParams p) {
     using L = SmemLayout2<BN, STAGES, KS>;
-    static_assert(KS == 1 || KS == 2, "k-blocks per ring slot");
+    static_assert(KS == 1 || KS == 2 || KS == 4, "k-blocks per ring slot");
     static_assert((OUT == kOutI32 ? 2 : 1) * SplitRecv<BN>::kBytes <= L::kRingBytes,
                   "split-K receive area (and parked integer sums) must fit in the ring");
     static_assert(BN == 128 || BN == 256, "pair tile width");
@@ -254,9 +255,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int32_t a_row = c.m_blk * 2 * kBM + static_cast<int32_t>(rank) * kBM;
         const int32_t b_row = c.n_blk * BN + static_cast<int32_t>(rank) * (BN / 2);
         for (int32_t kb = c.kb_begin; kb < kb_end; kb += KS) {
-            if constexpr (KS == 2) {
-                prefetch_operand_2kb(&tmap_a, kb, a_row, kBM, p.a_mn_major);
-                prefetch_operand_2kb(&tmap_b, kb, b_row, BN / 2, p.b_mn_major);
+            if constexpr (KS > 1) {
+                prefetch_operand_kb(&tmap_a, kb, a_row, kBM, p.a_mn_major);
+                prefetch_operand_kb(&tmap_b, kb, b_row, BN / 2, p.b_mn_major);
             } else {
                 prefetch_operand(&tmap_a, kb, a_row, kBM, p.a_mn_major);
                 prefetch_operand(&tmap_b, kb, b_row, BN / 2, p.b_mn_major);
@@ -288,16 +289,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const uint32_t full_local = smem_addr(&ctl->full[stage]);
                     if (leader) mbar_arrive_expect_tx(full_local, kPairTx + p.tx_extra);
                     const uint32_t full_lead = map_to_rank(full_local, lead);
-                    if constexpr (KS == 2) {
-                        // both k-blocks of each operand in one copy (full box always)
-                        load_operand_2kb_pair(ring + stage * L::kASlotBytes, &tmap_a, full_lead, kb,
-                                              a_row, kBM, p.a_mn_major);
-                        load_operand_2kb_pair(ring_b + stage * L::kBTileBytes, &tmap_b, full_lead, kb,
-                                              b_row, BN / 2, p.b_mn_major);
+                    if constexpr (KS > 1) {
+                        // the slot's KS k-blocks of each operand in one copy (full box always)
+                        load_operand_kb_pair<KS>(ring + stage * L::kASlotBytes, &tmap_a, full_lead,
+                                                 kb, a_row, kBM, p.a_mn_major);
+                        load_operand_kb_pair<KS>(ring_b + stage * L::kBTileBytes, &tmap_b, full_lead,
+                                                 kb, b_row, BN / 2, p.b_mn_major);
                         if (p.l2_prefetch > 0 && kb + p.l2_prefetch < c.kb_end) {
-                            prefetch_operand_2kb(&tmap_a, kb + p.l2_prefetch, a_row, kBM, p.a_mn_major);
-                            prefetch_operand_2kb(&tmap_b, kb + p.l2_prefetch, b_row, BN / 2,
-                                                 p.b_mn_major);
+                            prefetch_operand_kb(&tmap_a, kb + p.l2_prefetch, a_row, kBM, p.a_mn_major);
+                            prefetch_operand_kb(&tmap_b, kb + p.l2_prefetch, b_row, BN / 2,
+                                                p.b_mn_major);
                         }
                     } else {
                         load_operand_pair(ring + stage * kATileBytes, &tmap_a, full_lead, kb, a_row,
@@ -370,7 +371,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         const uint32_t b_step = desc_k_step(p.b_mn_major);
 #pragma unroll
                         for (int32_t j = 0; j < KS; ++j) {
-                            if (j >= nsub) break;   // the slot's second k-block lies past the slice
+                            if (j >= nsub) break;   // the slot's later k-blocks lie past the slice
                             const uint64_t a_desc = operand_desc<KS>(
                                 ring + stage * L::kASlotBytes + kblock_offset(p.a_mn_major, kATileBytes, j),
                                 p.a_mn_major);

@@ -69,14 +69,19 @@ def candidates(M, N, K, dtype, sms):
                         and pair_tiles * ps * 2 <= sms and pair_tiles < sms // 2):
                     out.append({"block_n": bn, "split_k": ps, "raster_group": 8,
                                 "split_mode": 1, "cta_pair": 1})
-    # the one-SM narrow-tile candidates again with two k-blocks per ring slot
-    two = []
+    # the narrow-tile candidates again with two, and (one-SM 64-wide, SM-pair
+    # 128-wide tiles) four k-blocks per ring slot
+    more = []
     if K % 64 == 0:
         for c in out:
-            if ((c.get("cta_pair") or c["block_n"] <= 128) and not c.get("multicast")
-                    and -(-num_kb // c["split_k"]) >= 2):
-                two.append({**c, "kblocks_per_stage": 2})
-    return out + two
+            per = -(-num_kb // c["split_k"])
+            if c.get("multicast") or per < 2:
+                continue
+            if c.get("cta_pair") or c["block_n"] <= 128:
+                more.append({**c, "kblocks_per_stage": 2})
+            if per >= 4 and c["block_n"] == (128 if c.get("cta_pair") else 64):
+                more.append({**c, "kblocks_per_stage": 4})
+    return out + more
 
 
 def _time(plan, copies, stream, flush, batches=5, reps_warm=20):
