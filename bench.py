@@ -68,6 +68,8 @@ def parse_args(argv=None):
                     help="run the TMA load-mode x FMA-intensity experiment and print its table")
     ap.add_argument("--shape", default=None,
                     help="with --ncu-steps: run only this workload, 'M,N,K,dtype' (profiling)")
+    ap.add_argument("--config", default=None,
+                    help="with --shape: a JSON kernel configuration instead of the table's")
     return ap.parse_args(argv)
 
 
@@ -640,8 +642,9 @@ def cpu_oracle_named(full_limit_s: float = 2.0, block_rows: int = 64):
     return out, single, threads
 
 
-def profile_one(spec, calls, stream):
-    """`calls` launches of one shape with the table's configuration (for ncu)."""
+def profile_one(spec, calls, stream, config=None):
+    """`calls` launches of one shape with the table's configuration, or `config`
+    (a JSON object of gemm_config_t fields), for ncu."""
     import dense_gemm_hgemm_gb300 as g
     M, N, K, dtype = spec.split(",")
     M, N, K = int(M), int(N), int(K)
@@ -654,7 +657,7 @@ def profile_one(spec, calls, stream):
         A = torch.randn(M, K, generator=gen, device="cuda").to(inputs.TORCH_DTYPE[dtype])
         B = torch.randn(N, K, generator=gen, device="cuda").to(inputs.TORCH_DTYPE[dtype])
     C = torch.empty(M, N, device="cuda", dtype=inputs.OUT_DTYPE[dtype])
-    with g.Plan(M, N, K, dtype) as plan:
+    with g.Plan(M, N, K, dtype, json.loads(config) if config else None) as plan:
         for _ in range(calls):
             plan.run(A, B, C, stream)
         plan.check(stream)
@@ -693,7 +696,7 @@ def ours(args):
     stream = torch.cuda.Stream()
     sms = torch.cuda.get_device_properties(0).multi_processor_count
     if args.ncu_steps and args.shape:
-        profile_one(args.shape, args.ncu_steps, stream)
+        profile_one(args.shape, args.ncu_steps, stream, args.config)
         return
     items = make_sweep("cuda")
     flops_step = sum(w.flops for w, *_ in items)

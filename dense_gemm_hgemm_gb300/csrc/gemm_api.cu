@@ -129,7 +129,9 @@ gemm_status_t normalise_config(int64_t M, int64_t N, int64_t K, gemm_dtype_t dty
     if (m_blocks * n_blocks * s > INT32_MAX) return GEMM_ERR_INVALID_ARG;
     c.split_k = static_cast<int32_t>(s);
     if (c.split_k == 1) c.split_mode = 0;
-    if (c.multicast > 1 && (c.split_k != 1 || c.cta_pair)) return GEMM_ERR_INVALID_ARG;
+    if (c.multicast > 1 && c.split_k != 1) return GEMM_ERR_INVALID_ARG;
+    // SM pairs share A between two pairs of one four-CTA cluster
+    if (c.multicast > 2 && c.cta_pair) return GEMM_ERR_INVALID_ARG;
     // Cluster split: the slices of a tile share its 128 rows evenly (S | 128) and
     // form a portable cluster (S <= 8).
     if (c.split_mode == 1 && c.split_k != 2 && c.split_k != 4 && c.split_k != 8)
@@ -412,6 +414,10 @@ gemm_status_t create_plan(int64_t M, int64_t N, int64_t K, gemm_dtype_t dtype,
     if (cfg.cta_pair && kp.cluster_split) {   // one unit per pair, split_k pairs per cluster
         p->shape.grid = 2 * kp.num_units;
         p->shape.cluster = 2 * cfg.split_k;
+    } else if (cfg.cta_pair && kp.mcast > 1) { // persistent clusters of two pairs sharing A
+        const int quads_cap = cap / 4 > 0 ? cap / 4 : 1;
+        p->shape.grid = 4 * (kp.num_units < quads_cap ? kp.num_units : quads_cap);
+        p->shape.cluster = 4;
     } else if (cfg.cta_pair) {                 // persistent SM pairs: two CTAs per tile
         const int pairs_cap = cap / 2 > 0 ? cap / 2 : 1;
         p->shape.grid = 2 * (kp.num_units < pairs_cap ? kp.num_units : pairs_cap);
@@ -422,9 +428,9 @@ gemm_status_t create_plan(int64_t M, int64_t N, int64_t K, gemm_dtype_t dtype,
     p->shape.smem_bytes = smem;
     if (kp.mcast > 1) {   // no more persistent clusters than fit on the GPU at once
         int fit = 0;
-        if (gbg::gemm_max_clusters(cfg.block_n, cfg.stages, p->out_kind, 0, p->shape, &fit) ==
-                cudaSuccess && fit > 0) {
-            if (p->shape.grid > fit * kp.mcast) p->shape.grid = fit * kp.mcast;
+        if (gbg::gemm_max_clusters(cfg.block_n, cfg.stages, p->out_kind, cfg.cta_pair, p->shape,
+                                   &fit) == cudaSuccess && fit > 0) {
+            if (p->shape.grid > fit * p->shape.cluster) p->shape.grid = fit * p->shape.cluster;
         } else {
             cudaGetLastError();
         }

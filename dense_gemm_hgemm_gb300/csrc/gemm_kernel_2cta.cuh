@@ -19,6 +19,14 @@
 // pair), double-buffered TMEM accumulator, bounded waits with an error word,
 // programmatic dependent launch, L2 prefetch before the dependency wait.
 //
+// A multicast (mcast = 2): a cluster of four CTAs holds two pairs that compute
+// adjacent N-tiles (2g, 2g+1) of the same 256 rows.  CTA (pair q, half h) loads
+// rows [64q, 64q+64) of its half's 128 A rows and multicasts them to CTA (0, h)
+// and CTA (1, h), so each A row crosses from L2 once for both pairs.  Each pair
+// leader's MMA commit releases the slot in all four CTAs (every empty barrier
+// counts both pairs), so a slot is refilled only when both pairs consumed it; a
+// tile past N loads zeros and stores nothing.
+//
 // Split-K in the cluster (cluster_split, S = 2 or 4): a cluster of 2S CTAs holds
 // S pairs (ranks 2s, 2s+1 form pair s) that compute K-slices s of one 256 x BN
 // tile; each CTA stages its fp32 partial rows in its (then idle) ring, and CTA
@@ -94,6 +102,21 @@ __device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap
         "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes"
         " [%0], [%1, {%3, %4}], [%2];" ::"r"(dst),
         "l"(reinterpret_cast<uint64_t>(map)), "r"(bar_cluster), "r"(x), "r"(y)
+        : "memory");
+}
+
+// Multicast form: the box lands at the same shared-memory offset in every CTA of
+// `cta_mask`, and for each destination CTA the bytes are counted on the barrier
+// at `bar_cluster`'s offset in that destination's pair leader (checked on GB300:
+// with the barrier operand naming the issuing pair's leader, destinations 0/2
+// and 1/3 of a four-CTA cluster all complete the barriers of CTAs 0 and 2).
+__device__ __forceinline__ void tma_load_2d_pair_mcast(uint32_t dst, const CUtensorMap* map,
+                                                       uint32_t bar_cluster, int32_t x, int32_t y,
+                                                       uint16_t cta_mask) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes"
+        ".multicast::cluster [%0], [%1, {%3, %4}], [%2], %5;" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(bar_cluster), "r"(x), "r"(y), "h"(cta_mask)
         : "memory");
 }
 
@@ -207,8 +230,19 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t lead = crank & ~1u;                 // cluster rank of this pair's leader
     const uint16_t pair_mask = static_cast<uint16_t>(3u << lead);
     const bool leader = rank == 0;
-    const int32_t pair = static_cast<int32_t>(blockIdx.x >> 1);
-    const int32_t npairs = static_cast<int32_t>(gridDim.x >> 1);
+    // With A multicast a unit is a group of two n-tiles owned by one four-CTA
+    // cluster; otherwise one tile (or K-slice) per pair.
+    const bool mcast = p.mcast > 1;
+    const uint32_t qpair = (crank >> 1) & 1u;          // pair within a multicast cluster
+    const uint16_t release_mask = mcast ? static_cast<uint16_t>(0xFu) : pair_mask;
+    const uint16_t a_mask = static_cast<uint16_t>((1u << rank) | (1u << (2u + rank)));
+    const int32_t pair = static_cast<int32_t>(blockIdx.x >> (mcast ? 2 : 1));
+    const int32_t npairs = static_cast<int32_t>(gridDim.x >> (mcast ? 2 : 1));
+    auto coord = [&](int32_t u) {
+        UnitCoord c = unit_coord_fast(u, p);
+        if (mcast) c.n_blk = c.n_blk * 2 + static_cast<int32_t>(qpair);
+        return c;
+    };
 
     if (warp == 0 && lane == 0) {
         prefetch_tmap(&tmap_a);
@@ -216,7 +250,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         prefetch_tmap(&tmap_c);
         for (int s = 0; s < STAGES; ++s) {
             mbar_init(smem_addr(&ctl->full[s]), 1);
-            mbar_init(smem_addr(&ctl->empty[s]), 1);
+            mbar_init(smem_addr(&ctl->empty[s]), mcast ? 2 : 1);   // both pairs' releases
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(smem_addr(&ctl->tmem_full[b]), 1);
@@ -247,19 +281,22 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     bool epi_ok = false;   // epilogue: this CTA's accumulator is complete (split-K in the cluster)
     // This pair's first unit, worked out while the previous kernel may still run.
-    const UnitCoord c_first = unit_coord_fast(pair, p);
+    const UnitCoord c_first = coord(pair);
     if (warp == 0 && lane == 0 && pair < p.num_units) {
         const UnitCoord c = c_first;
         const int32_t ahead = STAGES * KS > p.l2_prefetch ? STAGES * KS : p.l2_prefetch;
         const int32_t kb_end = c.kb_begin + ahead < c.kb_end ? c.kb_begin + ahead : c.kb_end;
-        const int32_t a_row = c.m_blk * 2 * kBM + static_cast<int32_t>(rank) * kBM;
+        // with multicast, this CTA's 64-row share of its half's A rows
+        const int32_t a_rows = mcast ? kBM / 2 : kBM;
+        const int32_t a_row = c.m_blk * 2 * kBM + static_cast<int32_t>(rank) * kBM +
+                              (mcast ? static_cast<int32_t>(qpair) * a_rows : 0);
         const int32_t b_row = c.n_blk * BN + static_cast<int32_t>(rank) * (BN / 2);
         for (int32_t kb = c.kb_begin; kb < kb_end; kb += KS) {
             if constexpr (KS > 1) {
-                prefetch_operand_kb(&tmap_a, kb, a_row, kBM, p.a_mn_major);
+                prefetch_operand_kb(&tmap_a, kb, a_row, a_rows, p.a_mn_major);
                 prefetch_operand_kb(&tmap_b, kb, b_row, BN / 2, p.b_mn_major);
             } else {
-                prefetch_operand(&tmap_a, kb, a_row, kBM, p.a_mn_major);
+                prefetch_operand(&tmap_a, kb, a_row, a_rows, p.a_mn_major);
                 prefetch_operand(&tmap_b, kb, b_row, BN / 2, p.b_mn_major);
             }
         }
@@ -275,7 +312,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             int issued = 0;
             bool ok = true;
             for (int32_t u = pair; ok && u < p.num_units; u += npairs) {
-                const UnitCoord c = u == pair ? c_first : unit_coord_fast(u, p);
+                const UnitCoord c = u == pair ? c_first : coord(u);
                 const int32_t a_row = c.m_blk * 2 * kBM + static_cast<int32_t>(rank) * kBM;
                 const int32_t b_row = c.n_blk * BN + static_cast<int32_t>(rank) * (BN / 2);
                 for (int32_t kb = c.kb_begin; kb < c.kb_end; kb += KS) {
@@ -301,12 +338,31 @@ __global__ void __launch_bounds__(kThreads, 1)
                                                 p.b_mn_major);
                         }
                     } else {
-                        load_operand_pair(ring + stage * kATileBytes, &tmap_a, full_lead, kb, a_row,
-                                          kBM, p.a_mn_major);
+                        if (mcast) {
+                            // this CTA's 64 rows of its half's A tile, into the same slot
+                            // offset of the matching CTA of both pairs; the bytes count on
+                            // each destination pair's leader barrier (K-major: 64 rows of
+                            // 128 B; M-major: one 64-element block, either way 8 KiB in)
+                            const uint32_t a_dst = ring + stage * kATileBytes + qpair * 8192u;
+                            const int32_t a_r = a_row + static_cast<int32_t>(qpair) * (kBM / 2);
+                            if (p.a_mn_major)
+                                tma_load_2d_pair_mcast(a_dst, &tmap_a, full_lead, a_r, kb * kBK, a_mask);
+                            else
+                                tma_load_2d_pair_mcast(a_dst, &tmap_a, full_lead, kb * kBK, a_r, a_mask);
+                        } else {
+                            load_operand_pair(ring + stage * kATileBytes, &tmap_a, full_lead, kb,
+                                              a_row, kBM, p.a_mn_major);
+                        }
                         load_operand_pair(ring_b + stage * L::kBTileBytes, &tmap_b, full_lead, kb,
                                           b_row, BN / 2, p.b_mn_major);
                         if (p.l2_prefetch > 0 && kb + p.l2_prefetch < c.kb_end) {
-                            prefetch_operand(&tmap_a, kb + p.l2_prefetch, a_row, kBM, p.a_mn_major);
+                            if (mcast)
+                                prefetch_operand(&tmap_a, kb + p.l2_prefetch,
+                                                 a_row + static_cast<int32_t>(qpair) * (kBM / 2),
+                                                 kBM / 2, p.a_mn_major);
+                            else
+                                prefetch_operand(&tmap_a, kb + p.l2_prefetch, a_row, kBM,
+                                                 p.a_mn_major);
                             prefetch_operand(&tmap_b, kb + p.l2_prefetch, b_row, BN / 2,
                                              p.b_mn_major);
                         }
@@ -318,9 +374,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                 }
             }
-            if (leader) {
+            {
                 // Both CTAs' copies count on the leader's barriers: wait for them to
                 // land before the pair can leave (immediate in normal operation).
+                // With multicast every CTA also waits until both pairs have released
+                // its last slots, so no peer's commit arrives after it exits.
                 int s = stage;
                 uint32_t ph = phase;
                 const int pending = issued < STAGES ? issued : STAGES;
@@ -329,7 +387,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                         s = STAGES - 1;
                         ph ^= 1u;
                     }
-                    wait_phase_unwind(smem_addr(&ctl->full[s]), ph, 100000000ull);
+                    if (leader) wait_phase_unwind(smem_addr(&ctl->full[s]), ph, 100000000ull);
+                    if (mcast) wait_phase_unwind(smem_addr(&ctl->empty[s]), ph, 100000000ull);
                 }
             }
             (void)ok;
@@ -343,7 +402,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint32_t acc_iter = 0;
             bool ok = true;
             for (int32_t u = pair; ok && u < p.num_units; u += npairs) {
-                const UnitCoord c = u == pair ? c_first : unit_coord_fast(u, p);
+                const UnitCoord c = u == pair ? c_first : coord(u);
                 // One accumulation per chunk of k-blocks (the whole K range except in
                 // integer mode, where a chunk keeps every fp32 partial sum exact).
                 for (int32_t k0 = c.kb_begin; ok && k0 < c.kb_end; k0 += p.chunk_kb) {
@@ -384,7 +443,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                                 umma_f16_pair(d_tmem, a_desc + a_step * k, b_desc + b_step * k,
                                               p.idesc, (kb > k0 || j > 0 || k > 0) ? 1u : 0u);
                         }
-                        umma_commit_pair(smem_addr(&ctl->empty[stage]), pair_mask);
+                        umma_commit_pair(smem_addr(&ctl->empty[stage]), release_mask);
                         if (++stage == STAGES) {
                             stage = 0;
                             phase ^= 1u;
@@ -408,7 +467,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t acc_iter = 0;
         bool ok = true;
         for (int32_t u = pair; ok && u < p.num_units; u += npairs) {
-            const UnitCoord c = u == pair ? c_first : unit_coord_fast(u, p);
+            const UnitCoord c = u == pair ? c_first : coord(u);
             const int32_t y = c.m_blk * 2 * kBM + static_cast<int32_t>(rank) * kBM + quad * 32;
             const int32_t col0 = c.n_blk * BN;
             const int row_in_tile = quad * 32 + lane;

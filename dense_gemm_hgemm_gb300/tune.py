@@ -62,6 +62,10 @@ def candidates(M, N, K, dtype, sms):
             for g in groups:
                 out.append({"block_n": bn, "split_k": 1, "raster_group": g, "split_mode": 0,
                             "cta_pair": 1})
+                if -(-N // bn) >= 2 and K >= 256:
+                    # two pairs of a four-CTA cluster sharing each A tile by multicast
+                    out.append({"block_n": bn, "split_k": 1, "raster_group": g, "split_mode": 0,
+                                "cta_pair": 1, "multicast": 2})
             for ps in (2, 4):
                 # K sliced over the pairs of one cluster (2 * ps CTAs), one wave at most
                 per = -(-num_kb // ps)

@@ -105,7 +105,11 @@ typedef enum {
  *   multicast    : 0/1 = off; 2 or 4 = clusters of that many CTAs compute
  *                  adjacent N-tiles of the same rows, each loading 1/multicast
  *                  of the shared A tile and multicasting it to the others
- *                  (one-SM kernel, split_k 1; 4 needs A stored M x K)
+ *                  (one-SM kernel, split_k 1; 4 needs A stored M x K).  With
+ *                  cta_pair, 2 = clusters of two SM pairs computing adjacent
+ *                  N-tiles of the same 256 rows, each CTA loading 64 of its 128
+ *                  A rows for both pairs (split_k 1, kblocks_per_stage 1).
+ *                  Multicast copies stay within this GPU's own memory.
  *   kblocks_per_stage : 0 = the table's choice; 1, 2 or 4 = 64-wide k-blocks
  *                  per ring slot.  2: one-SM kernel with block_n 64 or 128 or
  *                  the SM-pair kernel; 4: one-SM kernel with block_n 64 or the

@@ -240,9 +240,15 @@ def test_multicast_config_validation(gemm_lib):
     for bad in ({"block_n": 64, "multicast": 3},
                 {"block_n": 64, "multicast": 8},
                 {"block_n": 64, "multicast": 2, "split_k": 2},
-                {"block_n": 256, "multicast": 2, "cta_pair": 1}):
+                {"block_n": 256, "multicast": 4, "cta_pair": 1},
+                {"block_n": 256, "multicast": 2, "cta_pair": 1, "split_k": 2, "split_mode": 1},
+                {"block_n": 128, "multicast": 2, "cta_pair": 1, "kblocks_per_stage": 2}):
         with pytest.raises(gemm_lib.GemmError):
             gemm_lib.gemm_workspace_bytes(1024, 1024, 4096, "f16", bad)
+    # two SM pairs sharing A (a four-CTA cluster)
+    for cfg in ({"block_n": 256, "multicast": 2, "cta_pair": 1},
+                {"block_n": 128, "multicast": 2, "cta_pair": 1}):
+        assert gemm_lib.gemm_workspace_bytes(1024, 1024, 4096, "f16", cfg) > 0
 
 
 def test_multicast_four_needs_k_major_a(gemm_lib):
