@@ -382,6 +382,9 @@ gemm_status_t create_plan(int64_t M, int64_t N, int64_t K, gemm_dtype_t dtype,
     kp.b_mn_major = b_mn_major(layout) ? 1 : 0;
     kp.mcast = cfg.multicast > 1 ? cfg.multicast : 1;
     kp.l2_prefetch = cfg.l2_prefetch;
+    // M <= 64 on one SM: copy only the tile's 64 real A rows (the copy engine would
+    // otherwise deliver 64 zero-filled rows at the same cost per byte)
+    kp.a_half = (M <= gbg::kBM / 2 && !cfg.cta_pair && kp.mcast == 1) ? 1 : 0;
     // with A multicast a unit is a group of `mcast` adjacent n-blocks
     kp.num_units = kp.mcast > 1 ? kp.m_blocks * ((kp.n_blocks + kp.mcast - 1) / kp.mcast)
                                 : kp.m_blocks * kp.n_blocks * kp.split_k;
@@ -437,7 +440,8 @@ gemm_status_t create_plan(int64_t M, int64_t N, int64_t K, gemm_dtype_t dtype,
     }
 
     if (dtype == GEMM_I8_I32 && M > 0 && N > 0 && K > 0) {
-        st = encode_operand_map(&p->map_a, p->d_a16, M, K, gbg::kBM / kp.mcast, a_mn_major(layout),
+        st = encode_operand_map(&p->map_a, p->d_a16, M, K,
+                                kp.a_half ? gbg::kBM / 2 : gbg::kBM / kp.mcast, a_mn_major(layout),
                                 CU_TENSOR_MAP_DATA_TYPE_FLOAT16, cfg.kblocks_per_stage);
         if (st == GEMM_OK)
             st = encode_operand_map(&p->map_b, p->d_b16, N, K,
@@ -565,7 +569,8 @@ gemm_status_t gemm_run_bias_act(gemm_plan_t p, const void* A, const void* B, voi
         if (!p->map_a_valid || p->map_a_src != A) {
             p->map_a_valid = false;
             const gemm_status_t st =
-                encode_operand_map(&p->map_a, A, p->M, p->K, gbg::kBM / p->kp.mcast,
+                encode_operand_map(&p->map_a, A, p->M, p->K,
+                                   p->kp.a_half ? gbg::kBM / 2 : gbg::kBM / p->kp.mcast,
                                    a_mn_major(p->layout), dt, p->cfg.kblocks_per_stage);
             if (st != GEMM_OK) return st;
             p->map_a_src = A;

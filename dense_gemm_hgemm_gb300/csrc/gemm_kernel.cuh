@@ -919,7 +919,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int32_t ahead = STAGES * KS > p.l2_prefetch ? STAGES * KS : p.l2_prefetch;
         const int32_t kb_end = c.kb_begin + ahead < c.kb_end ? c.kb_begin + ahead : c.kb_end;
         // with multicast, this CTA's slice of the A tile (its A box is that slice)
-        const int32_t a_rows = kBM >> p.mcast_shift;
+        const int32_t a_rows = p.a_half ? kBM / 2 : (kBM >> p.mcast_shift);
         const int32_t a_row0 =
             c.m_blk * kBM + static_cast<int32_t>(blockIdx.x & ((1u << p.mcast_shift) - 1u)) * a_rows;
         for (int32_t kb = c.kb_begin; kb < kb_end; kb += KS) {
@@ -955,18 +955,19 @@ __global__ void __launch_bounds__(kThreads, 1)
                         ok = false;
                         break;
                     }
-                    mbar_arrive_expect_tx(full, kStageTx + p.tx_extra);
+                    // (a half-height A tile delivers 8 KiB less per k-block)
+                    mbar_arrive_expect_tx(full, kStageTx - (p.a_half ? KS * 8192u : 0u) + p.tx_extra);
                     if constexpr (KS > 1) {
                         // the slot's KS k-blocks of each operand in one copy; a copy
                         // past the end of K is zero-filled and past the slice end is
                         // unused, but always delivers the full box
                         load_operand_kb<KS>(ring + stage * L::kASlotBytes, &tmap_a, full, kb,
-                                            c.m_blk * kBM, kBM, p.a_mn_major);
+                                            c.m_blk * kBM, p.a_half ? kBM / 2 : kBM, p.a_mn_major);
                         load_operand_kb<KS>(ring_b + stage * L::kBTileBytes, &tmap_b, full, kb,
                                             c.n_blk * BN, BN, p.b_mn_major);
                         if (p.l2_prefetch > 0 && kb + p.l2_prefetch < c.kb_end) {
-                            prefetch_operand_kb(&tmap_a, kb + p.l2_prefetch, c.m_blk * kBM, kBM,
-                                                p.a_mn_major);
+                            prefetch_operand_kb(&tmap_a, kb + p.l2_prefetch, c.m_blk * kBM,
+                                                p.a_half ? kBM / 2 : kBM, p.a_mn_major);
                             prefetch_operand_kb(&tmap_b, kb + p.l2_prefetch, c.n_blk * BN, BN,
                                                 p.b_mn_major);
                         }
@@ -989,13 +990,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                             }
                         } else {
                             load_operand(ring + stage * kATileBytes, &tmap_a, full, kb, c.m_blk * kBM,
-                                         kBM, p.a_mn_major);
+                                         p.a_half ? kBM / 2 : kBM, p.a_mn_major);
                         }
                         load_operand(ring_b + stage * L::kBTileBytes, &tmap_b, full, kb, c.n_blk * BN,
                                      BN, p.b_mn_major);
                         if (p.l2_prefetch > 0 && kb + p.l2_prefetch < c.kb_end) {
                             // warm L2 with a later k-block of this tile (this CTA's A share)
-                            const int32_t a_rows = kBM >> p.mcast_shift;
+                            const int32_t a_rows = p.a_half ? kBM / 2 : (kBM >> p.mcast_shift);
                             const int32_t a_rank =
                                 static_cast<int32_t>(blockIdx.x & ((1u << p.mcast_shift) - 1u));
                             prefetch_operand(&tmap_a, kb + p.l2_prefetch,
@@ -1068,7 +1069,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                         for (int32_t j = 0; j < KS; ++j) {
                             if (j >= nsub) break;   // the slot's later k-blocks lie past the slice
                             const uint64_t a_desc = operand_desc<KS>(
-                                ring + stage * L::kASlotBytes + kblock_offset(p.a_mn_major, kATileBytes, j),
+                                ring + stage * L::kASlotBytes +
+                                    kblock_offset(p.a_mn_major | p.a_half, kATileBytes, j),
                                 p.a_mn_major);
                             const uint64_t b_desc = operand_desc<KS>(
                                 ring_b + stage * L::kBTileBytes +

@@ -39,6 +39,9 @@ struct KParams {
                             // rows; each loads 1/mcast of the A tile and multicasts it to all
                             // (num_units then counts tile groups)
     int32_t l2_prefetch;    // > 0: the producer also prefetches k-block kb + l2_prefetch into L2
+    int32_t a_half;         // 1 (M <= 64, one-SM kernel): only A rows 0..63 of the tile are
+                            // copied, 8 KiB per k-block (k-block j of a slot at 8 KiB * j); the
+                            // MMA's rows 64..127 read whatever the slot holds and are never stored
     int32_t num_units;      // m_blocks * n_blocks * split_k
     uint32_t idesc;         // tcgen05 instruction descriptor
     uint32_t tx_extra;      // extra bytes each ring slot expects (0 in normal operation)
