@@ -82,7 +82,7 @@ gemm_status_t validate_shape(int64_t M, int64_t N, int64_t K, gemm_dtype_t dtype
 
 bool valid_block_n(int bn, gemm_dtype_t dtype) {
     if (dtype == GEMM_I8_I32) return bn == 64 || bn == 128;
-    return bn == 64 || bn == 128 || bn == 256;
+    return bn == 64 || bn == 128 || bn == 224 || bn == 256;
 }
 
 // Fill the derived fields of a configuration for a shape (split-K made exact:
@@ -105,6 +105,10 @@ gemm_status_t normalise_config(int64_t M, int64_t N, int64_t K, gemm_dtype_t dty
     if (c.kblocks_per_stage == 2 && !c.cta_pair && c.block_n > 128) return GEMM_ERR_INVALID_ARG;
     // four k-blocks per slot: two 96 KiB slots, one-SM 64-wide or SM-pair 128-wide tiles
     if (c.kblocks_per_stage == 4 && c.block_n != (c.cta_pair ? 128 : 64))
+        return GEMM_ERR_INVALID_ARG;
+    // 224-wide tiles: SM pairs only, one K slice, no multicast (each CTA's 112 B
+    // rows are one copy box; the epilogue stores the last 32 columns directly)
+    if (c.block_n == 224 && (!c.cta_pair || c.split_k != 1 || c.multicast > 1))
         return GEMM_ERR_INVALID_ARG;
     if (c.cta_pair) {
         // SM pair: 256-row tiles; K is sliced only across the pairs of a cluster.
@@ -295,6 +299,8 @@ gemm_status_t create_plan(int64_t M, int64_t N, int64_t K, gemm_dtype_t dtype,
     if (st != GEMM_OK) return st;
     // A stored K x M is copied in 64-column blocks: at most two multicast slices
     if (user_cfg && user_cfg->multicast > 2 && a_mn_major(layout)) return GEMM_ERR_INVALID_ARG;
+    // ... and so is a B stored K x N: a 224-wide pair tile's 112 rows per CTA are not
+    if (user_cfg && user_cfg->block_n == 224 && b_mn_major(layout)) return GEMM_ERR_INVALID_ARG;
     // several k-blocks per slot of a K-contiguous operand come from its 3-D view,
     // which needs K % 64 == 0
     const bool some_k_major = !a_mn_major(layout) || !b_mn_major(layout);
@@ -312,6 +318,10 @@ gemm_status_t create_plan(int64_t M, int64_t N, int64_t K, gemm_dtype_t dtype,
 
     gemm_config_t want = user_cfg ? *user_cfg : gbg::select_config(M, N, K, dtype, sms);
     if (want.multicast > 2 && a_mn_major(layout)) want.multicast = 2;
+    if (want.block_n == 224 && b_mn_major(layout)) {
+        want.block_n = 256;
+        want.stages = 0;
+    }
     if (want.kblocks_per_stage > 1 && some_k_major && K % gbg::kBK != 0) {
         want.kblocks_per_stage = 1;
         want.stages = 0;

@@ -5,7 +5,9 @@
 // A variant is (tile width BN, ring depth STAGES, k-blocks per slot KS) of the
 // one-SM kernel or of the SM-pair kernel; (BN, STAGES) identifies it, because
 // every KS has its own depth for a given BN.  The integer output mode keeps BN int32 sums per
-// thread in registers, so it has the narrower variants only.
+// thread in registers, so it has the narrower variants only.  The 224-wide SM-pair tile
+// (fp16/bf16 output, K-contiguous B, no K split or multicast) fills the last wave of SM
+// pairs on shapes whose 256-wide tile count leaves most of it idle.
 #pragma once
 
 #include "gemm_kernel.cuh"
@@ -15,7 +17,8 @@
 // X(BN, STAGES, KS) for every variant of each kernel.
 #define GBG_ONE_SM_VARIANTS(X) \
     X(64, 8, 1) X(128, 6, 1) X(256, 4, 1) X(64, 4, 2) X(128, 3, 2) X(64, 2, 4)
-#define GBG_PAIR_VARIANTS(X) X(256, 6, 1) X(128, 8, 1) X(256, 3, 2) X(128, 4, 2) X(128, 2, 4)
+#define GBG_PAIR_VARIANTS(X) \
+    X(256, 6, 1) X(224, 6, 1) X(128, 8, 1) X(256, 3, 2) X(224, 3, 2) X(128, 4, 2) X(128, 2, 4)
 
 namespace gbg {
 namespace inst {

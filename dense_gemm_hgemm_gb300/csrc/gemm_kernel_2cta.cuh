@@ -1,7 +1,7 @@
 // gemm_kernel_2cta.cuh -- the SM-pair (tcgen05 cta_group::2) variant of the TN GEMM.
 //
 // A thread-block cluster of two CTAs (ranks 0 = leader, 1 = peer, on two SMs)
-// computes a 256 x BN output tile:
+// computes a 256 x BN output tile (BN = 128, 224 or 256):
 //   * each CTA streams its own 128 rows of A (128 x 64 per stage) and its half
 //     of the tile's B rows (BN/2 x 64 per stage) into its own 128B-swizzled
 //     ring; both CTAs' copies count bytes on the LEADER's `full` barrier;
@@ -10,8 +10,10 @@
 //     writes accumulator rows 0-127 to the leader's TMEM, rows 128-255 to the
 //     peer's; tcgen05.commit multicasts ring-slot releases and "accumulator
 //     ready" to the same barriers in both CTAs;
-//   * each CTA's four epilogue warps drain its own TMEM half and TMA-store it,
-//     then arrive (locally or remotely) on the leader's `tmem_empty` barrier.
+//   * each CTA's four epilogue warps drain its own TMEM half and TMA-store it
+//     (64 columns per store; the last 32 columns of a 224-wide tile are stored
+//     from registers, as a 64-column box would reach into the next tile), then
+//     arrive (locally or remotely) on the leader's `tmem_empty` barrier.
 // Per SM this moves 32 KiB per 64-wide k-block for 128 x BN x 64 MACs (BN=256)
 // instead of 48 KiB in the one-SM kernel, and the ring holds 6 stages.
 //
@@ -209,9 +211,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     static_assert(KS == 1 || KS == 2 || KS == 4, "k-blocks per ring slot");
     static_assert((OUT == kOutI32 ? 2 : 1) * SplitRecv<BN>::kBytes <= L::kRingBytes,
                   "split-K receive area (and parked integer sums) must fit in the ring");
-    static_assert(BN == 128 || BN == 256, "pair tile width");
+    static_assert(BN == 128 || BN == 224 || BN == 256, "pair tile width");
     static_assert(OUT != kOutI32 || BN == 128, "integer mode keeps BN int32 sums in registers");
-    constexpr uint32_t kTmemCols = 2 * BN;
+    // two accumulator buffers of BN columns; an allocation is a power of two
+    constexpr uint32_t kTmemCols = 2 * BN <= 256 ? 256u : 512u;
     constexpr uint32_t kPairTx = 2 * L::kStageBytes;   // both CTAs' bytes per stage
 
     extern __shared__ uint8_t smem_raw[];
@@ -566,6 +569,18 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 store_sel ^= 1u;
             }
+            if constexpr (BN % 64 != 0) {
+                // The tile's last 32 columns (BN = 224): a 64-column store box would
+                // reach into the next tile, so each thread stores its own row.
+                const int32_t x = col0 + (BN / 64) * 64;
+                if (!p.cluster_split && y < p.M && x < p.N) {   // warp-uniform
+                    uint32_t v[32];
+                    tmem_ld_32x32b_x32(tmem_base + lane_addr + buf * BN + (BN / 64) * 64, v);
+                    tmem_ld_wait();
+                    apply_bias_act<8>(v, p, x);
+                    if (y + lane < p.M) store_half_row32<OUT>(p.C, p.N, y + lane, x, v);
+                }
+            }
             tc_fence_before();
             __syncwarp();
             if (lane == 0) {
@@ -578,24 +593,27 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 
     // ------------------------------------- split-K reduction across the cluster's pairs
-    if (p.cluster_split) {
-        fence_proxy_async_smem();   // the TMA-written ring now receives peers' stores
-        cluster_sync_all();         // every pair's main loop is over: all rings are idle
-        tc_fence_after();
-        const UnitCoord c = c_first;
-        if (warp >= 2 && epi_ok) {
-            // rows of this CTA's half go to the CTAs (s', same half) of the cluster;
-            // this warp's (idle) TMA-store buffers serve as its transpose staging
-            const uint32_t stg = staging + static_cast<uint32_t>((warp - 2) * 2 * L::kStoreBufBytes);
-            cluster_push_any<BN, OUT, 4>(p.split_k, ring, stg, tmem_base,
-                                         ring + SplitRecv<BN>::kBytes, warp & 3, lane, c.split,
-                                         2u, rank);
+    // (tile widths that are multiples of 64; the host never splits a 224-wide tile)
+    if constexpr (BN % 64 == 0) {
+        if (p.cluster_split) {
+            fence_proxy_async_smem();   // the TMA-written ring now receives peers' stores
+            cluster_sync_all();         // every pair's main loop is over: all rings are idle
+            tc_fence_after();
+            const UnitCoord c = c_first;
+            if (warp >= 2 && epi_ok) {
+                // rows of this CTA's half go to the CTAs (s', same half) of the cluster;
+                // this warp's (idle) TMA-store buffers serve as its transpose staging
+                const uint32_t stg = staging + static_cast<uint32_t>((warp - 2) * 2 * L::kStoreBufBytes);
+                cluster_push_any<BN, OUT, 4>(p.split_k, ring, stg, tmem_base,
+                                             ring + SplitRecv<BN>::kBytes, warp & 3, lane, c.split,
+                                             2u, rank);
+            }
+            cluster_sync_all();         // every slice has arrived at its owner
+            if (warp >= 2)
+                cluster_sum_store<BN, OUT, 4>(p, c.m_blk * 2 * kBM + static_cast<int32_t>(rank) * kBM,
+                                              c.n_blk * BN, static_cast<int>(crank >> 1), ring,
+                                              static_cast<int>(threadIdx.x) - 64);
         }
-        cluster_sync_all();         // every slice has arrived at its owner
-        if (warp >= 2)
-            cluster_sum_store<BN, OUT, 4>(p, c.m_blk * 2 * kBM + static_cast<int32_t>(rank) * kBM,
-                                          c.n_blk * BN, static_cast<int>(crank >> 1), ring,
-                                          static_cast<int>(threadIdx.x) - 64);
     }
 
     // ---------------------------------------------------------------- teardown

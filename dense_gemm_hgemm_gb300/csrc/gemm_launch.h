@@ -13,8 +13,8 @@ constexpr int default_stages(int bn) { return bn == 256 ? 4 : (bn == 128 ? 6 : 8
 // Two k-blocks per ring slot (one-SM kernel, BN 64 / 128): the same ~192 KiB ring.
 constexpr int default_stages_ks2(int bn) { return bn == 128 ? 3 : 4; }
 // SM-pair kernel: each CTA holds A 128 x 64 and half of B per stage.
-constexpr int default_pair_stages_ks2(int bn) { return bn == 256 ? 3 : 4; }
-constexpr int default_pair_stages(int bn) { return bn == 256 ? 6 : 8; }
+constexpr int default_pair_stages_ks2(int bn) { return bn >= 224 ? 3 : 4; }
+constexpr int default_pair_stages(int bn) { return bn >= 224 ? 6 : 8; }
 // Four k-blocks per ring slot (one-SM BN 64, SM-pair BN 128): two 96 KiB slots.
 constexpr int default_stages_ks4(int) { return 2; }
 // Ring depth of a variant: one-SM or pair kernel, tile width, k-blocks per slot.

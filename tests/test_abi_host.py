@@ -117,7 +117,8 @@ def test_select_config_valid_for_every_workload(gemm_lib):
     for M, N, K, dt in shapes:
         c = gemm_lib.gemm_select_config(M, N, K, dt, 152)
         bn = c["block_n"]
-        assert bn in ((64, 128) if dt == "i8" else (64, 128, 256)), (M, N, K, c)
+        assert bn in ((64, 128) if dt == "i8" else (64, 128, 224, 256)), (M, N, K, c)
+        assert bn != 224 or (c["cta_pair"] == 1 and c["split_k"] == 1), (M, N, K, c)
         assert c["stages"] in (3, 4, 6, 8)
         num_kb = -(-K // 64)
         assert 1 <= c["split_k"] <= num_kb
@@ -230,6 +231,24 @@ def test_pair_config_validation(gemm_lib):
                        ("f16", {"block_n": 256, "cta_pair": 1, "split_k": 8, "split_mode": 1}),
                        ("f16", {"block_n": 256, "cta_pair": 1, "stages": 4}),
                        ("f16", {"block_n": 256, "cta_pair": 3})):
+        with pytest.raises(gemm_lib.GemmError):
+            gemm_lib.gemm_workspace_bytes(4096, 4096, 4096, dtype, bad)
+
+
+def test_pair_224_config_validation(gemm_lib):
+    """224-wide tiles: SM pairs, fp16/bf16, one K slice, no multicast."""
+    for dtype in ("f16", "bf16"):
+        for ks in (1, 2):
+            cfg = {"block_n": 224, "cta_pair": 1, "kblocks_per_stage": ks}
+            assert gemm_lib.gemm_workspace_bytes(4096, 4096, 4096, dtype, cfg) > 0
+    for dtype, bad in (("f16", {"block_n": 224}),
+                       ("f16", {"block_n": 224, "cta_pair": 1, "split_k": 2, "split_mode": 1}),
+                       ("f16", {"block_n": 224, "cta_pair": 1, "split_k": 2}),
+                       ("f16", {"block_n": 224, "cta_pair": 1, "multicast": 2}),
+                       ("f16", {"block_n": 224, "cta_pair": 1, "stages": 8}),
+                       ("f16", {"block_n": 224, "cta_pair": 1, "kblocks_per_stage": 4}),
+                       ("i8", {"block_n": 224}),
+                       ("i8", {"block_n": 224, "cta_pair": 1})):
         with pytest.raises(gemm_lib.GemmError):
             gemm_lib.gemm_workspace_bytes(4096, 4096, 4096, dtype, bad)
 
