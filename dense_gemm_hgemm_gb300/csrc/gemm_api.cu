@@ -80,10 +80,7 @@ gemm_status_t validate_shape(int64_t M, int64_t N, int64_t K, gemm_dtype_t dtype
     return GEMM_OK;
 }
 
-bool valid_block_n(int bn, gemm_dtype_t dtype) {
-    if (dtype == GEMM_I8_I32) return bn == 64 || bn == 128;
-    return bn == 64 || bn == 128 || bn == 224 || bn == 256;
-}
+bool valid_block_n(int bn) { return bn == 64 || bn == 128 || bn == 224 || bn == 256; }
 
 // Fill the derived fields of a configuration for a shape (split-K made exact:
 // every K slice non-empty).  Returns GEMM_ERR_INVALID_ARG for a bad config.
@@ -91,7 +88,7 @@ gemm_status_t normalise_config(int64_t M, int64_t N, int64_t K, gemm_dtype_t dty
                                const gemm_config_t& in, gemm_config_t* out,
                                int32_t* kb_per_split) {
     gemm_config_t c = in;
-    if (!valid_block_n(c.block_n, dtype)) return GEMM_ERR_INVALID_ARG;
+    if (!valid_block_n(c.block_n)) return GEMM_ERR_INVALID_ARG;
     if (c.cta_pair != 0 && c.cta_pair != 1) return GEMM_ERR_INVALID_ARG;
     if (c.direct_store != 0 && c.direct_store != 1) return GEMM_ERR_INVALID_ARG;
     if (c.direct_store && c.cta_pair) return GEMM_ERR_INVALID_ARG;
@@ -110,10 +107,14 @@ gemm_status_t normalise_config(int64_t M, int64_t N, int64_t K, gemm_dtype_t dty
     // rows are one copy box; the epilogue stores the last 32 columns directly)
     if (c.block_n == 224 && (!c.cta_pair || c.split_k != 1 || c.multicast > 1))
         return GEMM_ERR_INVALID_ARG;
+    // Integer tiles keep their int32 sums in registers: up to 128 columns on one SM,
+    // 224/256 on SM pairs with eight epilogue warps (one K slice, no multicast).
+    if (dtype == GEMM_I8_I32 && c.block_n > 128 &&
+        (!c.cta_pair || c.split_k != 1 || c.multicast > 1))
+        return GEMM_ERR_INVALID_ARG;
     if (c.cta_pair) {
         // SM pair: 256-row tiles; K is sliced only across the pairs of a cluster.
         if (c.block_n < 128) return GEMM_ERR_INVALID_ARG;
-        if (dtype == GEMM_I8_I32 && c.block_n != 128) return GEMM_ERR_INVALID_ARG;
         if (c.split_k != 1 && c.split_mode != 1) return GEMM_ERR_INVALID_ARG;
     }
     const int want_stages = gbg::default_ring_stages(c.cta_pair, c.block_n, c.kblocks_per_stage);
@@ -437,7 +438,7 @@ gemm_status_t create_plan(int64_t M, int64_t N, int64_t K, gemm_dtype_t dtype,
         p->shape.cluster = 2;
     }
     if (p->shape.grid < 1) p->shape.grid = 1;
-    p->shape.block = gbg::kThreads;
+    p->shape.block = cfg.cta_pair ? gbg::pair_threads(cfg.block_n, p->out_kind) : gbg::kThreads;
     p->shape.smem_bytes = smem;
     if (kp.mcast > 1) {   // no more persistent clusters than fit on the GPU at once
         int fit = 0;

@@ -4,10 +4,11 @@
 //
 // A variant is (tile width BN, ring depth STAGES, k-blocks per slot KS) of the
 // one-SM kernel or of the SM-pair kernel; (BN, STAGES) identifies it, because
-// every KS has its own depth for a given BN.  The integer output mode keeps BN int32 sums per
-// thread in registers, so it has the narrower variants only.  The 224-wide SM-pair tile
-// (fp16/bf16 output, K-contiguous B, no K split or multicast) fills the last wave of SM
-// pairs on shapes whose 256-wide tile count leaves most of it idle.
+// every KS has its own depth for a given BN.  The integer output mode keeps its int32 sums
+// in registers: the one-SM kernel has the narrower variants only, the SM-pair kernel all of
+// them (224/256-wide integer tiles with eight epilogue warps).  The 224-wide SM-pair tile
+// (K-contiguous B, no K split or multicast) fills the last wave of SM pairs on shapes whose
+// 256-wide tile count leaves most of it idle.
 #pragma once
 
 #include "gemm_kernel.cuh"
@@ -26,7 +27,7 @@ namespace inst {
 template <int OUT, int BN>
 constexpr bool one_sm_ok() { return OUT != kOutI32 || BN <= 128; }
 template <int OUT, int BN>
-constexpr bool pair_ok() { return OUT != kOutI32 || BN == 128; }
+constexpr bool pair_ok() { return true; }
 
 template <bool PAIR, int BN, int STAGES, int OUT, int KS>
 const void* kernel_fn() {

@@ -203,16 +203,20 @@ __device__ __forceinline__ uint32_t ld_dsmem_u32(uint32_t cluster_addr) {
 }
 
 template <int BN, int STAGES, int OUT, int KS = 1>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(64 + 32 * kPairEpiWarps<BN, OUT>, 1)
     gemm_tn_pair_kernel(const __grid_constant__ CUtensorMap tmap_a,
                         const __grid_constant__ CUtensorMap tmap_b,
                         const __grid_constant__ CUtensorMap tmap_c, const KParams p) {
     using L = SmemLayout2<BN, STAGES, KS>;
     static_assert(KS == 1 || KS == 2 || KS == 4, "k-blocks per ring slot");
-    static_assert((OUT == kOutI32 ? 2 : 1) * SplitRecv<BN>::kBytes <= L::kRingBytes,
+    // integer tiles wider than 128: eight epilogue warps, one store buffer each
+    constexpr bool kIntWide = OUT == kOutI32 && BN > 128;
+    constexpr int kEpi = kPairEpiWarps<BN, OUT>;
+    static_assert(((OUT == kOutI32 && !kIntWide) ? 2 : 1) * SplitRecv<BN>::kBytes <= L::kRingBytes,
                   "split-K receive area (and parked integer sums) must fit in the ring");
     static_assert(BN == 128 || BN == 224 || BN == 256, "pair tile width");
-    static_assert(OUT != kOutI32 || BN == 128, "integer mode keeps BN int32 sums in registers");
+    static_assert(kEpi * (kIntWide ? 1 : 2) * L::kStoreBufBytes <= L::kStagingBytes,
+                  "epilogue store buffers");
     // two accumulator buffers of BN columns; an allocation is a power of two
     constexpr uint32_t kTmemCols = 2 * BN <= 256 ? 256u : 512u;
     constexpr uint32_t kPairTx = 2 * L::kStageBytes;   // both CTAs' bytes per stage
@@ -257,7 +261,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(smem_addr(&ctl->tmem_full[b]), 1);
-            mbar_init(smem_addr(&ctl->tmem_empty[b]), 2 * kEpiWarps);   // both CTAs' epilogues
+            mbar_init(smem_addr(&ctl->tmem_empty[b]), 2 * kEpi);   // both CTAs' epilogues
         }
         mbar_init(smem_addr(&ctl->drain), 1);
         ctl->abort = 0;
@@ -465,7 +469,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         // ------------------------------------------------------------ epilogue (both CTAs)
         const int quad = warp & 3;
         const uint32_t lane_addr = static_cast<uint32_t>(quad * 32) << 16;
-        const uint32_t store_buf0 = staging + static_cast<uint32_t>((warp - 2) * 2 * L::kStoreBufBytes);
+        const uint32_t store_buf0 =
+            staging + static_cast<uint32_t>((warp - 2) * (kIntWide ? 1 : 2) * L::kStoreBufBytes);
         uint32_t store_sel = 0;
         uint32_t acc_iter = 0;
         bool ok = true;
@@ -474,7 +479,59 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int32_t y = c.m_blk * 2 * kBM + static_cast<int32_t>(rank) * kBM + quad * 32;
             const int32_t col0 = c.n_blk * BN;
             const int row_in_tile = quad * 32 + lane;
-            if constexpr (OUT == kOutI32) {
+            if constexpr (kIntWide) {
+                // Integer mode, 224/256-wide tiles: two warps per TMEM lane quarter;
+                // warps 2-5 take columns [0, 128) of their 32 rows, warps 6-9 columns
+                // [128, BN).  Each exact fp32 chunk is rounded to int32 and added in
+                // registers (mod 2^32); the sums are stored once per tile.
+                const int c_lo = ((warp - 2) >> 2) * 128;
+                const int nj = c_lo == 0 ? 4 : (BN - 128) / 32;
+                uint32_t sum[128];
+#pragma unroll
+                for (int i = 0; i < 128; ++i) sum[i] = 0u;
+                for (int32_t k0 = c.kb_begin; k0 < c.kb_end; k0 += p.chunk_kb) {
+                    const uint32_t buf = acc_iter & 1u;
+                    const uint32_t acc_phase = (acc_iter >> 1) & 1u;
+                    if (!wait_phase(smem_addr(&ctl->tmem_full[buf]), acc_phase, watch,
+                                    kSiteEpiTmemFull)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        if (j >= nj) break;   // warp-uniform
+                        uint32_t v[32];
+                        tmem_ld_32x32b_x32(tmem_base + lane_addr + buf * BN + c_lo + j * 32, v);
+                        tmem_ld_wait();
+#pragma unroll
+                        for (int i = 0; i < 32; ++i)
+                            sum[j * 32 + i] +=
+                                static_cast<uint32_t>(__float2int_rn(__uint_as_float(v[i])));
+                    }
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0)
+                        mbar_arrive_remote(map_to_rank(smem_addr(&ctl->tmem_empty[buf]), lead));
+                    ++acc_iter;
+                }
+                if (!ok) break;
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const int32_t x = col0 + c_lo + j * 32;   // 32 int32 = one buffer row
+                    if (j >= nj || y >= p.M || x >= p.N) continue;   // warp-uniform
+                    if (lane == 0) bulk_wait_group_read<0>();   // one buffer per warp
+                    __syncwarp();
+                    stage_store_row(store_buf0, lane, 0, &sum[j * 32], 8);
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) {
+                        tma_store_2d(&tmap_c, store_buf0, x, y);
+                        bulk_commit_group();
+                    }
+                }
+                continue;
+            } else if constexpr (OUT == kOutI32) {
                 // Integer mode: round each exact fp32 chunk to int32 and add (mod 2^32).
                 uint32_t sum[BN];
 #pragma unroll
@@ -593,8 +650,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 
     // ------------------------------------- split-K reduction across the cluster's pairs
-    // (tile widths that are multiples of 64; the host never splits a 224-wide tile)
-    if constexpr (BN % 64 == 0) {
+    // (tile widths that are multiples of 64, integer ones of 128: the host splits no
+    // other tile)
+    if constexpr (BN % 64 == 0 && !kIntWide) {
         if (p.cluster_split) {
             fence_proxy_async_smem();   // the TMA-written ring now receives peers' stores
             cluster_sync_all();         // every pair's main loop is over: all rings are idle

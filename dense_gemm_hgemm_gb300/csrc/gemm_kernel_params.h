@@ -13,6 +13,13 @@ constexpr int kATileBytes = kBM * kBK * 2;   // 16 KiB
 
 enum OutKind : int { kOutF16 = 0, kOutBF16 = 1, kOutI32 = 2 };
 
+// SM-pair integer tiles wider than 128 columns keep their int32 sums in registers
+// across eight epilogue warps (two per TMEM lane quarter, splitting the columns).
+template <int BN, int OUT>
+inline constexpr int kPairEpiWarps = OUT == kOutI32 && BN > 128 ? 8 : kEpiWarps;
+// Threads of an SM-pair CTA (host side): producer and MMA warps + epilogue warps.
+constexpr int pair_threads(int bn, int out) { return 64 + 32 * (out == kOutI32 && bn > 128 ? 8 : kEpiWarps); }
+
 // Wait-site codes written to the error word when a wait runs out.
 enum WaitSite : int32_t {
     kSiteProducerEmpty = 1,

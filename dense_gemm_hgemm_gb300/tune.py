@@ -56,12 +56,13 @@ def candidates(M, N, K, dtype, sms):
             if s in (2, 4, 8) and -(-num_kb // per) == s:
                 out.append({"block_n": bn, "split_k": s, "raster_group": 16, "split_mode": 1})
     # SM pair: 256-row tiles (raster bands count 256-row blocks).  The 224-wide
-    # tile (fp16/bf16, one K slice, no multicast) fills the last wave of SM pairs
-    # where 256-wide tiles leave most of it idle (4096 columns: 19 tiles, not 16).
-    for bn in ((128,) if dtype == "i8" else (128, 224, 256)):
+    # tile fills the last wave of SM pairs where 256-wide tiles leave most of it
+    # idle (4096 columns: 19 tiles, not 16).  224-wide tiles, and integer tiles
+    # wider than 128, take one K slice and no multicast.
+    for bn in (128, 224, 256):
         if M <= 128:
             continue
-        plain_only = bn == 224
+        plain_only = bn == 224 or (dtype == "i8" and bn > 128)
         pair_tiles = -(-M // 256) * -(-N // bn)
         groups = (4, 8, 16) if pair_tiles >= 2 * sms else (8,)
         for g in groups:

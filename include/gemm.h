@@ -85,8 +85,9 @@ typedef enum {
 /*
  * Kernel configuration (what the per-shape table chooses; see gemm_select_config).
  *   block_n      : output tile width, 64, 128, 224 or 256 (tile height is 128
- *                  rows; int8 allows 64 or 128; 224 only with cta_pair, fp16/bf16,
- *                  split_k 1, no multicast and B stored N x K)
+ *                  rows; 224 only with cta_pair, split_k 1, no multicast and B
+ *                  stored N x K; int8 wider than 128 only with cta_pair, split_k 1
+ *                  and no multicast)
  *   stages       : depth of the shared-memory ring; 0 = the default for block_n
  *   split_k      : number of K slices per output tile (>= 1); slices are summed
  *                  in a fixed order, so results are run-to-run identical
@@ -98,8 +99,8 @@ typedef enum {
  *                      summed through distributed shared memory (split_k must
  *                      come out as 2, 4 or 8; one tile slice per CTA, no scratch)
  *   cta_pair     : 1 = 256-row tiles computed by an SM pair (tcgen05 cta_group::2
- *                  thread-block cluster of two CTAs): block_n 128, 224 or 256
- *                  (int8: 128); 0 = 128-row tiles on one SM
+ *                  thread-block cluster of two CTAs): block_n 128, 224 or 256;
+ *                  0 = 128-row tiles on one SM
  *   direct_store : epilogue store path: 0 = TMA tensor stores from a swizzled
  *                  shared-memory buffer; 1 = 16-byte global stores from each
  *                  thread's row (one-SM kernel only)

@@ -117,8 +117,10 @@ def test_select_config_valid_for_every_workload(gemm_lib):
     for M, N, K, dt in shapes:
         c = gemm_lib.gemm_select_config(M, N, K, dt, 152)
         bn = c["block_n"]
-        assert bn in ((64, 128) if dt == "i8" else (64, 128, 224, 256)), (M, N, K, c)
+        assert bn in (64, 128, 224, 256), (M, N, K, c)
         assert bn != 224 or (c["cta_pair"] == 1 and c["split_k"] == 1), (M, N, K, c)
+        if dt == "i8" and bn > 128:   # wide integer tiles: SM pairs, one K slice
+            assert c["cta_pair"] == 1 and c["split_k"] == 1 and c["multicast"] == 0, (M, N, K, c)
         assert c["stages"] in (3, 4, 6, 8)
         num_kb = -(-K // 64)
         assert 1 <= c["split_k"] <= num_kb
@@ -225,7 +227,7 @@ def test_pair_config_validation(gemm_lib):
     for s in (2, 4):   # K slices across the pairs of one cluster of 2 * s CTAs: no scratch
         cfg = {"block_n": 256, "cta_pair": 1, "split_k": s, "split_mode": 1}
         assert gemm_lib.gemm_workspace_bytes(1024, 1024, 4096, "f16", cfg) == base
-    for dtype, bad in (("i8", {"block_n": 256, "cta_pair": 1}),
+    for dtype, bad in (("i8", {"block_n": 256, "cta_pair": 1, "split_k": 2, "split_mode": 1}),
                        ("f16", {"block_n": 64, "cta_pair": 1}),
                        ("f16", {"block_n": 256, "cta_pair": 1, "split_k": 2}),
                        ("f16", {"block_n": 256, "cta_pair": 1, "split_k": 8, "split_mode": 1}),
@@ -236,8 +238,8 @@ def test_pair_config_validation(gemm_lib):
 
 
 def test_pair_224_config_validation(gemm_lib):
-    """224-wide tiles: SM pairs, fp16/bf16, one K slice, no multicast."""
-    for dtype in ("f16", "bf16"):
+    """224-wide tiles: SM pairs, one K slice, no multicast."""
+    for dtype in ("f16", "bf16", "i8"):
         for ks in (1, 2):
             cfg = {"block_n": 224, "cta_pair": 1, "kblocks_per_stage": ks}
             assert gemm_lib.gemm_workspace_bytes(4096, 4096, 4096, dtype, cfg) > 0
@@ -247,10 +249,22 @@ def test_pair_224_config_validation(gemm_lib):
                        ("f16", {"block_n": 224, "cta_pair": 1, "multicast": 2}),
                        ("f16", {"block_n": 224, "cta_pair": 1, "stages": 8}),
                        ("f16", {"block_n": 224, "cta_pair": 1, "kblocks_per_stage": 4}),
-                       ("i8", {"block_n": 224}),
-                       ("i8", {"block_n": 224, "cta_pair": 1})):
+                       ("i8", {"block_n": 224})):
         with pytest.raises(gemm_lib.GemmError):
             gemm_lib.gemm_workspace_bytes(4096, 4096, 4096, dtype, bad)
+
+
+def test_wide_integer_tile_validation(gemm_lib):
+    """int8 -> int32 wider than 128 columns: SM pairs only, one K slice, no multicast."""
+    for bn in (224, 256):
+        for ks in (1, 2):
+            cfg = {"block_n": bn, "cta_pair": 1, "kblocks_per_stage": ks}
+            assert gemm_lib.gemm_workspace_bytes(1024, 1024, 4096, "i8", cfg) > 0
+        for bad in ({"block_n": bn},
+                    {"block_n": bn, "cta_pair": 1, "split_k": 2, "split_mode": 1},
+                    {"block_n": bn, "cta_pair": 1, "multicast": 2}):
+            with pytest.raises(gemm_lib.GemmError):
+                gemm_lib.gemm_workspace_bytes(1024, 1024, 4096, "i8", bad)
 
 
 def test_multicast_config_validation(gemm_lib):

@@ -80,7 +80,7 @@ def test_bn224_launch_shape():
 
 def test_bn224_refused_configurations():
     for dtype, cfg in (("f16", {"block_n": 224}),                              # one-SM kernel
-                       ("i8", _cfg()),
+                       ("i8", {"block_n": 224}),
                        ("f16", _cfg(split_k=2, split_mode=1)),
                        ("f16", _cfg(multicast=2))):
         with pytest.raises(g.GemmError):
