@@ -9,6 +9,7 @@ result on the CPU or through another library.
 from __future__ import annotations
 
 import ctypes
+import functools
 import os
 import threading
 
@@ -318,14 +319,40 @@ def gemm_workspace_bytes(M, N, K, dtype, config) -> int:
     return int(b.value)
 
 
+def _plan_run(box, A, B, C, stream=None, bias=None, act=ACT_NONE) -> None:
+    """Plan.run for the plan handle in box[0] (None once the plan is closed)."""
+    handle = box[0]
+    if bias is not None or act not in (ACT_NONE, "none"):
+        gemm_run_bias_act(handle, A, B, C, bias, act, stream)
+        return
+    pc = _pycall
+    if pc is None:
+        gemm_run(handle, A, B, C, stream)
+        return
+    try:   # tensors and a stream object
+        st = pc.run(handle or 0, A.data_ptr(), B.data_ptr(), C.data_ptr(), stream.cuda_stream)
+    except AttributeError:   # addresses or a stream handle given as ints, or no stream
+        st = pc.run(handle or 0, _ptr(A) or 0, _ptr(B) or 0, _ptr(C) or 0, _stream(stream) or 0)
+    if st:
+        raise GemmError(st, "gemm_run")
+
+
 class Plan:
-    """Owning wrapper of a plan handle: ``with Plan(M, N, K, "f16") as p: p.run(A, B, C)``."""
+    """Owning wrapper of a plan handle: ``with Plan(M, N, K, "f16") as p: p.run(A, B, C)``.
+
+    ``run(A, B, C, stream)`` with tensors and a stream object, the per-call form of
+    a serving loop, goes straight to gemm_run through a C-level runner bound to the
+    plan (argument marshalling only); every other form takes the general path."""
 
     def __init__(self, M: int, N: int, K: int, dtype="f16", config=None, layout=GEMM_LAYOUT_TN):
         self.M, self.N, self.K, self.dtype = M, N, K, dtype
         lay = LAYOUTS[layout] if isinstance(layout, str) else int(layout)
         self.handle = (gemm_plan_create(M, N, K, dtype, lay) if config is None
                        else gemm_plan_create_with_config(M, N, K, dtype, config, lay))
+        self._box = [self.handle]
+        runner = getattr(_pycall, "Runner", None)
+        if runner is not None:   # an instance attribute: shadows the method below
+            self.run = runner(self._box, functools.partial(_plan_run, self._box))
 
     @property
     def config(self) -> dict:
@@ -336,21 +363,8 @@ class Plan:
         return gemm_plan_get_launch(self.handle)
 
     def run(self, A, B, C, stream=None, bias=None, act=ACT_NONE) -> None:
-        if bias is not None or act not in (ACT_NONE, "none"):
-            gemm_run_bias_act(self.handle, A, B, C, bias, act, stream)
-            return
-        pc = _pycall
-        if pc is None:
-            gemm_run(self.handle, A, B, C, stream)
-            return
-        try:   # tensors and a stream object: the per-call path, kept short
-            st = pc.run(self.handle or 0, A.data_ptr(), B.data_ptr(), C.data_ptr(),
-                        stream.cuda_stream)
-        except AttributeError:   # addresses or a stream handle given as ints, or no stream
-            st = pc.run(self.handle or 0, _ptr(A) or 0, _ptr(B) or 0, _ptr(C) or 0,
-                        _stream(stream) or 0)
-        if st:
-            raise GemmError(st, "gemm_run")
+        """C = A @ B.T (optionally act(A @ B.T + bias)) on `stream`."""
+        _plan_run(self._box, A, B, C, stream, bias, act)
 
     def check(self, stream=None) -> None:
         gemm_plan_check(self.handle, stream)
@@ -363,6 +377,7 @@ class Plan:
 
     def close(self) -> None:
         if self.handle:
+            self._box[0] = None   # the runner falls back to the general path, which refuses
             gemm_plan_destroy(self.handle)
             self.handle = None
 

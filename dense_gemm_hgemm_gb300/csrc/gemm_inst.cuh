@@ -1,6 +1,7 @@
-// gemm_inst.cuh -- the kernel variants and their launchers, one template per
-// output type (gemm_inst_f16.cu, gemm_inst_bf16.cu and gemm_inst_i32.cu each
-// instantiate it once, so the three compile in parallel).
+// gemm_inst.cuh -- the kernel variants (shared-memory set-up and host stub of
+// each), one template per output type (gemm_inst_f16.cu, gemm_inst_bf16.cu and
+// gemm_inst_i32.cu each instantiate it once, so the three compile in parallel).
+// The launches themselves go through the plan's driver function handle.
 //
 // A variant is (tile width BN, ring depth STAGES, k-blocks per slot KS) of the
 // one-SM kernel or of the SM-pair kernel; (BN, STAGES) identifies it, because
@@ -58,37 +59,6 @@ cudaError_t prepare(size_t* smem) {
                                     static_cast<int>(*smem));
 }
 
-// Programmatic dependent launch on every launch: the kernel's set-up may overlap
-// the tail of the previous kernel in the stream (it waits with
-// griddepcontrol.wait before touching global memory).  Clusters: SM pairs,
-// split-K slices of a tile, or CTAs sharing an A tile by multicast.
-template <bool PAIR, int BN, int STAGES, int OUT, int KS>
-cudaError_t launch(const LaunchShape& s, const CUtensorMap& a, const CUtensorMap& b,
-                   const CUtensorMap& c, const KParams& p, cudaStream_t stream) {
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(static_cast<unsigned>(s.grid));
-    cfg.blockDim = dim3(static_cast<unsigned>(s.block));
-    cfg.dynamicSmemBytes = s.smem_bytes;
-    cfg.stream = stream;
-    cudaLaunchAttribute attr[2];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    unsigned n = 1;
-    if (PAIR || s.cluster > 1) {
-        attr[1].id = cudaLaunchAttributeClusterDimension;
-        attr[1].val.clusterDim.x = static_cast<unsigned>(s.cluster);
-        attr[1].val.clusterDim.y = 1;
-        attr[1].val.clusterDim.z = 1;
-        n = 2;
-    }
-    cfg.attrs = attr;
-    cfg.numAttrs = n;
-    if constexpr (PAIR)
-        return cudaLaunchKernelEx(&cfg, gemm_tn_pair_kernel<BN, STAGES, OUT, KS>, a, b, c, p);
-    else
-        return cudaLaunchKernelEx(&cfg, gemm_tn_kernel<BN, STAGES, OUT, KS>, a, b, c, p);
-}
-
 }  // namespace inst
 
 template <int OUT>
@@ -101,25 +71,6 @@ cudaError_t gemm_prepare_out(int bn, int stages, int pair, size_t* smem) {
 #define X(B, S, K)                                                          \
     if constexpr (inst::pair_ok<OUT, B>())                                  \
         if (pair && bn == B && stages == S) return inst::prepare<true, B, S, OUT, K>(smem);
-    GBG_PAIR_VARIANTS(X)
-#undef X
-    return cudaErrorInvalidValue;
-}
-
-template <int OUT>
-cudaError_t gemm_launch_out(int bn, int stages, int pair, const LaunchShape& s,
-                            const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& c,
-                            const KParams& p, cudaStream_t stream) {
-#define X(B, S, K)                                                          \
-    if constexpr (inst::one_sm_ok<OUT, B>())                                \
-        if (!pair && bn == B && stages == S)                                \
-            return inst::launch<false, B, S, OUT, K>(s, a, b, c, p, stream);
-    GBG_ONE_SM_VARIANTS(X)
-#undef X
-#define X(B, S, K)                                                          \
-    if constexpr (inst::pair_ok<OUT, B>())                                  \
-        if (pair && bn == B && stages == S)                                 \
-            return inst::launch<true, B, S, OUT, K>(s, a, b, c, p, stream);
     GBG_PAIR_VARIANTS(X)
 #undef X
     return cudaErrorInvalidValue;
@@ -143,10 +94,6 @@ const void* gemm_kernel_ptr_out(int bn, int stages, int pair) {
 // One explicit instantiation per output type, in that type's translation unit.
 #define GBG_INSTANTIATE_OUTPUT(OUT)                                                        \
     template cudaError_t gemm_prepare_out<OUT>(int, int, int, size_t*);                   \
-    template cudaError_t gemm_launch_out<OUT>(int, int, int, const LaunchShape&,          \
-                                              const CUtensorMap&, const CUtensorMap&,      \
-                                              const CUtensorMap&, const KParams&,          \
-                                              cudaStream_t);                               \
     template const void* gemm_kernel_ptr_out<OUT>(int, int, int);
 
 }  // namespace gbg

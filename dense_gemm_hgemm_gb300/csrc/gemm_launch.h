@@ -32,20 +32,16 @@ struct LaunchShape {
 };
 
 // Kernel variant lookup.  `out` is kOutF16 / kOutBF16 / kOutI32, `pair` = 1 for
-// the SM-pair kernel.  cudaErrorInvalidValue if no variant exists for
-// (bn, stages, out, pair).
+// the SM-pair kernel.  gemm_prepare: cudaErrorInvalidValue if no variant exists
+// for (bn, stages, out, pair), else its shared-memory size (and the attribute
+// set); gemm_kernel_ptr: the variant's host stub, or null.  A launch passes the
+// kernel the three tensor maps and the KParams block, in that order.
 cudaError_t gemm_prepare(int bn, int stages, int out, int pair, size_t* smem_bytes);
-cudaError_t gemm_launch(int bn, int stages, int out, int pair, const LaunchShape& shape,
-                        const CUtensorMap& tmap_a, const CUtensorMap& tmap_b,
-                        const CUtensorMap& tmap_c, const KParams& p, cudaStream_t stream);
+const void* gemm_kernel_ptr(int bn, int stages, int out, int pair);
 
 // Per output type (defined in gemm_inst.cuh, instantiated in gemm_inst_<type>.cu).
 template <int OUT>
 cudaError_t gemm_prepare_out(int bn, int stages, int pair, size_t* smem_bytes);
-template <int OUT>
-cudaError_t gemm_launch_out(int bn, int stages, int pair, const LaunchShape& shape,
-                            const CUtensorMap& tmap_a, const CUtensorMap& tmap_b,
-                            const CUtensorMap& tmap_c, const KParams& p, cudaStream_t stream);
 template <int OUT>
 const void* gemm_kernel_ptr_out(int bn, int stages, int pair);
 

@@ -332,3 +332,35 @@ def test_tuner_proposes_only_configs_the_library_accepts(gemm_lib):
             gemm_lib.gemm_workspace_bytes(M, N, K, dt, c)   # raises on a rejected config
             n += 1
     assert n > 10000
+
+
+def test_plan_runner_falls_back_to_the_general_path(gemm_lib):
+    """The C-level runner a Plan binds for run(A, B, C, stream) hands every call it
+    does not take itself (a closed plan, other argument counts, keywords) to the
+    general path with the same arguments; no GPU call is made here."""
+    gemm_lib.library()
+    pc = gemm_lib._pycall
+    if pc is None or not hasattr(pc, "Runner"):
+        pytest.skip("CPython entry points not built")
+    seen = []
+
+    def general(*args, **kwargs):
+        seen.append((args, kwargs))
+        return "general"
+
+    class T:
+        def data_ptr(self):
+            return 256
+
+    class S:
+        cuda_stream = 0
+
+    r = pc.Runner([None], general)                     # a closed plan
+    t, s = T(), S()
+    assert r(t, t, t, s) == "general" and seen[-1] == ((t, t, t, s), {})
+    assert r(t, t, t) == "general" and seen[-1] == ((t, t, t), {})
+    assert r(t, t, t, s, bias=None) == "general" and seen[-1] == ((t, t, t, s), {"bias": None})
+    with pytest.raises(TypeError):
+        pc.Runner([], general)
+    with pytest.raises(TypeError):
+        pc.Runner([None], 5)
