@@ -40,6 +40,7 @@ struct gemm_plan {
     int device;
     int num_sms;
     int out_kind;
+    int plain;                  // 1: the one-SM kernel's plain form serves the plan
     gbg::LaunchShape shape;
     gbg::KParams kp;
     PlanMemory mem;
@@ -385,9 +386,18 @@ gemm_status_t create_plan(int64_t M, int64_t N, int64_t K, gemm_dtype_t dtype,
     p->d_a16 = p->dmem + p->mem.a16_off;
     p->d_b16 = p->dmem + p->mem.b16_off;
 
+    // The one-SM kernel's plain form when the plan (fp16/bf16) uses none of the
+    // modes it fixes (K slices, multicast, per-thread stores, M/N-contiguous
+    // operands, an L2 prefetch distance): its launches reach their copies and
+    // stores sooner.
+    p->plain = (dtype != GEMM_I8_I32 && !cfg.cta_pair && cfg.split_k == 1 && cfg.multicast <= 1 &&
+                !cfg.direct_store && cfg.l2_prefetch == 0 && !a_mn_major(layout) &&
+                !b_mn_major(layout))
+                   ? 1
+                   : 0;
     size_t smem = 0;
     const cudaError_t prep =
-        gbg::gemm_prepare(cfg.block_n, cfg.stages, p->out_kind, cfg.cta_pair, &smem);
+        gbg::gemm_prepare(cfg.block_n, cfg.stages, p->out_kind, cfg.cta_pair, p->plain, &smem);
     if (prep != cudaSuccess) {
         cudaGetLastError();
         cudaFree(p->dmem);
@@ -466,7 +476,8 @@ gemm_status_t create_plan(int64_t M, int64_t N, int64_t K, gemm_dtype_t dtype,
     p->shape.smem_bytes = smem;
     if (kp.mcast > 1) {   // no more persistent clusters than fit on the GPU at once
         int fit = 0;
-        if (gbg::gemm_max_clusters(cfg.block_n, cfg.stages, p->out_kind, cfg.cta_pair, p->shape,
+        if (gbg::gemm_max_clusters(cfg.block_n, cfg.stages, p->out_kind, cfg.cta_pair, p->plain,
+                                   p->shape,
                                    &fit) == cudaSuccess && fit > 0) {
             if (p->shape.grid > fit * p->shape.cluster) p->shape.grid = fit * p->shape.cluster;
         } else {
@@ -474,7 +485,8 @@ gemm_status_t create_plan(int64_t M, int64_t N, int64_t K, gemm_dtype_t dtype,
         }
     }
 
-    const void* kernel = gbg::gemm_kernel_ptr(cfg.block_n, cfg.stages, p->out_kind, cfg.cta_pair);
+    const void* kernel =
+        gbg::gemm_kernel_ptr(cfg.block_n, cfg.stages, p->out_kind, cfg.cta_pair, p->plain);
     if (!kernel || cudaGetFuncBySymbol(&p->fn, kernel) != cudaSuccess || !launch_fn()) {
         cudaGetLastError();
         cudaFree(p->dmem);
@@ -520,27 +532,27 @@ gemm_status_t create_plan(int64_t M, int64_t N, int64_t K, gemm_dtype_t dtype,
 
 namespace gbg {
 
-cudaError_t gemm_prepare(int bn, int stages, int out, int pair, size_t* smem_bytes) {
+cudaError_t gemm_prepare(int bn, int stages, int out, int pair, int plain, size_t* smem_bytes) {
     switch (out) {
-        case kOutF16: return gemm_prepare_out<kOutF16>(bn, stages, pair, smem_bytes);
-        case kOutBF16: return gemm_prepare_out<kOutBF16>(bn, stages, pair, smem_bytes);
-        case kOutI32: return gemm_prepare_out<kOutI32>(bn, stages, pair, smem_bytes);
+        case kOutF16: return gemm_prepare_out<kOutF16>(bn, stages, pair, plain, smem_bytes);
+        case kOutBF16: return gemm_prepare_out<kOutBF16>(bn, stages, pair, plain, smem_bytes);
+        case kOutI32: return gemm_prepare_out<kOutI32>(bn, stages, pair, plain, smem_bytes);
         default: return cudaErrorInvalidValue;
     }
 }
 
-const void* gemm_kernel_ptr(int bn, int stages, int out, int pair) {
+const void* gemm_kernel_ptr(int bn, int stages, int out, int pair, int plain) {
     switch (out) {
-        case kOutF16: return gemm_kernel_ptr_out<kOutF16>(bn, stages, pair);
-        case kOutBF16: return gemm_kernel_ptr_out<kOutBF16>(bn, stages, pair);
-        case kOutI32: return gemm_kernel_ptr_out<kOutI32>(bn, stages, pair);
+        case kOutF16: return gemm_kernel_ptr_out<kOutF16>(bn, stages, pair, plain);
+        case kOutBF16: return gemm_kernel_ptr_out<kOutBF16>(bn, stages, pair, plain);
+        case kOutI32: return gemm_kernel_ptr_out<kOutI32>(bn, stages, pair, plain);
         default: return nullptr;
     }
 }
 
-cudaError_t gemm_max_clusters(int bn, int stages, int out, int pair, const LaunchShape& shape,
-                              int* n) {
-    const void* fn = gemm_kernel_ptr(bn, stages, out, pair);
+cudaError_t gemm_max_clusters(int bn, int stages, int out, int pair, int plain,
+                              const LaunchShape& shape, int* n) {
+    const void* fn = gemm_kernel_ptr(bn, stages, out, pair, plain);
     if (!fn) return cudaErrorInvalidValue;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(shape.grid));
@@ -705,7 +717,7 @@ gemm_status_t gemm_plan_get_launch(gemm_plan_t p, int32_t* grid, int32_t* cluste
         cudaGetDevice(&prev);
         if (prev != p->device) cudaSetDevice(p->device);
         if (gbg::gemm_max_clusters(p->cfg.block_n, p->cfg.stages, p->out_kind, p->cfg.cta_pair,
-                                   p->shape, &n) != cudaSuccess) {
+                                   p->plain, p->shape, &n) != cudaSuccess) {
             cudaGetLastError();
             n = 0;
         }

@@ -30,12 +30,12 @@ constexpr bool one_sm_ok() { return OUT != kOutI32 || BN <= 128; }
 template <int OUT, int BN>
 constexpr bool pair_ok() { return true; }
 
-template <bool PAIR, int BN, int STAGES, int OUT, int KS>
+template <bool PAIR, int BN, int STAGES, int OUT, int KS, bool PLAIN>
 const void* kernel_fn() {
     if constexpr (PAIR)
         return reinterpret_cast<const void*>(gemm_tn_pair_kernel<BN, STAGES, OUT, KS>);
     else
-        return reinterpret_cast<const void*>(gemm_tn_kernel<BN, STAGES, OUT, KS>);
+        return reinterpret_cast<const void*>(gemm_tn_kernel<BN, STAGES, OUT, KS, PLAIN>);
 }
 
 template <bool PAIR, int BN, int STAGES, int KS>
@@ -46,46 +46,52 @@ constexpr size_t smem_bytes() {
         return SmemLayout<BN, STAGES, KS>::kTotal;
 }
 
-template <bool PAIR, int BN, int STAGES, int OUT, int KS>
+template <bool PAIR, int BN, int STAGES, int OUT, int KS, bool PLAIN>
 cudaError_t prepare(size_t* smem) {
     *smem = smem_bytes<PAIR, BN, STAGES, KS>();
-    if constexpr (PAIR)
-        return cudaFuncSetAttribute(gemm_tn_pair_kernel<BN, STAGES, OUT, KS>,
-                                    cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                    static_cast<int>(*smem));
-    else
-        return cudaFuncSetAttribute(gemm_tn_kernel<BN, STAGES, OUT, KS>,
-                                    cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                    static_cast<int>(*smem));
+    return cudaFuncSetAttribute(kernel_fn<PAIR, BN, STAGES, OUT, KS, PLAIN>(),
+                                cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                static_cast<int>(*smem));
 }
 
 }  // namespace inst
 
+// `plain` selects the one-SM kernel's plain form (gemm_tn_kernel<..., true>,
+// fp16/bf16 output; the integer mode's register sums leave it no room); the
+// SM-pair kernel has one form.
 template <int OUT>
-cudaError_t gemm_prepare_out(int bn, int stages, int pair, size_t* smem) {
-#define X(B, S, K)                                                          \
-    if constexpr (inst::one_sm_ok<OUT, B>())                                \
-        if (!pair && bn == B && stages == S) return inst::prepare<false, B, S, OUT, K>(smem);
+cudaError_t gemm_prepare_out(int bn, int stages, int pair, int plain, size_t* smem) {
+#define X(B, S, K)                                                              \
+    if constexpr (inst::one_sm_ok<OUT, B>())                                    \
+        if (!pair && bn == B && stages == S) {                                  \
+            if constexpr (OUT != kOutI32)                                       \
+                if (plain) return inst::prepare<false, B, S, OUT, K, true>(smem); \
+            return inst::prepare<false, B, S, OUT, K, false>(smem);             \
+        }
     GBG_ONE_SM_VARIANTS(X)
 #undef X
-#define X(B, S, K)                                                          \
-    if constexpr (inst::pair_ok<OUT, B>())                                  \
-        if (pair && bn == B && stages == S) return inst::prepare<true, B, S, OUT, K>(smem);
+#define X(B, S, K)                                                              \
+    if constexpr (inst::pair_ok<OUT, B>())                                      \
+        if (pair && bn == B && stages == S) return inst::prepare<true, B, S, OUT, K, false>(smem);
     GBG_PAIR_VARIANTS(X)
 #undef X
     return cudaErrorInvalidValue;
 }
 
 template <int OUT>
-const void* gemm_kernel_ptr_out(int bn, int stages, int pair) {
-#define X(B, S, K)                                                          \
-    if constexpr (inst::one_sm_ok<OUT, B>())                                \
-        if (!pair && bn == B && stages == S) return inst::kernel_fn<false, B, S, OUT, K>();
+const void* gemm_kernel_ptr_out(int bn, int stages, int pair, int plain) {
+#define X(B, S, K)                                                              \
+    if constexpr (inst::one_sm_ok<OUT, B>())                                    \
+        if (!pair && bn == B && stages == S) {                                  \
+            if constexpr (OUT != kOutI32)                                       \
+                if (plain) return inst::kernel_fn<false, B, S, OUT, K, true>(); \
+            return inst::kernel_fn<false, B, S, OUT, K, false>();               \
+        }
     GBG_ONE_SM_VARIANTS(X)
 #undef X
-#define X(B, S, K)                                                          \
-    if constexpr (inst::pair_ok<OUT, B>())                                  \
-        if (pair && bn == B && stages == S) return inst::kernel_fn<true, B, S, OUT, K>();
+#define X(B, S, K)                                                              \
+    if constexpr (inst::pair_ok<OUT, B>())                                      \
+        if (pair && bn == B && stages == S) return inst::kernel_fn<true, B, S, OUT, K, false>();
     GBG_PAIR_VARIANTS(X)
 #undef X
     return nullptr;
@@ -93,7 +99,7 @@ const void* gemm_kernel_ptr_out(int bn, int stages, int pair) {
 
 // One explicit instantiation per output type, in that type's translation unit.
 #define GBG_INSTANTIATE_OUTPUT(OUT)                                                        \
-    template cudaError_t gemm_prepare_out<OUT>(int, int, int, size_t*);                   \
-    template const void* gemm_kernel_ptr_out<OUT>(int, int, int);
+    template cudaError_t gemm_prepare_out<OUT>(int, int, int, int, size_t*);              \
+    template const void* gemm_kernel_ptr_out<OUT>(int, int, int, int);
 
 }  // namespace gbg

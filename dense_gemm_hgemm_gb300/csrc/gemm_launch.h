@@ -32,23 +32,24 @@ struct LaunchShape {
 };
 
 // Kernel variant lookup.  `out` is kOutF16 / kOutBF16 / kOutI32, `pair` = 1 for
-// the SM-pair kernel.  gemm_prepare: cudaErrorInvalidValue if no variant exists
-// for (bn, stages, out, pair), else its shared-memory size (and the attribute
-// set); gemm_kernel_ptr: the variant's host stub, or null.  A launch passes the
+// the SM-pair kernel, `plain` = 1 for the one-SM kernel's plain form (one K
+// slice, no multicast, TMA stores, K-contiguous operands, no L2 prefetch
+// distance).  gemm_prepare: cudaErrorInvalidValue if no variant exists for
+// (bn, stages, out, pair), else its shared-memory size (and the attribute set);
+// gemm_kernel_ptr: the variant's host stub, or null.  A launch passes the
 // kernel the three tensor maps and the KParams block, in that order.
-cudaError_t gemm_prepare(int bn, int stages, int out, int pair, size_t* smem_bytes);
-const void* gemm_kernel_ptr(int bn, int stages, int out, int pair);
+cudaError_t gemm_prepare(int bn, int stages, int out, int pair, int plain, size_t* smem_bytes);
+const void* gemm_kernel_ptr(int bn, int stages, int out, int pair, int plain);
 
 // Per output type (defined in gemm_inst.cuh, instantiated in gemm_inst_<type>.cu).
 template <int OUT>
-cudaError_t gemm_prepare_out(int bn, int stages, int pair, size_t* smem_bytes);
+cudaError_t gemm_prepare_out(int bn, int stages, int pair, int plain, size_t* smem_bytes);
 template <int OUT>
-const void* gemm_kernel_ptr_out(int bn, int stages, int pair);
+const void* gemm_kernel_ptr_out(int bn, int stages, int pair, int plain);
 
-// Co-resident clusters of shape.cluster CTAs of a kernel variant (pair = 1: the
-// SM-pair kernel).
-cudaError_t gemm_max_clusters(int bn, int stages, int out, int pair, const LaunchShape& shape,
-                              int* n);
+// Co-resident clusters of shape.cluster CTAs of a kernel variant.
+cudaError_t gemm_max_clusters(int bn, int stages, int out, int pair, int plain,
+                              const LaunchShape& shape, int* n);
 
 // Auxiliary kernels (gemm_aux.cu).
 cudaError_t launch_widen_i8(const int8_t* a, int64_t na, const int8_t* b, int64_t nb, void* a16,
