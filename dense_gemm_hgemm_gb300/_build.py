@@ -21,7 +21,8 @@ BUILD_DIR = os.path.join(ROOT, "_build")
 LIB_PATH = os.path.join(PKG, "libgemm_gb300.so")
 
 SOURCES = ["gemm_api.cu", "gemm_aux.cu", "gemm_inst_f16.cu", "gemm_inst_bf16.cu",
-           "gemm_inst_i32.cu", "gemm_noalloc.cu", "gemm_probe.cu", "tma_intensity.cu"]
+           "gemm_inst_i32.cu", "gemm_inst_f16_pair.cu", "gemm_inst_bf16_pair.cu",
+           "gemm_inst_i32_pair.cu", "gemm_noalloc.cu", "gemm_probe.cu", "tma_intensity.cu"]
 PYCALL_SRC = os.path.join(CSRC, "gemm_pycall.c")
 PYCALL_PATH = os.path.join(PKG, "_gemm_pycall" + (sysconfig.get_config_var("EXT_SUFFIX") or ".so"))
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]

@@ -40,7 +40,7 @@ struct gemm_plan {
     int device;
     int num_sms;
     int out_kind;
-    int plain;                  // 1: the one-SM kernel's plain form serves the plan
+    int form;                   // the kernel's compiled form (gbg::KernelForm) for the plan
     gbg::LaunchShape shape;
     gbg::KParams kp;
     PlanMemory mem;
@@ -386,18 +386,30 @@ gemm_status_t create_plan(int64_t M, int64_t N, int64_t K, gemm_dtype_t dtype,
     p->d_a16 = p->dmem + p->mem.a16_off;
     p->d_b16 = p->dmem + p->mem.b16_off;
 
-    // The one-SM kernel's plain form when the plan (fp16/bf16) uses none of the
-    // modes it fixes (K slices, multicast, per-thread stores, M/N-contiguous
-    // operands, an L2 prefetch distance): its launches reach their copies and
-    // stores sooner.
-    p->plain = (dtype != GEMM_I8_I32 && !cfg.cta_pair && cfg.split_k == 1 && cfg.multicast <= 1 &&
-                !cfg.direct_store && cfg.l2_prefetch == 0 && !a_mn_major(layout) &&
-                !b_mn_major(layout))
-                   ? 1
-                   : 0;
+    // The kernel's compiled form: plain (or, for one-SM K slices in a cluster,
+    // cluster split) when the plan uses none of the modes that form fixes
+    // (multicast, per-thread stores, M/N-contiguous operands, an L2 prefetch
+    // distance, four k-blocks per slot); its launches reach their copies and
+    // stores sooner.  The one-SM integer mode and 128-wide integer SM-pair tiles
+    // have the general form only.
+    {
+        const bool fixed_ok = cfg.multicast <= 1 && !cfg.direct_store && cfg.l2_prefetch == 0 &&
+                              !a_mn_major(layout) && !b_mn_major(layout) &&
+                              cfg.kblocks_per_stage != 4;
+        p->form = gbg::kFormGeneral;
+        if (fixed_ok && cfg.cta_pair) {
+            if (cfg.split_k == 1 && !(dtype == GEMM_I8_I32 && cfg.block_n == 128))
+                p->form = gbg::kFormPlain;
+        } else if (fixed_ok && dtype != GEMM_I8_I32) {
+            if (cfg.split_k == 1)
+                p->form = gbg::kFormPlain;
+            else if (cfg.split_mode == 1)
+                p->form = gbg::kFormClusterSplit;
+        }
+    }
     size_t smem = 0;
     const cudaError_t prep =
-        gbg::gemm_prepare(cfg.block_n, cfg.stages, p->out_kind, cfg.cta_pair, p->plain, &smem);
+        gbg::gemm_prepare(cfg.block_n, cfg.stages, p->out_kind, cfg.cta_pair, p->form, &smem);
     if (prep != cudaSuccess) {
         cudaGetLastError();
         cudaFree(p->dmem);
@@ -476,7 +488,7 @@ gemm_status_t create_plan(int64_t M, int64_t N, int64_t K, gemm_dtype_t dtype,
     p->shape.smem_bytes = smem;
     if (kp.mcast > 1) {   // no more persistent clusters than fit on the GPU at once
         int fit = 0;
-        if (gbg::gemm_max_clusters(cfg.block_n, cfg.stages, p->out_kind, cfg.cta_pair, p->plain,
+        if (gbg::gemm_max_clusters(cfg.block_n, cfg.stages, p->out_kind, cfg.cta_pair, p->form,
                                    p->shape,
                                    &fit) == cudaSuccess && fit > 0) {
             if (p->shape.grid > fit * p->shape.cluster) p->shape.grid = fit * p->shape.cluster;
@@ -486,7 +498,7 @@ gemm_status_t create_plan(int64_t M, int64_t N, int64_t K, gemm_dtype_t dtype,
     }
 
     const void* kernel =
-        gbg::gemm_kernel_ptr(cfg.block_n, cfg.stages, p->out_kind, cfg.cta_pair, p->plain);
+        gbg::gemm_kernel_ptr(cfg.block_n, cfg.stages, p->out_kind, cfg.cta_pair, p->form);
     if (!kernel || cudaGetFuncBySymbol(&p->fn, kernel) != cudaSuccess || !launch_fn()) {
         cudaGetLastError();
         cudaFree(p->dmem);
@@ -532,27 +544,41 @@ gemm_status_t create_plan(int64_t M, int64_t N, int64_t K, gemm_dtype_t dtype,
 
 namespace gbg {
 
-cudaError_t gemm_prepare(int bn, int stages, int out, int pair, int plain, size_t* smem_bytes) {
+namespace {
+
+const void* variant(int bn, int stages, int out, int pair, int form, size_t* smem,
+                    cudaError_t* st) {
     switch (out) {
-        case kOutF16: return gemm_prepare_out<kOutF16>(bn, stages, pair, plain, smem_bytes);
-        case kOutBF16: return gemm_prepare_out<kOutBF16>(bn, stages, pair, plain, smem_bytes);
-        case kOutI32: return gemm_prepare_out<kOutI32>(bn, stages, pair, plain, smem_bytes);
-        default: return cudaErrorInvalidValue;
+        case kOutF16:
+            return pair ? gemm_variant_pair<kOutF16>(bn, stages, form, smem, st)
+                        : gemm_variant_one_sm<kOutF16>(bn, stages, form, smem, st);
+        case kOutBF16:
+            return pair ? gemm_variant_pair<kOutBF16>(bn, stages, form, smem, st)
+                        : gemm_variant_one_sm<kOutBF16>(bn, stages, form, smem, st);
+        case kOutI32:
+            return pair ? gemm_variant_pair<kOutI32>(bn, stages, form, smem, st)
+                        : gemm_variant_one_sm<kOutI32>(bn, stages, form, smem, st);
+        default:
+            if (smem) *st = cudaErrorInvalidValue;
+            return nullptr;
     }
 }
 
-const void* gemm_kernel_ptr(int bn, int stages, int out, int pair, int plain) {
-    switch (out) {
-        case kOutF16: return gemm_kernel_ptr_out<kOutF16>(bn, stages, pair, plain);
-        case kOutBF16: return gemm_kernel_ptr_out<kOutBF16>(bn, stages, pair, plain);
-        case kOutI32: return gemm_kernel_ptr_out<kOutI32>(bn, stages, pair, plain);
-        default: return nullptr;
-    }
+}  // namespace
+
+cudaError_t gemm_prepare(int bn, int stages, int out, int pair, int form, size_t* smem_bytes) {
+    cudaError_t st = cudaErrorInvalidValue;
+    const void* fn = variant(bn, stages, out, pair, form, smem_bytes, &st);
+    return fn ? st : cudaErrorInvalidValue;
 }
 
-cudaError_t gemm_max_clusters(int bn, int stages, int out, int pair, int plain,
+const void* gemm_kernel_ptr(int bn, int stages, int out, int pair, int form) {
+    return variant(bn, stages, out, pair, form, nullptr, nullptr);
+}
+
+cudaError_t gemm_max_clusters(int bn, int stages, int out, int pair, int form,
                               const LaunchShape& shape, int* n) {
-    const void* fn = gemm_kernel_ptr(bn, stages, out, pair, plain);
+    const void* fn = gemm_kernel_ptr(bn, stages, out, pair, form);
     if (!fn) return cudaErrorInvalidValue;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(shape.grid));
@@ -717,7 +743,7 @@ gemm_status_t gemm_plan_get_launch(gemm_plan_t p, int32_t* grid, int32_t* cluste
         cudaGetDevice(&prev);
         if (prev != p->device) cudaSetDevice(p->device);
         if (gbg::gemm_max_clusters(p->cfg.block_n, p->cfg.stages, p->out_kind, p->cfg.cta_pair,
-                                   p->plain, p->shape, &n) != cudaSuccess) {
+                                   p->form, p->shape, &n) != cudaSuccess) {
             cudaGetLastError();
             n = 0;
         }

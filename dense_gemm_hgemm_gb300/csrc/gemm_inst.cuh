@@ -1,15 +1,19 @@
 // gemm_inst.cuh -- the kernel variants (shared-memory set-up and host stub of
-// each), one template per output type (gemm_inst_f16.cu, gemm_inst_bf16.cu and
-// gemm_inst_i32.cu each instantiate it once, so the three compile in parallel).
-// The launches themselves go through the plan's driver function handle.
+// each), one template per output type and kernel: gemm_inst_<type>.cu and
+// gemm_inst_<type>_pair.cu instantiate the one-SM and the SM-pair half for fp16,
+// bf16 and int32 output, so the six compile in parallel.  The launches
+// themselves go through the plan's driver function handle.
 //
 // A variant is (tile width BN, ring depth STAGES, k-blocks per slot KS) of the
 // one-SM kernel or of the SM-pair kernel; (BN, STAGES) identifies it, because
-// every KS has its own depth for a given BN.  The integer output mode keeps its int32 sums
-// in registers: the one-SM kernel has the narrower variants only, the SM-pair kernel all of
-// them (224/256-wide integer tiles with eight epilogue warps).  The 224-wide SM-pair tile
-// (K-contiguous B, no K split or multicast) fills the last wave of SM pairs on shapes whose
-// 256-wide tile count leaves most of it idle.
+// every KS has its own depth for a given BN.  Each variant is compiled in the
+// general form and, where a plan can use them, in the plain and cluster-split
+// forms (KernelForm).  The integer output mode keeps its int32 sums in
+// registers: the one-SM kernel has the narrower variants only, and only the
+// general form (the plain forms spill there); the SM-pair kernel has them all
+// (224/256-wide integer tiles with eight epilogue warps).  The 224-wide SM-pair
+// tile (K-contiguous B, no K split or multicast) fills the last wave of SM pairs
+// on shapes whose 256-wide tile count leaves most of it idle.
 #pragma once
 
 #include "gemm_kernel.cuh"
@@ -27,15 +31,26 @@ namespace inst {
 
 template <int OUT, int BN>
 constexpr bool one_sm_ok() { return OUT != kOutI32 || BN <= 128; }
-template <int OUT, int BN>
-constexpr bool pair_ok() { return true; }
+// Forms compiled per one-SM variant: the four-k-block variant (never chosen by
+// the table) and the integer mode have the general form only.
+template <int OUT, int KS, int FORM>
+constexpr bool one_sm_form_ok() {
+    return FORM == kFormGeneral || (OUT != kOutI32 && KS != 4);
+}
+// (the 128-wide integer tiles, whose register sums already spill a little in the
+// general form, have that form only)
+template <int OUT, int BN, int KS, int FORM>
+constexpr bool pair_form_ok() {
+    return FORM == kFormGeneral ||
+           (FORM == kFormPlain && KS != 4 && !(OUT == kOutI32 && BN == 128));
+}
 
-template <bool PAIR, int BN, int STAGES, int OUT, int KS, bool PLAIN>
+template <bool PAIR, int BN, int STAGES, int OUT, int KS, int FORM>
 const void* kernel_fn() {
     if constexpr (PAIR)
-        return reinterpret_cast<const void*>(gemm_tn_pair_kernel<BN, STAGES, OUT, KS>);
+        return reinterpret_cast<const void*>(gemm_tn_pair_kernel<BN, STAGES, OUT, KS, FORM>);
     else
-        return reinterpret_cast<const void*>(gemm_tn_kernel<BN, STAGES, OUT, KS, PLAIN>);
+        return reinterpret_cast<const void*>(gemm_tn_kernel<BN, STAGES, OUT, KS, FORM>);
 }
 
 template <bool PAIR, int BN, int STAGES, int KS>
@@ -46,60 +61,61 @@ constexpr size_t smem_bytes() {
         return SmemLayout<BN, STAGES, KS>::kTotal;
 }
 
-template <bool PAIR, int BN, int STAGES, int OUT, int KS, bool PLAIN>
+template <bool PAIR, int BN, int STAGES, int OUT, int KS, int FORM>
 cudaError_t prepare(size_t* smem) {
     *smem = smem_bytes<PAIR, BN, STAGES, KS>();
-    return cudaFuncSetAttribute(kernel_fn<PAIR, BN, STAGES, OUT, KS, PLAIN>(),
+    return cudaFuncSetAttribute(kernel_fn<PAIR, BN, STAGES, OUT, KS, FORM>(),
                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
                                 static_cast<int>(*smem));
 }
 
 }  // namespace inst
 
-// `plain` selects the one-SM kernel's plain form (gemm_tn_kernel<..., true>,
-// fp16/bf16 output; the integer mode's register sums leave it no room); the
-// SM-pair kernel has one form.
-template <int OUT>
-cudaError_t gemm_prepare_out(int bn, int stages, int pair, int plain, size_t* smem) {
-#define X(B, S, K)                                                              \
-    if constexpr (inst::one_sm_ok<OUT, B>())                                    \
-        if (!pair && bn == B && stages == S) {                                  \
-            if constexpr (OUT != kOutI32)                                       \
-                if (plain) return inst::prepare<false, B, S, OUT, K, true>(smem); \
-            return inst::prepare<false, B, S, OUT, K, false>(smem);             \
-        }
-    GBG_ONE_SM_VARIANTS(X)
-#undef X
-#define X(B, S, K)                                                              \
-    if constexpr (inst::pair_ok<OUT, B>())                                      \
-        if (pair && bn == B && stages == S) return inst::prepare<true, B, S, OUT, K, false>(smem);
-    GBG_PAIR_VARIANTS(X)
-#undef X
-    return cudaErrorInvalidValue;
-}
+// One kernel's variants: the host stub of (bn, stages, form) and, with `smem`
+// non-null, its shared-memory size with the attribute set.  cudaErrorInvalidValue
+// (stub: null) for a combination that is not compiled.
+#define GBG_FORM_CASE(PAIR, B, S, K, F)                                         \
+    if (form == F) {                                                            \
+        if (smem) *st = inst::prepare<PAIR, B, S, OUT, K, F>(smem);             \
+        return inst::kernel_fn<PAIR, B, S, OUT, K, F>();                        \
+    }
 
 template <int OUT>
-const void* gemm_kernel_ptr_out(int bn, int stages, int pair, int plain) {
+const void* gemm_variant_one_sm(int bn, int stages, int form, size_t* smem, cudaError_t* st) {
 #define X(B, S, K)                                                              \
     if constexpr (inst::one_sm_ok<OUT, B>())                                    \
-        if (!pair && bn == B && stages == S) {                                  \
-            if constexpr (OUT != kOutI32)                                       \
-                if (plain) return inst::kernel_fn<false, B, S, OUT, K, true>(); \
-            return inst::kernel_fn<false, B, S, OUT, K, false>();               \
+        if (bn == B && stages == S) {                                           \
+            if constexpr (inst::one_sm_form_ok<OUT, K, kFormPlain>())           \
+                GBG_FORM_CASE(false, B, S, K, kFormPlain)                       \
+            if constexpr (inst::one_sm_form_ok<OUT, K, kFormClusterSplit>())    \
+                GBG_FORM_CASE(false, B, S, K, kFormClusterSplit)                \
+            GBG_FORM_CASE(false, B, S, K, kFormGeneral)                         \
         }
     GBG_ONE_SM_VARIANTS(X)
 #undef X
-#define X(B, S, K)                                                              \
-    if constexpr (inst::pair_ok<OUT, B>())                                      \
-        if (pair && bn == B && stages == S) return inst::kernel_fn<true, B, S, OUT, K, false>();
-    GBG_PAIR_VARIANTS(X)
-#undef X
+    if (smem) *st = cudaErrorInvalidValue;
     return nullptr;
 }
 
-// One explicit instantiation per output type, in that type's translation unit.
-#define GBG_INSTANTIATE_OUTPUT(OUT)                                                        \
-    template cudaError_t gemm_prepare_out<OUT>(int, int, int, int, size_t*);              \
-    template const void* gemm_kernel_ptr_out<OUT>(int, int, int, int);
+template <int OUT>
+const void* gemm_variant_pair(int bn, int stages, int form, size_t* smem, cudaError_t* st) {
+#define X(B, S, K)                                                              \
+    if (bn == B && stages == S) {                                               \
+        if constexpr (inst::pair_form_ok<OUT, B, K, kFormPlain>())              \
+            GBG_FORM_CASE(true, B, S, K, kFormPlain)                            \
+        GBG_FORM_CASE(true, B, S, K, kFormGeneral)                              \
+    }
+    GBG_PAIR_VARIANTS(X)
+#undef X
+    if (smem) *st = cudaErrorInvalidValue;
+    return nullptr;
+}
+#undef GBG_FORM_CASE
+
+// One explicit instantiation per output type and kernel, in its own translation unit.
+#define GBG_INSTANTIATE_ONE_SM(OUT) \
+    template const void* gemm_variant_one_sm<OUT>(int, int, int, size_t*, cudaError_t*);
+#define GBG_INSTANTIATE_PAIR(OUT) \
+    template const void* gemm_variant_pair<OUT>(int, int, int, size_t*, cudaError_t*);
 
 }  // namespace gbg

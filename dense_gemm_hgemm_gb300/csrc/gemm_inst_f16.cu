@@ -1,6 +1,6 @@
-// gemm_inst_f16.cu -- the kernel variants with fp16 output (see gemm_inst.cuh).
+// gemm_inst_f16.cu -- the one-SM kernel variants with fp16 output (see gemm_inst.cuh).
 #include "gemm_inst.cuh"
 
 namespace gbg {
-GBG_INSTANTIATE_OUTPUT(kOutF16)
+GBG_INSTANTIATE_ONE_SM(kOutF16)
 }  // namespace gbg

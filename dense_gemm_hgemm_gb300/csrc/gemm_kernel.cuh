@@ -843,37 +843,46 @@ __device__ __forceinline__ UnitCoord unit_at(const KParams& p, int32_t u) {
     return c;
 }
 
-// The plain form of the kernel's parameters: one K slice, no multicast, TMA
-// stores, both operands K-contiguous, no L2 prefetch distance.  With these as
-// compile-time constants the paths for the other modes compile away, and a
+// The kernel's parameters in compiled form FORM (see KernelForm): the fields the
+// form fixes are constants, so the paths of the other modes compile away.  A
 // launch's chain from the dependency release to its last exit is ~0.75 us
-// shorter for a one-tile GEMM (2.33 -> 1.58 us, 64x64x64 on GB300: the code
-// each role runs first after the wait is smaller and branch-free).
-__device__ __forceinline__ KParams plain_params(const KParams& in) {
-    KParams p = in;
-    p.split_k = 1;
-    p.cluster_split = 0;
-    p.mcast = 1;
-    p.mcast_shift = 0;
-    p.direct_store = 0;
-    p.l2_prefetch = 0;
-    p.a_mn_major = 0;
-    p.b_mn_major = 0;
-    return p;
+// shorter in the plain form for a one-tile GEMM (2.33 -> 1.58 us, 64x64x64 on
+// GB300: the code each role runs first after the wait is smaller and has no
+// mode branches).
+template <int FORM>
+__device__ __forceinline__ KParams form_params(const KParams& in) {
+    if constexpr (FORM == kFormGeneral) {
+        return in;
+    } else {
+        KParams p = in;
+        p.mcast = 1;
+        p.mcast_shift = 0;
+        p.direct_store = 0;
+        p.l2_prefetch = 0;
+        p.a_mn_major = 0;
+        p.b_mn_major = 0;
+        if constexpr (FORM == kFormPlain) {
+            p.split_k = 1;
+            p.cluster_split = 0;
+        } else {
+            p.cluster_split = 1;   // split_k (2, 4 or 8) stays a run-time value
+        }
+        return p;
+    }
 }
 
 // ----------------------------------------------------------------------------
 // the kernel
 // ----------------------------------------------------------------------------
 // KS > 1: each K-major operand's map is the 3-D view (the host guarantees it
-// and K % 64 == 0; multicast is not combined with it).  PLAIN: the plan uses
-// none of the modes plain_params fixes (the host picks this form then).
-template <int BN, int STAGES, int OUT, int KS = 1, bool PLAIN = false>
+// and K % 64 == 0; multicast is not combined with it).  FORM: a KernelForm whose
+// fixed fields match the plan's (the host picks the form).
+template <int BN, int STAGES, int OUT, int KS = 1, int FORM = kFormGeneral>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_tn_kernel(const __grid_constant__ CUtensorMap tmap_a,
                    const __grid_constant__ CUtensorMap tmap_b,
                    const __grid_constant__ CUtensorMap tmap_c, const KParams p_in) {
-    const KParams p = PLAIN ? plain_params(p_in) : p_in;
+    const KParams p = form_params<FORM>(p_in);
     using L = SmemLayout<BN, STAGES, KS>;
     static_assert(KS == 1 || KS == 2 || KS == 4, "k-blocks per ring slot");
     static_assert((OUT == kOutI32 ? 2 : 1) * SplitRecv<BN>::kBytes <= L::kRingBytes,

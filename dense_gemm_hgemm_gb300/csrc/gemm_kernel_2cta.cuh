@@ -202,11 +202,14 @@ __device__ __forceinline__ uint32_t ld_dsmem_u32(uint32_t cluster_addr) {
     return v;
 }
 
-template <int BN, int STAGES, int OUT, int KS = 1>
+// FORM: kFormGeneral or kFormPlain (see KernelForm; the host picks it).
+template <int BN, int STAGES, int OUT, int KS = 1, int FORM = kFormGeneral>
 __global__ void __launch_bounds__(64 + 32 * kPairEpiWarps<BN, OUT>, 1)
     gemm_tn_pair_kernel(const __grid_constant__ CUtensorMap tmap_a,
                         const __grid_constant__ CUtensorMap tmap_b,
-                        const __grid_constant__ CUtensorMap tmap_c, const KParams p) {
+                        const __grid_constant__ CUtensorMap tmap_c, const KParams p_in) {
+    static_assert(FORM == kFormGeneral || FORM == kFormPlain, "SM-pair kernel forms");
+    const KParams p = form_params<FORM>(p_in);
     using L = SmemLayout2<BN, STAGES, KS>;
     static_assert(KS == 1 || KS == 2 || KS == 4, "k-blocks per ring slot");
     // integer tiles wider than 128: eight epilogue warps, one store buffer each

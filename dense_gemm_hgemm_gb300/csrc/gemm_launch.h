@@ -32,23 +32,24 @@ struct LaunchShape {
 };
 
 // Kernel variant lookup.  `out` is kOutF16 / kOutBF16 / kOutI32, `pair` = 1 for
-// the SM-pair kernel, `plain` = 1 for the one-SM kernel's plain form (one K
-// slice, no multicast, TMA stores, K-contiguous operands, no L2 prefetch
-// distance).  gemm_prepare: cudaErrorInvalidValue if no variant exists for
-// (bn, stages, out, pair), else its shared-memory size (and the attribute set);
-// gemm_kernel_ptr: the variant's host stub, or null.  A launch passes the
-// kernel the three tensor maps and the KParams block, in that order.
-cudaError_t gemm_prepare(int bn, int stages, int out, int pair, int plain, size_t* smem_bytes);
-const void* gemm_kernel_ptr(int bn, int stages, int out, int pair, int plain);
+// the SM-pair kernel, `form` a KernelForm.  gemm_prepare: cudaErrorInvalidValue
+// if the variant (bn, stages, out, pair, form) is not compiled, else its
+// shared-memory size (and the attribute set); gemm_kernel_ptr: the variant's
+// host stub, or null.  A launch passes the kernel the three tensor maps and the
+// KParams block, in that order.
+cudaError_t gemm_prepare(int bn, int stages, int out, int pair, int form, size_t* smem_bytes);
+const void* gemm_kernel_ptr(int bn, int stages, int out, int pair, int form);
 
-// Per output type (defined in gemm_inst.cuh, instantiated in gemm_inst_<type>.cu).
+// Per output type and kernel (defined in gemm_inst.cuh, instantiated in
+// gemm_inst_<type>.cu and gemm_inst_<type>_pair.cu): the host stub, and with
+// `smem` non-null the shared-memory size and the attribute's status in *st.
 template <int OUT>
-cudaError_t gemm_prepare_out(int bn, int stages, int pair, int plain, size_t* smem_bytes);
+const void* gemm_variant_one_sm(int bn, int stages, int form, size_t* smem, cudaError_t* st);
 template <int OUT>
-const void* gemm_kernel_ptr_out(int bn, int stages, int pair, int plain);
+const void* gemm_variant_pair(int bn, int stages, int form, size_t* smem, cudaError_t* st);
 
 // Co-resident clusters of shape.cluster CTAs of a kernel variant.
-cudaError_t gemm_max_clusters(int bn, int stages, int out, int pair, int plain,
+cudaError_t gemm_max_clusters(int bn, int stages, int out, int pair, int form,
                               const LaunchShape& shape, int* n);
 
 // Auxiliary kernels (gemm_aux.cu).
