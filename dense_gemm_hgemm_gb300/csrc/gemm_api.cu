@@ -59,6 +59,7 @@ struct gemm_plan {
     // kernel's driver function handle, grid / block / shared memory, programmatic
     // dependent launch and the cluster shape.
     CUfunction fn;
+    CUfunction fn_epilogue;     // the general form, for calls with a fused bias or activation
     CUlaunchConfig launch;
     CUlaunchAttribute launch_attr[2];
 };
@@ -499,7 +500,14 @@ gemm_status_t create_plan(int64_t M, int64_t N, int64_t K, gemm_dtype_t dtype,
 
     const void* kernel =
         gbg::gemm_kernel_ptr(cfg.block_n, cfg.stages, p->out_kind, cfg.cta_pair, p->form);
-    if (!kernel || cudaGetFuncBySymbol(&p->fn, kernel) != cudaSuccess || !launch_fn()) {
+    const void* kernel_epi =
+        gbg::gemm_kernel_ptr(cfg.block_n, cfg.stages, p->out_kind, cfg.cta_pair, gbg::kFormGeneral);
+    size_t smem_epi = 0;
+    if (!kernel || !kernel_epi || cudaGetFuncBySymbol(&p->fn, kernel) != cudaSuccess ||
+        cudaGetFuncBySymbol(&p->fn_epilogue, kernel_epi) != cudaSuccess || !launch_fn() ||
+        (p->form != gbg::kFormGeneral &&
+         gbg::gemm_prepare(cfg.block_n, cfg.stages, p->out_kind, cfg.cta_pair, gbg::kFormGeneral,
+                           &smem_epi) != cudaSuccess)) {
         cudaGetLastError();
         cudaFree(p->dmem);
         delete p;
@@ -690,9 +698,11 @@ gemm_status_t gemm_run_bias_act(gemm_plan_t p, const void* A, const void* B, voi
     p->kp.act = static_cast<int32_t>(act);
     void* args[4] = {&p->map_a, &p->map_b, &p->map_c, &p->kp};
     p->launch.hStream = reinterpret_cast<CUstream>(stream);
-    CUresult r = launch_fn()(&p->launch, p->fn, args, nullptr);
+    // (the plain forms compile the fused epilogue out)
+    const CUfunction fn = (bias != nullptr || act != GEMM_ACT_NONE) ? p->fn_epilogue : p->fn;
+    CUresult r = launch_fn()(&p->launch, fn, args, nullptr);
     if (r == CUDA_ERROR_INVALID_CONTEXT && cudaSetDevice(p->device) == cudaSuccess)
-        r = launch_fn()(&p->launch, p->fn, args, nullptr);   // a thread without a current context
+        r = launch_fn()(&p->launch, fn, args, nullptr);   // a thread without a current context
     return r == CUDA_SUCCESS ? GEMM_OK : GEMM_ERR_LAUNCH;
 }
 

@@ -861,6 +861,8 @@ __device__ __forceinline__ KParams form_params(const KParams& in) {
         p.l2_prefetch = 0;
         p.a_mn_major = 0;
         p.b_mn_major = 0;
+        p.bias = nullptr;   // a call with a fused bias or activation launches the general form
+        p.act = 0;
         if constexpr (FORM == kFormPlain) {
             p.split_k = 1;
             p.cluster_split = 0;

@@ -15,10 +15,10 @@ enum OutKind : int { kOutF16 = 0, kOutBF16 = 1, kOutI32 = 2 };
 
 // Compiled forms of a kernel.  General: every mode is a run-time field of
 // KParams.  Plain: one K slice, no multicast, TMA stores, K-contiguous operands,
-// no L2 prefetch distance.  Cluster split (one-SM kernel): as plain, but the K
-// slices of a tile form one thread-block cluster (split_k stays a run-time
-// value).  The fixed fields become constants, so the code of the other modes
-// compiles out of the launch's critical path.
+// no L2 prefetch distance, no fused bias or activation.  Cluster split (one-SM
+// kernel): as plain, but the K slices of a tile form one thread-block cluster
+// (split_k stays a run-time value).  The fixed fields become constants, so the
+// code of the other modes compiles out of the launch's critical path.
 enum KernelForm : int { kFormGeneral = 0, kFormPlain = 1, kFormClusterSplit = 2 };
 
 // SM-pair integer tiles wider than 128 columns keep their int32 sums in registers
