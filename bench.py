@@ -332,25 +332,33 @@ def e2e_sweep(items, stream, steps, groups=32):
     ev_out = [torch.cuda.Event() for _ in range(groups)]
     torch.cuda.synchronize()
 
-    def one(compute=True, copy_out=True):
+    def timed_copy(st, dst, src, marks):
+        # one copy on stream `st`; with `marks`, bracketed by timing events
+        if marks is None:
+            dst.copy_(src, non_blocking=True)
+            return
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(st)
+        dst.copy_(src, non_blocking=True)
+        b.record(st)
+        marks.append((a, b))
+
+    def one(busy_in=None, busy_out=None):
         for g in range(groups):
             lo, hi = rng_in[g]
             with torch.cuda.stream(s_in):
                 s_in.wait_event(ev_mm[g])          # the previous step's GEMMs read this range
-                d_in[lo:hi].copy_(h_in[lo:hi], non_blocking=True)
+                timed_copy(s_in, d_in[lo:hi], h_in[lo:hi], busy_in)
                 ev_in[g].record(s_in)
             stream.wait_event(ev_in[g])
             stream.wait_event(ev_out[g])           # the previous step's copy-out of this range
-            if compute:
-                for plan, dA, dB, dC in views[bounds[g]:bounds[g + 1]]:
-                    plan.run(dA, dB, dC, stream)
+            for plan, dA, dB, dC in views[bounds[g]:bounds[g + 1]]:
+                plan.run(dA, dB, dC, stream)
             ev_mm[g].record(stream)
-            if not copy_out:
-                continue
             lo, hi = rng_out[g]
             with torch.cuda.stream(s_out):
                 s_out.wait_event(ev_mm[g])
-                h_out[lo:hi].copy_(d_out[lo:hi], non_blocking=True)
+                timed_copy(s_out, h_out[lo:hi], d_out[lo:hi], busy_out)
                 ev_out[g].record(s_out)
 
     one()
@@ -360,15 +368,17 @@ def e2e_sweep(items, stream, steps, groups=32):
         one()
     torch.cuda.synchronize()
     wall = time.perf_counter() - t0
-    # the step's host-to-device copies alone (the larger direction; the results
-    # travel back concurrently): the floor the host link sets for this step
-    one(compute=False, copy_out=False)
-    torch.cuda.synchronize()
-    t0 = time.perf_counter()
-    for _ in range(steps):
-        one(compute=False, copy_out=False)
-    torch.cuda.synchronize()
-    copy_ms = (time.perf_counter() - t0) * 1e3 / steps
+    # How long the host link is busy in the step: the summed durations of the
+    # step's copies in each direction, timed on the copy streams in untimed
+    # steps run the same way (median of three)
+    busy = []
+    for _ in range(3):
+        m_in, m_out = [], []
+        one(m_in, m_out)
+        torch.cuda.synchronize()
+        busy.append((sum(a.elapsed_time(b) for a, b in m_in),
+                     sum(a.elapsed_time(b) for a, b in m_out)))
+    busy_ms = (statistics.median(x[0] for x in busy), statistics.median(x[1] for x in busy))
     # results came back: spot-check one C against the device copy of the eager run
     mid = len(items) // 2
     w, plan, A, B, C = items[mid]
@@ -378,7 +388,7 @@ def e2e_sweep(items, stream, steps, groups=32):
     torch.cuda.synchronize()
     if not torch.equal(got.view(torch.int16), C.cpu().view(torch.int16)):
         raise RuntimeError("e2e: copied-back result differs from the device result")
-    return wall * 1e3 / steps, h2d, d2h, copy_ms
+    return wall * 1e3 / steps, h2d, d2h, busy_ms
 
 
 def launch_floor_us(stream, sms, n=2000, graph=False):
@@ -809,15 +819,17 @@ def ours(args):
             "skinny_64x4096x64_us": round(times.get("sweep_64x4096x64_f16", 0) * 1e3, 3),
             "note": "each launch alone between CUDA events (no launch overlap)",
         }
-        e2e_ms, h2d, d2h, copy_ms = e2e_sweep(items, stream, steps=max(3, min(20, args.steps)))
+        e2e_ms, h2d, d2h, busy_ms = e2e_sweep(items, stream, steps=max(3, min(20, args.steps)))
         line["e2e"] = {"value": round(flops_step / (e2e_ms * 1e-3) / 1e12, 3), "unit": UNIT,
                        "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                        "ms_per_step": round(e2e_ms, 3),
-                       "h2d_only_ms_per_step": round(copy_ms, 3),
-                       "frac_of_h2d_floor": round(copy_ms / e2e_ms, 4),
-                       "note": "h2d_only: the step's host-to-device copies alone (no GEMM, no "
-                               "copy back); the step is bound by the host link when the "
-                               "fraction is near 1"}
+                       "h2d_busy_ms_per_step": round(busy_ms[0], 3),
+                       "d2h_busy_ms_per_step": round(busy_ms[1], 3),
+                       "link_busy_frac": round(max(busy_ms) / e2e_ms, 4),
+                       "note": "busy: the summed durations of the step's host-to-device and "
+                               "device-to-host copies, timed on their streams in the "
+                               "pipelined step; link_busy_frac = the busier direction / "
+                               "step time (near 1: the step is bound by the host link)"}
         del graph
         for _, plan, *_ in items:
             plan.close()
