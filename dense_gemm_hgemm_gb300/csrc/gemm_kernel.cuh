@@ -943,19 +943,21 @@ __global__ void __launch_bounds__(kThreads, 1)
     const UnitIter it = unit_iter(p);
     // This CTA's first unit, worked out while the previous kernel may still run.
     const UnitCoord c_first = unit_at(p, it.first);
-    // (a half-height A tile delivers 8 KiB less per k-block)
-    const uint32_t slot_tx = kStageTx - (p.a_half ? KS * 8192u : 0u) + p.tx_extra;
-    // ring slots of the first unit armed before the wait (copy thread only)
+    // Plain and cluster split forms: ring slots of the first unit that the copy
+    // thread arms before the wait (shared memory only), so that right after it
+    // only their copies are issued.  (The general form arms each slot in its
+    // loop: the extra copy-issue code measured slower there, next to a fused
+    // epilogue.)
     int32_t n_armed = 0;
-    if (warp == 0 && lane == 0 && it.first < p.num_units) {
-        // Arm the ring's first slots with their byte counts (shared memory only),
-        // so that after the wait the copy thread just issues their copies.
-        {
+    if constexpr (FORM != kFormGeneral) {
+        if (warp == 0 && lane == 0 && it.first < p.num_units) {
             const int32_t nslots = (c_first.kb_end - c_first.kb_begin + KS - 1) / KS;
             n_armed = nslots < STAGES ? nslots : STAGES;
             for (int32_t s = 0; s < n_armed; ++s)
-                mbar_arrive_expect_tx(smem_addr(&ctl->full[s]), slot_tx);
+                mbar_arrive_expect_tx(smem_addr(&ctl->full[s]), kStageTx - (p.a_half ? KS * 8192u : 0u) + p.tx_extra);
         }
+    }
+    if (warp == 0 && lane == 0 && it.first < p.num_units) {
         // Warm L2 with this CTA's first k-blocks while the previous kernel drains.
         // Only L2 is touched (the coherence point); the data is read after the
         // wait below, so this cannot observe stale values.
@@ -983,78 +985,124 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     if (warp == 0) {
         // ------------------------------------------------------------ producer
-        if (lane == 0) {   // the thread that armed the first slots
-            // The copies of ring slot `stage` (armed) for k-block kb of unit c.
-            auto issue = [&](int stage, int32_t kb, const UnitCoord& c) {
-                const uint32_t full = smem_addr(&ctl->full[stage]);
-                if constexpr (KS > 1) {
-                    // the slot's KS k-blocks of each operand in one copy; a copy
-                    // past the end of K is zero-filled and past the slice end is
-                    // unused, but always delivers the full box
-                    load_operand_kb<KS>(ring + stage * L::kASlotBytes, &tmap_a, full, kb,
-                                        c.m_blk * kBM, p.a_half ? kBM / 2 : kBM, p.a_mn_major);
-                    load_operand_kb<KS>(ring_b + stage * L::kBTileBytes, &tmap_b, full, kb,
-                                        c.n_blk * BN, BN, p.b_mn_major);
-                    if (p.l2_prefetch > 0 && kb + p.l2_prefetch < c.kb_end) {
-                        prefetch_operand_kb(&tmap_a, kb + p.l2_prefetch, c.m_blk * kBM,
-                                            p.a_half ? kBM / 2 : kBM, p.a_mn_major);
-                        prefetch_operand_kb(&tmap_b, kb + p.l2_prefetch, c.n_blk * BN, BN,
-                                            p.b_mn_major);
-                    }
-                } else {
-                    if (p.mcast > 1) {
-                        // this CTA's 1/mcast of the A tile, delivered to every CTA of
-                        // the cluster (the slot's bytes arrive from all of them)
-                        const int32_t rank = static_cast<int32_t>(blockIdx.x & (p.mcast - 1));
-                        const uint16_t all = static_cast<uint16_t>((1u << p.mcast) - 1u);
-                        const uint32_t a_slot = ring + stage * kATileBytes;
-                        if (p.a_mn_major) {   // mcast == 2: one 64-row M block each
-                            tma_load_2d_mcast(a_slot + static_cast<uint32_t>(rank) * 8192u,
-                                              &tmap_a, full, c.m_blk * kBM + rank * 64, kb * kBK,
-                                              all);
-                        } else {
-                            const int32_t rows = kBM >> p.mcast_shift;
-                            tma_load_2d_mcast(a_slot + static_cast<uint32_t>(rank * rows * 128),
-                                              &tmap_a, full, kb * kBK, c.m_blk * kBM + rank * rows,
-                                              all);
-                        }
+        if constexpr (FORM != kFormGeneral) {
+            // (no multicast, no L2 prefetch distance, K-contiguous operands)
+            if (lane == 0) {   // the thread that armed the first slots
+                const uint32_t slot_tx = kStageTx - (p.a_half ? KS * 8192u : 0u) + p.tx_extra;
+                auto issue = [&](int stage, int32_t kb, const UnitCoord& c) {
+                    const uint32_t full = smem_addr(&ctl->full[stage]);
+                    if constexpr (KS > 1) {
+                        load_operand_kb<KS>(ring + stage * L::kASlotBytes, &tmap_a, full, kb,
+                                            c.m_blk * kBM, p.a_half ? kBM / 2 : kBM, 0);
+                        load_operand_kb<KS>(ring_b + stage * L::kBTileBytes, &tmap_b, full, kb,
+                                            c.n_blk * BN, BN, 0);
                     } else {
                         load_operand(ring + stage * kATileBytes, &tmap_a, full, kb, c.m_blk * kBM,
-                                     p.a_half ? kBM / 2 : kBM, p.a_mn_major);
+                                     p.a_half ? kBM / 2 : kBM, 0);
+                        load_operand(ring_b + stage * L::kBTileBytes, &tmap_b, full, kb,
+                                     c.n_blk * BN, BN, 0);
                     }
-                    load_operand(ring_b + stage * L::kBTileBytes, &tmap_b, full, kb, c.n_blk * BN,
-                                 BN, p.b_mn_major);
-                    if (p.l2_prefetch > 0 && kb + p.l2_prefetch < c.kb_end) {
-                        // warm L2 with a later k-block of this tile (this CTA's A share)
-                        const int32_t a_rows = p.a_half ? kBM / 2 : (kBM >> p.mcast_shift);
-                        const int32_t a_rank =
-                            static_cast<int32_t>(blockIdx.x & ((1u << p.mcast_shift) - 1u));
-                        prefetch_operand(&tmap_a, kb + p.l2_prefetch,
-                                         c.m_blk * kBM + a_rank * a_rows, a_rows, p.a_mn_major);
-                        prefetch_operand(&tmap_b, kb + p.l2_prefetch, c.n_blk * BN, BN,
-                                         p.b_mn_major);
+                };
+                for (int32_t s = 0; s < n_armed; ++s) issue(s, c_first.kb_begin + s * KS, c_first);
+                int stage = n_armed == STAGES ? 0 : n_armed;
+                uint32_t phase = n_armed == STAGES ? 1u : 0u;
+                int issued = n_armed;
+                bool ok = true;
+                for (int32_t u = it.first; ok && u < p.num_units; u += it.stride) {
+                    const UnitCoord c = u == it.first ? c_first : unit_at(p, u);
+                    for (int32_t kb = u == it.first ? c.kb_begin + n_armed * KS : c.kb_begin;
+                         kb < c.kb_end; kb += KS) {
+                        if (issued >= STAGES &&
+                            !wait_phase(smem_addr(&ctl->empty[stage]), phase ^ 1u, watch,
+                                        kSiteProducerEmpty)) {
+                            ok = false;
+                            break;
+                        }
+                        mbar_arrive_expect_tx(smem_addr(&ctl->full[stage]), slot_tx);
+                        issue(stage, kb, c);
+                        ++issued;
+                        if (++stage == STAGES) {
+                            stage = 0;
+                            phase ^= 1u;
+                        }
                     }
                 }
-            };
-            // the first unit's armed slots (the first pass over the ring finds
-            // every slot free)
-            for (int32_t s = 0; s < n_armed; ++s) issue(s, c_first.kb_begin + s * KS, c_first);
-            int stage = n_armed == STAGES ? 0 : n_armed;
-            uint32_t phase = n_armed == STAGES ? 1u : 0u;
-            int issued = n_armed;
+                // every copy issued lands before the CTA can exit (see below)
+                const int pending = issued < STAGES ? issued : STAGES;
+                for (int i = 0; i < pending; ++i) {
+                    if (--stage < 0) {
+                        stage = STAGES - 1;
+                        phase ^= 1u;
+                    }
+                    wait_phase_unwind(smem_addr(&ctl->full[stage]), phase, 100000000ull);
+                }
+            }
+        } else if (elect_one_sync()) {
+            int stage = 0;
+            uint32_t phase = 0;
+            int issued = 0;
             bool ok = true;
             for (int32_t u = it.first; ok && u < p.num_units; u += it.stride) {
                 const UnitCoord c = u == it.first ? c_first : unit_at(p, u);
-                const int32_t kb0 = u == it.first ? c.kb_begin + n_armed * KS : c.kb_begin;
-                for (int32_t kb = kb0; kb < c.kb_end; kb += KS) {
+                for (int32_t kb = c.kb_begin; kb < c.kb_end; kb += KS) {
+                    const uint32_t full = smem_addr(&ctl->full[stage]);
+                    // (the first pass over the ring finds every slot free)
                     if (issued >= STAGES &&
                         !wait_phase(smem_addr(&ctl->empty[stage]), phase ^ 1u, watch,
                                     kSiteProducerEmpty)) {
                         ok = false;
                         break;
                     }
-                    mbar_arrive_expect_tx(smem_addr(&ctl->full[stage]), slot_tx);
-                    issue(stage, kb, c);
+                    // (a half-height A tile delivers 8 KiB less per k-block)
+                    mbar_arrive_expect_tx(full, kStageTx - (p.a_half ? KS * 8192u : 0u) + p.tx_extra);
+                    if constexpr (KS > 1) {
+                        // the slot's KS k-blocks of each operand in one copy; a copy
+                        // past the end of K is zero-filled and past the slice end is
+                        // unused, but always delivers the full box
+                        load_operand_kb<KS>(ring + stage * L::kASlotBytes, &tmap_a, full, kb,
+                                            c.m_blk * kBM, p.a_half ? kBM / 2 : kBM, p.a_mn_major);
+                        load_operand_kb<KS>(ring_b + stage * L::kBTileBytes, &tmap_b, full, kb,
+                                            c.n_blk * BN, BN, p.b_mn_major);
+                        if (p.l2_prefetch > 0 && kb + p.l2_prefetch < c.kb_end) {
+                            prefetch_operand_kb(&tmap_a, kb + p.l2_prefetch, c.m_blk * kBM,
+                                                p.a_half ? kBM / 2 : kBM, p.a_mn_major);
+                            prefetch_operand_kb(&tmap_b, kb + p.l2_prefetch, c.n_blk * BN, BN,
+                                                p.b_mn_major);
+                        }
+                    } else {
+                        if (p.mcast > 1) {
+                            // this CTA's 1/mcast of the A tile, delivered to every CTA of
+                            // the cluster (the slot's bytes arrive from all of them)
+                            const int32_t rank = static_cast<int32_t>(blockIdx.x & (p.mcast - 1));
+                            const uint16_t all = static_cast<uint16_t>((1u << p.mcast) - 1u);
+                            const uint32_t a_slot = ring + stage * kATileBytes;
+                            if (p.a_mn_major) {   // mcast == 2: one 64-row M block each
+                                tma_load_2d_mcast(a_slot + static_cast<uint32_t>(rank) * 8192u,
+                                                  &tmap_a, full, c.m_blk * kBM + rank * 64, kb * kBK,
+                                                  all);
+                            } else {
+                                const int32_t rows = kBM >> p.mcast_shift;
+                                tma_load_2d_mcast(a_slot + static_cast<uint32_t>(rank * rows * 128),
+                                                  &tmap_a, full, kb * kBK, c.m_blk * kBM + rank * rows,
+                                                  all);
+                            }
+                        } else {
+                            load_operand(ring + stage * kATileBytes, &tmap_a, full, kb, c.m_blk * kBM,
+                                         p.a_half ? kBM / 2 : kBM, p.a_mn_major);
+                        }
+                        load_operand(ring_b + stage * L::kBTileBytes, &tmap_b, full, kb, c.n_blk * BN,
+                                     BN, p.b_mn_major);
+                        if (p.l2_prefetch > 0 && kb + p.l2_prefetch < c.kb_end) {
+                            // warm L2 with a later k-block of this tile (this CTA's A share)
+                            const int32_t a_rows = p.a_half ? kBM / 2 : (kBM >> p.mcast_shift);
+                            const int32_t a_rank =
+                                static_cast<int32_t>(blockIdx.x & ((1u << p.mcast_shift) - 1u));
+                            prefetch_operand(&tmap_a, kb + p.l2_prefetch,
+                                             c.m_blk * kBM + a_rank * a_rows, a_rows, p.a_mn_major);
+                            prefetch_operand(&tmap_b, kb + p.l2_prefetch, c.n_blk * BN, BN,
+                                             p.b_mn_major);
+                        }
+                    }
                     ++issued;
                     if (++stage == STAGES) {
                         stage = 0;

@@ -292,19 +292,22 @@ __global__ void __launch_bounds__(64 + 32 * kPairEpiWarps<BN, OUT>, 1)
     bool epi_ok = false;   // epilogue: this CTA's accumulator is complete (split-K in the cluster)
     // This pair's first unit, worked out while the previous kernel may still run.
     const UnitCoord c_first = coord(pair);
-    // ring slots of the first unit armed before the wait (copy thread only)
+    // Plain form: ring slots of the first unit that the leader's copy thread arms
+    // before the wait (shared memory only), so that right after it both copy
+    // threads only issue their copies.  (The general form arms each slot in its
+    // loop: the extra copy-issue code measured slower there, next to a fused
+    // epilogue.)
     int32_t n_armed = 0;
-    if (warp == 0 && lane == 0 && pair < p.num_units) {
-        // The leader arms the ring's first slots with the pair's byte counts
-        // (shared memory only), so that after the wait the copy threads just
-        // issue their copies.
-        {
+    if constexpr (FORM != kFormGeneral) {
+        if (warp == 0 && lane == 0 && pair < p.num_units) {
             const int32_t nslots = (c_first.kb_end - c_first.kb_begin + KS - 1) / KS;
             n_armed = nslots < STAGES ? nslots : STAGES;
             if (leader)
                 for (int32_t s = 0; s < n_armed; ++s)
                     mbar_arrive_expect_tx(smem_addr(&ctl->full[s]), kPairTx + p.tx_extra);
         }
+    }
+    if (warp == 0 && lane == 0 && pair < p.num_units) {
         const UnitCoord c = c_first;
         const int32_t ahead = STAGES * KS > p.l2_prefetch ? STAGES * KS : p.l2_prefetch;
         const int32_t kb_end = c.kb_begin + ahead < c.kb_end ? c.kb_begin + ahead : c.kb_end;
@@ -328,75 +331,122 @@ __global__ void __launch_bounds__(64 + 32 * kPairEpiWarps<BN, OUT>, 1)
 
     if (warp == 0) {
         // ------------------------------------------------------------ producer (both CTAs)
-        if (lane == 0) {   // the thread that armed the first slots
-            // The copies of ring slot `stage` (armed on the leader) for k-block kb
-            // of unit c.
-            auto issue = [&](int stage, int32_t kb, const UnitCoord& c) {
-                const int32_t a_row = c.m_blk * 2 * kBM + static_cast<int32_t>(rank) * kBM;
-                const int32_t b_row = c.n_blk * BN + static_cast<int32_t>(rank) * (BN / 2);
-                const uint32_t full_lead = map_to_rank(smem_addr(&ctl->full[stage]), lead);
-                if constexpr (KS > 1) {
-                    // the slot's KS k-blocks of each operand in one copy (full box always)
-                    load_operand_kb_pair<KS>(ring + stage * L::kASlotBytes, &tmap_a, full_lead,
-                                             kb, a_row, kBM, p.a_mn_major);
-                    load_operand_kb_pair<KS>(ring_b + stage * L::kBTileBytes, &tmap_b, full_lead,
-                                             kb, b_row, BN / 2, p.b_mn_major);
-                    if (p.l2_prefetch > 0 && kb + p.l2_prefetch < c.kb_end) {
-                        prefetch_operand_kb(&tmap_a, kb + p.l2_prefetch, a_row, kBM, p.a_mn_major);
-                        prefetch_operand_kb(&tmap_b, kb + p.l2_prefetch, b_row, BN / 2,
-                                            p.b_mn_major);
-                    }
-                } else {
-                    if (mcast) {
-                        // this CTA's 64 rows of its half's A tile, into the same slot
-                        // offset of the matching CTA of both pairs; the bytes count on
-                        // each destination pair's leader barrier (K-major: 64 rows of
-                        // 128 B; M-major: one 64-element block, either way 8 KiB in)
-                        const uint32_t a_dst = ring + stage * kATileBytes + qpair * 8192u;
-                        const int32_t a_r = a_row + static_cast<int32_t>(qpair) * (kBM / 2);
-                        if (p.a_mn_major)
-                            tma_load_2d_pair_mcast(a_dst, &tmap_a, full_lead, a_r, kb * kBK, a_mask);
-                        else
-                            tma_load_2d_pair_mcast(a_dst, &tmap_a, full_lead, kb * kBK, a_r, a_mask);
+        if constexpr (FORM != kFormGeneral) {
+            // (no multicast, no L2 prefetch distance, K-contiguous operands)
+            if (lane == 0) {   // the thread that armed the first slots
+                auto issue = [&](int stage, int32_t kb, const UnitCoord& c) {
+                    const int32_t a_row = c.m_blk * 2 * kBM + static_cast<int32_t>(rank) * kBM;
+                    const int32_t b_row = c.n_blk * BN + static_cast<int32_t>(rank) * (BN / 2);
+                    const uint32_t full_lead = map_to_rank(smem_addr(&ctl->full[stage]), lead);
+                    if constexpr (KS > 1) {
+                        load_operand_kb_pair<KS>(ring + stage * L::kASlotBytes, &tmap_a, full_lead,
+                                                 kb, a_row, kBM, 0);
+                        load_operand_kb_pair<KS>(ring_b + stage * L::kBTileBytes, &tmap_b,
+                                                 full_lead, kb, b_row, BN / 2, 0);
                     } else {
                         load_operand_pair(ring + stage * kATileBytes, &tmap_a, full_lead, kb,
-                                          a_row, kBM, p.a_mn_major);
+                                          a_row, kBM, 0);
+                        load_operand_pair(ring_b + stage * L::kBTileBytes, &tmap_b, full_lead, kb,
+                                          b_row, BN / 2, 0);
                     }
-                    load_operand_pair(ring_b + stage * L::kBTileBytes, &tmap_b, full_lead, kb,
-                                      b_row, BN / 2, p.b_mn_major);
-                    if (p.l2_prefetch > 0 && kb + p.l2_prefetch < c.kb_end) {
-                        if (mcast)
-                            prefetch_operand(&tmap_a, kb + p.l2_prefetch,
-                                             a_row + static_cast<int32_t>(qpair) * (kBM / 2),
-                                             kBM / 2, p.a_mn_major);
-                        else
-                            prefetch_operand(&tmap_a, kb + p.l2_prefetch, a_row, kBM,
-                                             p.a_mn_major);
-                        prefetch_operand(&tmap_b, kb + p.l2_prefetch, b_row, BN / 2,
-                                         p.b_mn_major);
+                };
+                for (int32_t s = 0; s < n_armed; ++s) issue(s, c_first.kb_begin + s * KS, c_first);
+                int stage = n_armed == STAGES ? 0 : n_armed;
+                uint32_t phase = n_armed == STAGES ? 1u : 0u;
+                int issued = n_armed;
+                bool ok = true;
+                for (int32_t u = pair; ok && u < p.num_units; u += npairs) {
+                    const UnitCoord c = u == pair ? c_first : coord(u);
+                    for (int32_t kb = u == pair ? c.kb_begin + n_armed * KS : c.kb_begin;
+                         kb < c.kb_end; kb += KS) {
+                        if (issued >= STAGES &&
+                            !wait_phase(smem_addr(&ctl->empty[stage]), phase ^ 1u, watch,
+                                        kSiteProducerEmpty)) {
+                            ok = false;
+                            break;
+                        }
+                        if (leader)
+                            mbar_arrive_expect_tx(smem_addr(&ctl->full[stage]), kPairTx + p.tx_extra);
+                        issue(stage, kb, c);
+                        ++issued;
+                        if (++stage == STAGES) {
+                            stage = 0;
+                            phase ^= 1u;
+                        }
                     }
                 }
-            };
-            // the first unit's armed slots (the first pass over the ring finds
-            // every slot free)
-            for (int32_t s = 0; s < n_armed; ++s) issue(s, c_first.kb_begin + s * KS, c_first);
-            int stage = n_armed == STAGES ? 0 : n_armed;
-            uint32_t phase = n_armed == STAGES ? 1u : 0u;
-            int issued = n_armed;
+                // both CTAs' copies count on the leader's barriers: they land before
+                // the pair can leave (see below)
+                const int pending = issued < STAGES ? issued : STAGES;
+                for (int i = 0; i < pending; ++i) {
+                    if (--stage < 0) {
+                        stage = STAGES - 1;
+                        phase ^= 1u;
+                    }
+                    if (leader) wait_phase_unwind(smem_addr(&ctl->full[stage]), phase, 100000000ull);
+                }
+            }
+        } else if (elect_one_sync()) {
+            int stage = 0;
+            uint32_t phase = 0;
+            int issued = 0;
             bool ok = true;
             for (int32_t u = pair; ok && u < p.num_units; u += npairs) {
                 const UnitCoord c = u == pair ? c_first : coord(u);
-                const int32_t kb0 = u == pair ? c.kb_begin + n_armed * KS : c.kb_begin;
-                for (int32_t kb = kb0; kb < c.kb_end; kb += KS) {
+                const int32_t a_row = c.m_blk * 2 * kBM + static_cast<int32_t>(rank) * kBM;
+                const int32_t b_row = c.n_blk * BN + static_cast<int32_t>(rank) * (BN / 2);
+                for (int32_t kb = c.kb_begin; kb < c.kb_end; kb += KS) {
+                    // (the first pass over the ring finds every slot free)
                     if (issued >= STAGES &&
                         !wait_phase(smem_addr(&ctl->empty[stage]), phase ^ 1u, watch,
                                     kSiteProducerEmpty)) {
                         ok = false;
                         break;
                     }
-                    if (leader)
-                        mbar_arrive_expect_tx(smem_addr(&ctl->full[stage]), kPairTx + p.tx_extra);
-                    issue(stage, kb, c);
+                    const uint32_t full_local = smem_addr(&ctl->full[stage]);
+                    if (leader) mbar_arrive_expect_tx(full_local, kPairTx + p.tx_extra);
+                    const uint32_t full_lead = map_to_rank(full_local, lead);
+                    if constexpr (KS > 1) {
+                        // the slot's KS k-blocks of each operand in one copy (full box always)
+                        load_operand_kb_pair<KS>(ring + stage * L::kASlotBytes, &tmap_a, full_lead,
+                                                 kb, a_row, kBM, p.a_mn_major);
+                        load_operand_kb_pair<KS>(ring_b + stage * L::kBTileBytes, &tmap_b, full_lead,
+                                                 kb, b_row, BN / 2, p.b_mn_major);
+                        if (p.l2_prefetch > 0 && kb + p.l2_prefetch < c.kb_end) {
+                            prefetch_operand_kb(&tmap_a, kb + p.l2_prefetch, a_row, kBM, p.a_mn_major);
+                            prefetch_operand_kb(&tmap_b, kb + p.l2_prefetch, b_row, BN / 2,
+                                                p.b_mn_major);
+                        }
+                    } else {
+                        if (mcast) {
+                            // this CTA's 64 rows of its half's A tile, into the same slot
+                            // offset of the matching CTA of both pairs; the bytes count on
+                            // each destination pair's leader barrier (K-major: 64 rows of
+                            // 128 B; M-major: one 64-element block, either way 8 KiB in)
+                            const uint32_t a_dst = ring + stage * kATileBytes + qpair * 8192u;
+                            const int32_t a_r = a_row + static_cast<int32_t>(qpair) * (kBM / 2);
+                            if (p.a_mn_major)
+                                tma_load_2d_pair_mcast(a_dst, &tmap_a, full_lead, a_r, kb * kBK, a_mask);
+                            else
+                                tma_load_2d_pair_mcast(a_dst, &tmap_a, full_lead, kb * kBK, a_r, a_mask);
+                        } else {
+                            load_operand_pair(ring + stage * kATileBytes, &tmap_a, full_lead, kb,
+                                              a_row, kBM, p.a_mn_major);
+                        }
+                        load_operand_pair(ring_b + stage * L::kBTileBytes, &tmap_b, full_lead, kb,
+                                          b_row, BN / 2, p.b_mn_major);
+                        if (p.l2_prefetch > 0 && kb + p.l2_prefetch < c.kb_end) {
+                            if (mcast)
+                                prefetch_operand(&tmap_a, kb + p.l2_prefetch,
+                                                 a_row + static_cast<int32_t>(qpair) * (kBM / 2),
+                                                 kBM / 2, p.a_mn_major);
+                            else
+                                prefetch_operand(&tmap_a, kb + p.l2_prefetch, a_row, kBM,
+                                                 p.a_mn_major);
+                            prefetch_operand(&tmap_b, kb + p.l2_prefetch, b_row, BN / 2,
+                                             p.b_mn_major);
+                        }
+                    }
                     ++issued;
                     if (++stage == STAGES) {
                         stage = 0;
