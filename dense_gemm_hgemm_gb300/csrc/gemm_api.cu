@@ -59,7 +59,8 @@ struct gemm_plan {
     // kernel's driver function handle, grid / block / shared memory, programmatic
     // dependent launch and the cluster shape.
     CUfunction fn;
-    CUfunction fn_epilogue;     // the general form, for calls with a fused bias or activation
+    CUfunction fn_epilogue;     // for calls with a fused bias or activation: the epilogue
+                                // form of a plain plan, else the general form
     CUlaunchConfig launch;
     CUlaunchAttribute launch_attr[2];
 };
@@ -500,13 +501,16 @@ gemm_status_t create_plan(int64_t M, int64_t N, int64_t K, gemm_dtype_t dtype,
 
     const void* kernel =
         gbg::gemm_kernel_ptr(cfg.block_n, cfg.stages, p->out_kind, cfg.cta_pair, p->form);
+    // (integer plans have no fused epilogue: theirs is never launched)
+    const int form_epi = p->form == gbg::kFormPlain && dtype != GEMM_I8_I32 ? gbg::kFormEpilogue
+                                                                           : gbg::kFormGeneral;
     const void* kernel_epi =
-        gbg::gemm_kernel_ptr(cfg.block_n, cfg.stages, p->out_kind, cfg.cta_pair, gbg::kFormGeneral);
+        gbg::gemm_kernel_ptr(cfg.block_n, cfg.stages, p->out_kind, cfg.cta_pair, form_epi);
     size_t smem_epi = 0;
     if (!kernel || !kernel_epi || cudaGetFuncBySymbol(&p->fn, kernel) != cudaSuccess ||
         cudaGetFuncBySymbol(&p->fn_epilogue, kernel_epi) != cudaSuccess || !launch_fn() ||
-        (p->form != gbg::kFormGeneral &&
-         gbg::gemm_prepare(cfg.block_n, cfg.stages, p->out_kind, cfg.cta_pair, gbg::kFormGeneral,
+        (form_epi != p->form &&
+         gbg::gemm_prepare(cfg.block_n, cfg.stages, p->out_kind, cfg.cta_pair, form_epi,
                            &smem_epi) != cudaSuccess)) {
         cudaGetLastError();
         cudaFree(p->dmem);

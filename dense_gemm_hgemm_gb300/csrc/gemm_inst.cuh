@@ -7,8 +7,8 @@
 // A variant is (tile width BN, ring depth STAGES, k-blocks per slot KS) of the
 // one-SM kernel or of the SM-pair kernel; (BN, STAGES) identifies it, because
 // every KS has its own depth for a given BN.  Each variant is compiled in the
-// general form and, where a plan can use them, in the plain and cluster-split
-// forms (KernelForm).  The integer output mode keeps its int32 sums in
+// general form and, where a plan can use them, in the plain, cluster-split and
+// epilogue forms (KernelForm).  The integer output mode keeps its int32 sums in
 // registers: the one-SM kernel has the narrower variants only, and only the
 // general form (the plain forms spill there); the SM-pair kernel has them all
 // (224/256-wide integer tiles with eight epilogue warps).  The 224-wide SM-pair
@@ -32,7 +32,7 @@ namespace inst {
 template <int OUT, int BN>
 constexpr bool one_sm_ok() { return OUT != kOutI32 || BN <= 128; }
 // Forms compiled per one-SM variant: the four-k-block variant (never chosen by
-// the table) and the integer mode have the general form only.
+// the table) and the integer mode (no fused epilogue) have the general form only.
 template <int OUT, int KS, int FORM>
 constexpr bool one_sm_form_ok() {
     return FORM == kFormGeneral || (OUT != kOutI32 && KS != 4);
@@ -42,7 +42,8 @@ constexpr bool one_sm_form_ok() {
 template <int OUT, int BN, int KS, int FORM>
 constexpr bool pair_form_ok() {
     return FORM == kFormGeneral ||
-           (FORM == kFormPlain && KS != 4 && !(OUT == kOutI32 && BN == 128));
+           (FORM == kFormPlain && KS != 4 && !(OUT == kOutI32 && BN == 128)) ||
+           (FORM == kFormEpilogue && KS != 4 && OUT != kOutI32);
 }
 
 template <bool PAIR, int BN, int STAGES, int OUT, int KS, int FORM>
@@ -89,6 +90,8 @@ const void* gemm_variant_one_sm(int bn, int stages, int form, size_t* smem, cuda
                 GBG_FORM_CASE(false, B, S, K, kFormPlain)                       \
             if constexpr (inst::one_sm_form_ok<OUT, K, kFormClusterSplit>())    \
                 GBG_FORM_CASE(false, B, S, K, kFormClusterSplit)                \
+            if constexpr (inst::one_sm_form_ok<OUT, K, kFormEpilogue>())        \
+                GBG_FORM_CASE(false, B, S, K, kFormEpilogue)                    \
             GBG_FORM_CASE(false, B, S, K, kFormGeneral)                         \
         }
     GBG_ONE_SM_VARIANTS(X)
@@ -103,6 +106,8 @@ const void* gemm_variant_pair(int bn, int stages, int form, size_t* smem, cudaEr
     if (bn == B && stages == S) {                                               \
         if constexpr (inst::pair_form_ok<OUT, B, K, kFormPlain>())              \
             GBG_FORM_CASE(true, B, S, K, kFormPlain)                            \
+        if constexpr (inst::pair_form_ok<OUT, B, K, kFormEpilogue>())           \
+            GBG_FORM_CASE(true, B, S, K, kFormEpilogue)                         \
         GBG_FORM_CASE(true, B, S, K, kFormGeneral)                              \
     }
     GBG_PAIR_VARIANTS(X)

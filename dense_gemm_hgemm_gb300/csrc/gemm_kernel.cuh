@@ -62,8 +62,9 @@ struct SmemLayout {
     static constexpr int kStoreBufBytes = 32 * 128;
     static constexpr int kStagingBytes = kEpiWarps * 2 * kStoreBufBytes;
     static constexpr int kCtlBytes = 256;
+    static constexpr int kBiasBytes = kEpiWarps * kBiasSlotBytes;   // after the control block
     static constexpr int kTotal =
-        1024 /* alignment slack */ + kRingBytes + kStagingBytes + kCtlBytes;
+        1024 /* alignment slack */ + kRingBytes + kStagingBytes + kCtlBytes + kBiasBytes;
     static_assert(kTotal <= 232448, "exceeds the 227 KiB a CTA may use");
     static_assert(kBTileBytes % 1024 == 0, "128B-swizzle tiles must stay 1024-byte aligned");
     static_assert(STAGES * 16 + 5 * 8 + 16 <= kCtlBytes, "control block overflow");
@@ -476,6 +477,48 @@ __device__ __forceinline__ void apply_bias_act(uint32_t* v, const KParams& p, in
     }
 }
 
+// The fused bias of a 64-column chunk, staged in the epilogue warp's shared
+// memory slot: each lane fetches two columns one chunk ahead (global latency off
+// the chunk's path), the warp writes them to its slot, and the 32-column halves
+// read them back four columns per broadcast load.  N % 8 == 0 and col is even:
+// both columns are inside or outside C.
+__device__ __forceinline__ float2 bias_fetch2(const float* bias, int32_t N, int32_t col) {
+    if (bias == nullptr || col >= N) return make_float2(0.f, 0.f);
+    return __ldg(reinterpret_cast<const float2*>(bias + col));
+}
+__device__ __forceinline__ void st_shared_f2(uint32_t saddr, float2 v) {
+    asm volatile("st.shared.v2.f32 [%0], {%1, %2};" ::"r"(saddr), "f"(v.x), "f"(v.y) : "memory");
+}
+__device__ __forceinline__ float4 ld_shared_f4(uint32_t saddr) {
+    float4 v;
+    asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
+                 : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+                 : "r"(saddr)
+                 : "memory");
+    return v;
+}
+template <int ACT, int G>
+__device__ __forceinline__ void bias_act_staged(uint32_t* v, uint32_t b_addr) {
+#pragma unroll
+    for (int g = 0; g < G; ++g) {
+        const float4 b = ld_shared_f4(b_addr + static_cast<uint32_t>(g * 16));
+        v[g * 4 + 0] = __float_as_uint(act_fn<ACT>(__uint_as_float(v[g * 4 + 0]) + b.x));
+        v[g * 4 + 1] = __float_as_uint(act_fn<ACT>(__uint_as_float(v[g * 4 + 1]) + b.y));
+        v[g * 4 + 2] = __float_as_uint(act_fn<ACT>(__uint_as_float(v[g * 4 + 2]) + b.z));
+        v[g * 4 + 3] = __float_as_uint(act_fn<ACT>(__uint_as_float(v[g * 4 + 3]) + b.w));
+    }
+}
+// v: 4*G columns whose bias values start at shared address b_addr.
+template <int G>
+__device__ __forceinline__ void apply_bias_act_staged(uint32_t* v, const KParams& p, uint32_t b_addr) {
+    switch (p.act) {
+        case 1: bias_act_staged<1, G>(v, b_addr); break;
+        case 2: bias_act_staged<2, G>(v, b_addr); break;
+        case 3: bias_act_staged<3, G>(v, b_addr); break;
+        default: bias_act_staged<0, G>(v, b_addr); break;
+    }
+}
+
 // Store 32 fp32 values (as bits) of row `row`, columns [col, col+32) as fp16/bf16.
 template <int OUT>
 __device__ __forceinline__ void store_half_row32(void* C, int32_t N, int32_t row, int32_t col,
@@ -861,9 +904,13 @@ __device__ __forceinline__ KParams form_params(const KParams& in) {
         p.l2_prefetch = 0;
         p.a_mn_major = 0;
         p.b_mn_major = 0;
-        p.bias = nullptr;   // a call with a fused bias or activation launches the general form
-        p.act = 0;
-        if constexpr (FORM == kFormPlain) {
+        if constexpr (FORM != kFormEpilogue) {
+            // a call with a fused bias or activation launches the epilogue or the
+            // general form
+            p.bias = nullptr;
+            p.act = 0;
+        }
+        if constexpr (FORM == kFormPlain || FORM == kFormEpilogue) {
             p.split_k = 1;
             p.cluster_split = 0;
         } else {
@@ -945,11 +992,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     const UnitCoord c_first = unit_at(p, it.first);
     // Plain and cluster split forms: ring slots of the first unit that the copy
     // thread arms before the wait (shared memory only), so that right after it
-    // only their copies are issued.  (The general form arms each slot in its
-    // loop: the extra copy-issue code measured slower there, next to a fused
-    // epilogue.)
+    // only their copies are issued (kArmedCopy).
     int32_t n_armed = 0;
-    if constexpr (FORM != kFormGeneral) {
+    if constexpr (kArmedCopy<FORM>) {
         if (warp == 0 && lane == 0 && it.first < p.num_units) {
             const int32_t nslots = (c_first.kb_end - c_first.kb_begin + KS - 1) / KS;
             n_armed = nslots < STAGES ? nslots : STAGES;
@@ -985,7 +1030,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     if (warp == 0) {
         // ------------------------------------------------------------ producer
-        if constexpr (FORM != kFormGeneral) {
+        if constexpr (kArmedCopy<FORM>) {
             // (no multicast, no L2 prefetch distance, K-contiguous operands)
             if (lane == 0) {   // the thread that armed the first slots
                 const uint32_t slot_tx = kStageTx - (p.a_half ? KS * 8192u : 0u) + p.tx_extra;
@@ -1208,6 +1253,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t lane_addr = static_cast<uint32_t>(quad * 32) << 16;
         // This warp's two TMA-store buffers and which one is next.
         const uint32_t store_buf0 = staging + static_cast<uint32_t>((warp - 2) * 2 * L::kStoreBufBytes);
+        // This warp's slot for a chunk's fused bias (after the control block).
+        const uint32_t bias_slot = staging + static_cast<uint32_t>(L::kStagingBytes + L::kCtlBytes +
+                                                                   (warp - 2) * kBiasSlotBytes);
         uint32_t store_sel = 0;
         uint32_t acc_iter = 0;
         bool ok = true;
@@ -1287,6 +1335,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             } else {
                 const uint32_t buf = acc_iter & 1u;
                 const uint32_t acc_phase = (acc_iter >> 1) & 1u;
+                // A fused bias / activation in the TMA-store path: the bias is staged
+                // per chunk (bias_fetch2), the first chunk's fetched while the
+                // accumulator is being computed.
+                const bool epi = (p.bias != nullptr || p.act != 0) && !cluster && !split &&
+                                 !p.direct_store;
+                float2 b_next = make_float2(0.f, 0.f);
+                if (epi) b_next = bias_fetch2(p.bias, p.N, col0 + 2 * lane);
                 if (!wait_phase(smem_addr(&ctl->tmem_full[buf]), acc_phase, watch,
                                 kSiteEpiTmemFull)) {
                     ok = false;
@@ -1323,12 +1378,18 @@ __global__ void __launch_bounds__(kThreads, 1)
                         const uint32_t sbuf = store_buf0 + store_sel * L::kStoreBufBytes;
                         if (lane == 0) bulk_wait_group_read<1>();
                         __syncwarp();
+                        if (epi) {
+                            // (the warp's reads of the previous chunk's bias are done)
+                            st_shared_f2(bias_slot + static_cast<uint32_t>(lane * 8), b_next);
+                            __syncwarp();
+                            if (sc + 1 < BN / 64) b_next = bias_fetch2(p.bias, p.N, x + 64 + 2 * lane);
+                        }
 #pragma unroll
                         for (int h = 0; h < 2; ++h) {
                             uint32_t v[32];
                             tmem_ld_32x32b_x32(tmem_base + lane_addr + buf * BN + sc * 64 + h * 32, v);
                             tmem_ld_wait();
-                            apply_bias_act<8>(v, p, x + h * 32);
+                            if (epi) apply_bias_act_staged<8>(v, p, bias_slot + static_cast<uint32_t>(h * 128));
                             uint32_t w[16];
 #pragma unroll
                             for (int i = 0; i < 16; ++i)

@@ -52,7 +52,8 @@ struct SmemLayout2 {
     static constexpr int kStoreBufBytes = 32 * 128;
     static constexpr int kStagingBytes = kEpiWarps * 2 * kStoreBufBytes;
     static constexpr int kCtlBytes = 256;
-    static constexpr int kTotal = 1024 + kRingBytes + kStagingBytes + kCtlBytes;
+    static constexpr int kBiasBytes = kEpiWarps * kBiasSlotBytes;   // after the control block
+    static constexpr int kTotal = 1024 + kRingBytes + kStagingBytes + kCtlBytes + kBiasBytes;
     static_assert(kBTileBytes % 1024 == 0, "128B-swizzle tiles must stay 1024-byte aligned");
     static_assert(kTotal <= 232448, "exceeds the 227 KiB a CTA may use");
 };
@@ -202,13 +203,14 @@ __device__ __forceinline__ uint32_t ld_dsmem_u32(uint32_t cluster_addr) {
     return v;
 }
 
-// FORM: kFormGeneral or kFormPlain (see KernelForm; the host picks it).
+// FORM: kFormGeneral, kFormPlain or kFormEpilogue (see KernelForm; the host picks it).
 template <int BN, int STAGES, int OUT, int KS = 1, int FORM = kFormGeneral>
 __global__ void __launch_bounds__(64 + 32 * kPairEpiWarps<BN, OUT>, 1)
     gemm_tn_pair_kernel(const __grid_constant__ CUtensorMap tmap_a,
                         const __grid_constant__ CUtensorMap tmap_b,
                         const __grid_constant__ CUtensorMap tmap_c, const KParams p_in) {
-    static_assert(FORM == kFormGeneral || FORM == kFormPlain, "SM-pair kernel forms");
+    static_assert(FORM == kFormGeneral || FORM == kFormPlain || FORM == kFormEpilogue,
+                  "SM-pair kernel forms");
     const KParams p = form_params<FORM>(p_in);
     using L = SmemLayout2<BN, STAGES, KS>;
     static_assert(KS == 1 || KS == 2 || KS == 4, "k-blocks per ring slot");
@@ -294,11 +296,9 @@ __global__ void __launch_bounds__(64 + 32 * kPairEpiWarps<BN, OUT>, 1)
     const UnitCoord c_first = coord(pair);
     // Plain form: ring slots of the first unit that the leader's copy thread arms
     // before the wait (shared memory only), so that right after it both copy
-    // threads only issue their copies.  (The general form arms each slot in its
-    // loop: the extra copy-issue code measured slower there, next to a fused
-    // epilogue.)
+    // threads only issue their copies (kArmedCopy).
     int32_t n_armed = 0;
-    if constexpr (FORM != kFormGeneral) {
+    if constexpr (kArmedCopy<FORM>) {
         if (warp == 0 && lane == 0 && pair < p.num_units) {
             const int32_t nslots = (c_first.kb_end - c_first.kb_begin + KS - 1) / KS;
             n_armed = nslots < STAGES ? nslots : STAGES;
@@ -331,7 +331,7 @@ __global__ void __launch_bounds__(64 + 32 * kPairEpiWarps<BN, OUT>, 1)
 
     if (warp == 0) {
         // ------------------------------------------------------------ producer (both CTAs)
-        if constexpr (FORM != kFormGeneral) {
+        if constexpr (kArmedCopy<FORM>) {
             // (no multicast, no L2 prefetch distance, K-contiguous operands)
             if (lane == 0) {   // the thread that armed the first slots
                 auto issue = [&](int stage, int32_t kb, const UnitCoord& c) {
@@ -665,6 +665,15 @@ __global__ void __launch_bounds__(64 + 32 * kPairEpiWarps<BN, OUT>, 1)
             }
             const uint32_t buf = acc_iter & 1u;
             const uint32_t acc_phase = (acc_iter >> 1) & 1u;
+            // A fused bias / activation: the bias is staged per chunk in this warp's
+            // slot (see the one-SM kernel), the first chunk's fetched while the
+            // accumulator is being computed.
+            const bool epi = (p.bias != nullptr || p.act != 0) && !p.cluster_split;
+            const uint32_t bias_slot =
+                staging + static_cast<uint32_t>(L::kStagingBytes + L::kCtlBytes +
+                                                (warp - 2) * kBiasSlotBytes);
+            float2 b_next = make_float2(0.f, 0.f);
+            if (epi) b_next = bias_fetch2(p.bias, p.N, col0 + 2 * lane);
             if (!wait_phase(smem_addr(&ctl->tmem_full[buf]), acc_phase, watch, kSiteEpiTmemFull)) {
                 ok = false;
                 break;
@@ -679,12 +688,18 @@ __global__ void __launch_bounds__(64 + 32 * kPairEpiWarps<BN, OUT>, 1)
                 const uint32_t sbuf = store_buf0 + store_sel * L::kStoreBufBytes;
                 if (lane == 0) bulk_wait_group_read<1>();
                 __syncwarp();
+                if (epi) {
+                    // (the warp's reads of the previous chunk's bias are done)
+                    st_shared_f2(bias_slot + static_cast<uint32_t>(lane * 8), b_next);
+                    __syncwarp();
+                    if (sc + 1 < BN / 64) b_next = bias_fetch2(p.bias, p.N, x + 64 + 2 * lane);
+                }
 #pragma unroll
                 for (int h = 0; h < 2; ++h) {
                     uint32_t v[32];
                     tmem_ld_32x32b_x32(tmem_base + lane_addr + buf * BN + sc * 64 + h * 32, v);
                     tmem_ld_wait();
-                    apply_bias_act<8>(v, p, x + h * 32);
+                    if (epi) apply_bias_act_staged<8>(v, p, bias_slot + static_cast<uint32_t>(h * 128));
                     uint32_t w[16];
 #pragma unroll
                     for (int i = 0; i < 16; ++i)

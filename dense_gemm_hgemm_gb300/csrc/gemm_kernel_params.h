@@ -17,9 +17,20 @@ enum OutKind : int { kOutF16 = 0, kOutBF16 = 1, kOutI32 = 2 };
 // KParams.  Plain: one K slice, no multicast, TMA stores, K-contiguous operands,
 // no L2 prefetch distance, no fused bias or activation.  Cluster split (one-SM
 // kernel): as plain, but the K slices of a tile form one thread-block cluster
-// (split_k stays a run-time value).  The fixed fields become constants, so the
-// code of the other modes compiles out of the launch's critical path.
-enum KernelForm : int { kFormGeneral = 0, kFormPlain = 1, kFormClusterSplit = 2 };
+// (split_k stays a run-time value).  Epilogue: as plain, with the fused bias and
+// activation run-time values (what a plain plan launches for such a call).  The
+// fixed fields become constants, so the code of the other modes compiles out of
+// the launch's critical path.
+enum KernelForm : int { kFormGeneral = 0, kFormPlain = 1, kFormClusterSplit = 2, kFormEpilogue = 3 };
+
+// Forms whose copy thread arms the ring's first slots before the dependency
+// wait.  (The general and epilogue forms arm each slot in their loop: the extra
+// copy-issue code measured slower next to a fused epilogue.)
+template <int FORM>
+inline constexpr bool kArmedCopy = FORM == kFormPlain || FORM == kFormClusterSplit;
+
+// Shared memory per epilogue warp for the fused bias of one 64-column chunk.
+constexpr int kBiasSlotBytes = 64 * 4;
 
 // SM-pair integer tiles wider than 128 columns keep their int32 sums in registers
 // across eight epilogue warps (two per TMEM lane quarter, splitting the columns).

@@ -32,6 +32,12 @@ MODES = [
     ("pair_split2", (520, 136, 1024), {"block_n": 128, "cta_pair": 1, "split_k": 2,
                                        "split_mode": 1}),
     ("two_kblock_slots", (300, 264, 1088), {"block_n": 128, "kblocks_per_stage": 2}),
+    # plain plans launch the epilogue form for a fused call: 256-wide one-SM tiles,
+    # SM pairs of 128- and 224-wide tiles (the last 32 columns stored per thread),
+    # ragged N
+    ("one_sm_256", (260, 600, 512), {"block_n": 256}),
+    ("sm_pair_128", (520, 200, 640), {"block_n": 128, "cta_pair": 1}),
+    ("sm_pair_224", (600, 472, 512), {"block_n": 224, "cta_pair": 1}),
 ]
 
 
