@@ -998,8 +998,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (warp == 0 && lane == 0 && it.first < p.num_units) {
             const int32_t nslots = (c_first.kb_end - c_first.kb_begin + KS - 1) / KS;
             n_armed = nslots < STAGES ? nslots : STAGES;
-            for (int32_t s = 0; s < n_armed; ++s)
-                mbar_arrive_expect_tx(smem_addr(&ctl->full[s]), kStageTx - (p.a_half ? KS * 8192u : 0u) + p.tx_extra);
+            const uint32_t tx = kStageTx - (p.a_half ? KS * 8192u : 0u) + p.tx_extra;
+            for (int32_t s = 0; s < n_armed; ++s) mbar_arrive_expect_tx(smem_addr(&ctl->full[s]), tx);
         }
     }
     if (warp == 0 && lane == 0 && it.first < p.num_units) {
@@ -1389,7 +1389,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                             uint32_t v[32];
                             tmem_ld_32x32b_x32(tmem_base + lane_addr + buf * BN + sc * 64 + h * 32, v);
                             tmem_ld_wait();
-                            if (epi) apply_bias_act_staged<8>(v, p, bias_slot + static_cast<uint32_t>(h * 128));
+                            if (epi)
+                                apply_bias_act_staged<8>(v, p, bias_slot + static_cast<uint32_t>(h * 128));
                             uint32_t w[16];
 #pragma unroll
                             for (int i = 0; i < 16; ++i)
