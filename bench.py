@@ -827,9 +827,11 @@ def ours(args):
                        "d2h_busy_ms_per_step": round(busy_ms[1], 3),
                        "link_busy_frac": round(max(busy_ms) / e2e_ms, 4),
                        "note": "busy: the summed durations of the step's host-to-device and "
-                               "device-to-host copies, timed on their streams in the "
-                               "pipelined step; link_busy_frac = the busier direction / "
-                               "step time (near 1: the step is bound by the host link)"}
+                               "device-to-host copies, timed on their streams in three "
+                               "untimed steps run the same way (median); link_busy_frac = "
+                               "the busier direction / the timed step (two separate "
+                               "measurements: near 1, within a percent or so either way, "
+                               "means the step is bound by the host link)"}
         del graph
         for _, plan, *_ in items:
             plan.close()
