@@ -38,6 +38,7 @@ MODES = [
     ("one_sm_256", (260, 600, 512), {"block_n": 256}),
     ("sm_pair_128", (520, 200, 640), {"block_n": 128, "cta_pair": 1}),
     ("sm_pair_224", (600, 472, 512), {"block_n": 224, "cta_pair": 1}),
+    ("half_a", (64, 520, 512), {"block_n": 128}),   # M <= 64: the 64-row A box
 ]
 
 
@@ -91,6 +92,22 @@ def test_ffn_shape_gelu_sampled():
     C = pu.run_gpu_epilogue(A, B, w.dtype, None, bias, oracle.ACT_GELU)
     rows, cols = inputs.sample_positions(w.M, w.N, 4096, 11)
     _check(A, B, w.dtype, C, bias.numpy(), oracle.ACT_GELU, "ffn gelu", rows.numpy(), cols.numpy())
+
+
+@pytest.mark.parametrize("shape,cfg", [((2560, 1280, 512), {"block_n": 64}),
+                                       ((4096, 2048, 256), {"block_n": 256})],
+                         ids=["one_sm_64", "one_sm_256"])
+def test_multi_tile_epilogue_sampled(shape, cfg):
+    """One-SM CTAs that run several tiles each (the bias of a tile's first chunk is
+    fetched while the previous tile is still being stored), sampled."""
+    M, N, K = shape
+    A, B = inputs.make_operands(M, N, K, "f16")
+    bias = (torch.randn(N, generator=torch.Generator().manual_seed(3)) * 2).float()
+    for act in (oracle.ACT_GELU, oracle.ACT_SILU):
+        C = pu.run_gpu_epilogue(A, B, "f16", cfg, bias, act)
+        rows, cols = inputs.sample_positions(M, N, 4096, 5 + act)
+        _check(A, B, "f16", C, bias.numpy(), act, "multi-tile act=%d" % act, rows.numpy(),
+               cols.numpy())
 
 
 def test_rejects_bad_epilogue_arguments(gemm_lib):
