@@ -60,11 +60,13 @@ inline gemm_config_t model_config(int64_t M, int64_t N, int64_t K, gemm_dtype_t 
             c.block_n = bn;
         }
     }
-    // Many 256-row tiles: SM pairs (each SM streams half of B; measured ~15%
-    // faster than one-SM tiles on the large shapes of the sweep, and int8 4096^3
-    // 105 vs 123 us with 256-wide integer tiles).
-    if (mb >= 2 && ceil_div(M, 2 * kBM) * ceil_div(N, 256) >= sms) {
-        c.block_n = 256;
+    // SM pairs (each SM streams half of B) once there is enough work per pair tile:
+    // the measured table picks them exactly where (256 x 256 tiles) x K >= 2^17
+    // (32 tiles from K = 4096, 64 from 2048, 128 from 1024, 256 from 512), with
+    // 128-wide tiles while 256-wide ones would leave most pairs idle.
+    const int64_t pair_tiles = ceil_div(M, 2 * kBM) * ceil_div(N, 256);
+    if (mb >= 2 && pair_tiles * K >= (int64_t(1) << 17)) {
+        c.block_n = pair_tiles * 5 >= sms * 2 ? 256 : 128;
         c.cta_pair = 1;
         c.raster_group = 8;
         return c;

@@ -136,6 +136,22 @@ def test_select_config_big_shapes_fill_the_gpu(gemm_lib):
         assert tiles >= 152 and c["split_k"] == 1
 
 
+def test_cost_model_matches_the_tables_sm_pair_choice(gemm_lib):
+    """Off the table (M shifted by 8 rows, the same tile counts) the cost model
+    chooses SM pairs exactly where the measured table does."""
+    import json
+    from dense_gemm_hgemm_gb300 import tune
+    doc = json.load(open(tune.TUNED_JSON))
+    n = 0
+    for r in doc["shapes"]:
+        if r["dtype"] != "f16" or r["M"] < 256:
+            continue
+        c = gemm_lib.gemm_select_config(r["M"] - 8, r["N"], r["K"], "f16", 152)
+        assert c["cta_pair"] == r["best"]["cta_pair"], (r, c)
+        n += 1
+    assert n > 200
+
+
 def test_select_config_splits_k_for_few_tiles(gemm_lib):
     c = gemm_lib.gemm_select_config(128, 128, 4096, "f16", 152)
     assert c["split_k"] > 1

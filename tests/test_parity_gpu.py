@@ -147,6 +147,17 @@ def test_default_config_headline_shapes():
         pu.check_full(A, B, w.dtype, C, w.name)
 
 
+@pytest.mark.parametrize("shape,dtype", [((2104, 2104, 2104), "f16"), ((1000, 3000, 4160), "bf16"),
+                                         ((2112, 2104, 2112), "i8")])
+def test_cost_model_shapes_sampled(shape, dtype):
+    """Shapes outside the measured table run the cost model's configuration (here
+    SM pairs, 256- or 128-wide, with ragged edges), checked on sampled elements."""
+    M, N, K = shape
+    A, B = inputs.make_operands(M, N, K, dtype)
+    C = pu.run_gpu(A, B, dtype)
+    pu.check_sampled(A, B, dtype, C, where="cost model %s %s" % (shape, dtype))
+
+
 # --------------------------------------------------------------------------- int8 -> int32
 
 @pytest.mark.parametrize("bn", [64, 128])
