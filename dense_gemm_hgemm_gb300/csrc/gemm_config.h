@@ -72,12 +72,13 @@ inline gemm_config_t model_config(int64_t M, int64_t N, int64_t K, gemm_dtype_t 
         return c;
     }
     // Few output tiles and a long K: one SM streams only ~110 GB/s, so slice K
-    // over a cluster of 2/4/8 CTAs per tile (reduced in distributed shared memory).
+    // over a cluster of 2/4/8 CTAs per tile (reduced in distributed shared memory),
+    // at least four k-blocks per slice (the measured table splits from K = 1024).
     const int64_t tiles = mb * ceil_div(N, c.block_n);
-    if (tiles * 2 <= sms && num_kb >= 8) {
+    if (tiles * 2 <= sms && num_kb >= 16) {
         for (int s = 8; s >= 2; s /= 2) {
             const int64_t per = ceil_div(num_kb, s);
-            if (tiles * s <= sms && num_kb >= 2 * s && ceil_div(num_kb, per) == s) {
+            if (tiles * s <= sms && num_kb >= 4 * s && ceil_div(num_kb, per) == s) {
                 c.split_k = s;
                 c.split_mode = 1;
                 break;
