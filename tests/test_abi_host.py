@@ -152,6 +152,20 @@ def test_cost_model_matches_the_tables_sm_pair_choice(gemm_lib):
     assert n > 200
 
 
+def test_cost_model_configs_are_valid_off_the_table(gemm_lib):
+    """Seeded random shapes (mostly off the table): the chosen configuration is one
+    that plan validation accepts."""
+    import random
+    rnd = random.Random(11)
+    for _ in range(600):
+        dt = rnd.choice(("f16", "bf16", "i8"))
+        M = rnd.randint(1, 12000)
+        N = rnd.randint(1, 3000) * 4 if dt == "i8" else rnd.randint(1, 1500) * 8
+        K = rnd.randint(1, 800) * (16 if dt == "i8" else 8)
+        c = gemm_lib.gemm_select_config(M, N, K, dt, 152)
+        assert gemm_lib.gemm_workspace_bytes(M, N, K, dt, c) >= 0, (M, N, K, dt, c)
+
+
 def test_select_config_splits_k_for_few_tiles(gemm_lib):
     c = gemm_lib.gemm_select_config(128, 128, 4096, "f16", 152)
     assert c["split_k"] > 1
