@@ -158,6 +158,27 @@ def test_cost_model_shapes_sampled(shape, dtype):
     pu.check_sampled(A, B, dtype, C, where="cost model %s %s" % (shape, dtype))
 
 
+def _random_shapes(n, seed):
+    import random
+    rnd = random.Random(seed)
+    out = []
+    for _ in range(n):
+        dt = rnd.choice(("f16", "bf16", "i8"))
+        M = rnd.randint(1, 3000)
+        N = rnd.randint(1, 500) * 4 if dt == "i8" else rnd.randint(1, 300) * 8
+        K = rnd.randint(1, 200) * (16 if dt == "i8" else 8)
+        out.append((M, N, K, dt))
+    return out
+
+
+@pytest.mark.parametrize("M,N,K,dtype", _random_shapes(12, 5))
+def test_random_shapes_cost_model_sampled(M, N, K, dtype):
+    """Seeded random shapes with the configuration the library chooses, sampled."""
+    A, B = inputs.make_operands(M, N, K, dtype)
+    C = pu.run_gpu(A, B, dtype)
+    pu.check_sampled(A, B, dtype, C, count=2048, where="random %dx%dx%d %s" % (M, N, K, dtype))
+
+
 # --------------------------------------------------------------------------- int8 -> int32
 
 @pytest.mark.parametrize("bn", [64, 128])
